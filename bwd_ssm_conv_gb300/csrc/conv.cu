@@ -1,0 +1,225 @@
+// conv.cu -- causal depthwise conv1d (+bias, +SiLU): forward, backward, reductions.
+//
+// Forward (ggmlR test-ssm-rwkv.R, "ggml_ssm_conv matches a depthwise convolution computed
+// in R"):  out[b][t][d] = act(sum_k sx[b][d][t+k] c[d][k] + bias[d]).  sx is time-fastest,
+// out is channel-fastest, so every tile is transposed through shared memory: loads run
+// along time, stores along channels, both coalesced.
+//
+// Backward (lattice-inference gdn_backward.rs step 5, ggmlR ssm_conv_back):
+//   gp[t]      = dout[t] * silu'(pre[t])            (pre recomputed from sx)
+//   d_sx[i]    = sum_k gp[i-k] c[k]                 (0 <= i-k < L)
+//   d_c[d][k]  = sum_{b,t} gp[b][t][d] sx[b][d][t+k],   d_bias[d] = sum_{b,t} gp
+// d_c / d_bias are summed per tile into the workspace and reduced in a fixed order.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace ssm {
+
+constexpr int kConvTD = 32;   // channels per tile
+constexpr int kConvTT = 64;   // time columns per tile
+constexpr int kConvThreads = 256;
+
+__host__ __device__ inline int odd_up(int v) { return v | 1; }
+
+template <typename IO>
+__global__ void __launch_bounds__(kConvThreads)
+conv_fwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                const float* __restrict__ bias, IO* __restrict__ out, int D, int L, int K,
+                int silu) {
+  extern __shared__ float sm[];
+  const int R = kConvTT + K - 1, Rp = odd_up(R), Kp = odd_up(K);
+  float* s = sm;                        // [TD][Rp]   odd row stride: conflict-free column reads
+  float* w = sm + kConvTD * Rp;         // [TD][Kp]
+  const int d0 = blockIdx.x * kConvTD, t0 = blockIdx.y * kConvTT, b = blockIdx.z;
+  const long W = (long)L + K - 1;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kConvTD * R; i += kConvThreads) {
+    int r = i / R, col = i - r * R;
+    int d = d0 + r;
+    long t = (long)t0 + col;
+    s[r * Rp + col] = (d < D && t < W) ? ld(sx + ((long)b * D + d) * W + t) : 0.0f;
+  }
+  for (int i = tid; i < kConvTD * K; i += kConvThreads) {
+    int r = i / K, k = i - r * K;
+    int d = d0 + r;
+    w[r * Kp + k] = d < D ? __ldg(c + (long)d * K + k) : 0.0f;
+  }
+  __syncthreads();
+  const int tx = tid & 31, ty = tid >> 5;
+  const int d = d0 + tx;
+  if (d >= D) return;
+  const float bv = bias ? __ldg(bias + d) : 0.0f;
+  for (int tt = ty; tt < kConvTT; tt += kConvThreads / 32) {
+    int t = t0 + tt;
+    if (t >= L) break;
+    float acc = 0.0f;
+    for (int k = 0; k < K; k++) acc = fmaf(s[tx * Rp + tt + k], w[tx * Kp + k], acc);
+    acc += bv;
+    st(out + ((long)b * L + t) * D + d, silu ? siluf_(acc) : acc);
+  }
+}
+
+template <typename IO>
+__global__ void conv_state_kernel(const IO* __restrict__ sx, IO* __restrict__ st_out, int n_s,
+                                  int D, int L, int K) {
+  const long total = (long)n_s * D * (K - 1);
+  const long W = (long)L + K - 1;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    long row = i / (K - 1);
+    int k = (int)(i - row * (K - 1));
+    st(st_out + i, ld(sx + row * W + L + k));
+  }
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kConvThreads)
+conv_bwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                const float* __restrict__ bias, const IO* __restrict__ dout,
+                IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int K, int silu) {
+  extern __shared__ float sm[];
+  // The tile owns d_sx columns [i0, i0+TT) and, for the d_c partials, tokens [i0, i0+TT).
+  const int Rs = odd_up(kConvTT + 2 * K - 2);   // sx columns i0-K+1 .. i0+TT+K-2
+  const int Rg = odd_up(kConvTT + K - 1);       // gp tokens  i0-K+1 .. i0+TT-1
+  const int Kp = odd_up(K);
+  float* sxs = sm;                               // [TD][Rs]
+  float* gps = sxs + kConvTD * Rs;               // [TD][Rg]
+  float* w = gps + kConvTD * Rg;                 // [TD][Kp]
+  const int d0 = blockIdx.x * kConvTD, i0 = blockIdx.y * kConvTT, b = blockIdx.z;
+  const long W = (long)L + K - 1;
+  const int tid = threadIdx.x;
+  const int base = i0 - K + 1;                   // global column of local index 0
+  const int ns = kConvTT + 2 * K - 2, ng = kConvTT + K - 1;
+  for (int i = tid; i < kConvTD * ns; i += kConvThreads) {
+    int r = i / ns, j = i - r * ns;
+    int d = d0 + r;
+    long col = (long)base + j;
+    sxs[r * Rs + j] = (d < D && col >= 0 && col < W) ? ld(sx + ((long)b * D + d) * W + col) : 0.0f;
+  }
+  for (int i = tid; i < kConvTD * K; i += kConvThreads) {
+    int r = i / K, k = i - r * K;
+    int d = d0 + r;
+    w[r * Kp + k] = d < D ? __ldg(c + (long)d * K + k) : 0.0f;
+  }
+  for (int i = tid; i < kConvTD * ng; i += kConvThreads) {  // dout is channel-fastest
+    int tl = i / kConvTD, r = i - tl * kConvTD;
+    int d = d0 + r;
+    long t = (long)base + tl;
+    gps[r * Rg + tl] = (d < D && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+  }
+  __syncthreads();
+  if (silu) {  // gp = dout * silu'(pre), pre recomputed (same tap order as the forward)
+    for (int i = tid; i < kConvTD * ng; i += kConvThreads) {
+      int r = i / ng, tl = i - r * ng;
+      int d = d0 + r;
+      long t = (long)base + tl;
+      if (d >= D || t < 0 || t >= L) continue;
+      float pre = 0.0f;
+      for (int k = 0; k < K; k++) pre = fmaf(sxs[r * Rs + tl + k], w[r * Kp + k], pre);
+      if (bias) pre += __ldg(bias + d);
+      gps[r * Rg + tl] *= silu_gradf_(pre);
+    }
+    __syncthreads();
+  }
+  // d_sx columns [i0, i0+TT): warp lanes along time -> coalesced row stores
+  const int lane = tid & 31, wid = tid >> 5;
+  for (int r = wid; r < kConvTD; r += kConvThreads / 32) {
+    int d = d0 + r;
+    if (d >= D) continue;
+    for (int il = lane; il < kConvTT; il += 32) {
+      long i = (long)i0 + il;
+      if (i >= W) break;
+      float acc = 0.0f;
+      for (int k = 0; k < K; k++) acc = fmaf(gps[r * Rg + il + K - 1 - k], w[r * Kp + k], acc);
+      st(d_sx + ((long)b * D + d) * W + i, acc);
+    }
+  }
+  // partial d_c[d][k] (k < K) and d_bias[d] (k == K) over the tokens this tile owns
+  const int nt = gridDim.y;
+  for (int i = tid; i < kConvTD * (K + 1); i += kConvThreads) {
+    int r = i / (K + 1), k = i - r * (K + 1);
+    int d = d0 + r;
+    if (d >= D) continue;
+    float acc = 0.0f;
+    for (int tl = 0; tl < kConvTT; tl++) {
+      long t = (long)i0 + tl;
+      if (t >= L) break;
+      float g = gps[r * Rg + tl + K - 1];
+      acc = (k < K) ? fmaf(g, sxs[r * Rs + tl + K - 1 + k], acc) : acc + g;
+    }
+    part[(((long)b * nt + blockIdx.y) * D + d) * (K + 1) + k] = acc;
+  }
+}
+
+__global__ void conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ d_c,
+                                   float* __restrict__ d_bias, int n_s, int nt, int D, int K) {
+  const long total = (long)D * (K + 1);
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    int d = (int)(i / (K + 1)), k = (int)(i - (long)d * (K + 1));
+    float acc = 0.0f;
+    for (int b = 0; b < n_s; b++)
+      for (int j = 0; j < nt; j++) acc += part[(((long)b * nt + j) * D + d) * (K + 1) + k];
+    if (k < K) d_c[(long)d * K + k] = acc;
+    else if (d_bias) d_bias[d] = acc;
+  }
+}
+
+// ---- host launchers ----------------------------------------------------------------------
+size_t conv_bwd_ws_bytes(int n_s, int D, int L, int K) {
+  long W = (long)L + K - 1;
+  long nt = (W + kConvTT - 1) / kConvTT;
+  return align_up(sizeof(float) * (size_t)n_s * nt * D * (K + 1), 256);
+}
+
+template <typename IO>
+static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias, void* out,
+                              void* cs, int n_s, int D, int L, int K, int silu, cudaStream_t st) {
+  dim3 grid((D + kConvTD - 1) / kConvTD, (L + kConvTT - 1) / kConvTT, n_s);
+  size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
+  conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (IO*)out, D, L, K,
+                                                        silu);
+  if (cs && K > 1) {
+    long total = (long)n_s * D * (K - 1);
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    conv_state_kernel<IO><<<blocks, 256, 0, st>>>((const IO*)sx, (IO*)cs, n_s, D, L, K);
+  }
+  return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias, const void* dout,
+                              void* d_sx, float* d_c, float* d_bias, void* ws, int n_s, int D,
+                              int L, int K, int silu, cudaStream_t st) {
+  long W = (long)L + K - 1;
+  int nt = (int)((W + kConvTT - 1) / kConvTT);
+  dim3 grid((D + kConvTD - 1) / kConvTD, nt, n_s);
+  size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + 2 * K - 2) +
+                                 kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
+  float* part = (float*)ws;
+  conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (const IO*)dout,
+                                                        (IO*)d_sx, part, D, L, K, silu);
+  long total = (long)D * (K + 1);
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  conv_reduce_kernel<<<blocks, 256, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_fwd(const void* sx, const float* c, const float* bias, void* out, void* cs,
+                            int n_s, int D, int L, int K, int io, int silu, cudaStream_t st) {
+  return io == SSM_BF16 ? conv_fwd_t<__nv_bfloat16>(sx, c, bias, out, cs, n_s, D, L, K, silu, st)
+                        : conv_fwd_t<float>(sx, c, bias, out, cs, n_s, D, L, K, silu, st);
+}
+
+cudaError_t launch_conv_bwd(const void* sx, const float* c, const float* bias, const void* dout,
+                            void* d_sx, float* d_c, float* d_bias, void* ws, int n_s, int D, int L,
+                            int K, int io, int silu, cudaStream_t st) {
+  return io == SSM_BF16
+             ? conv_bwd_t<__nv_bfloat16>(sx, c, bias, dout, d_sx, d_c, d_bias, ws, n_s, D, L, K,
+                                         silu, st)
+             : conv_bwd_t<float>(sx, c, bias, dout, d_sx, d_c, d_bias, ws, n_s, D, L, K, silu, st);
+}
+
+}  // namespace ssm

@@ -1,0 +1,61 @@
+// kernels.cuh -- host-side launchers of the kernel files, called by the C ABI in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace ssm {
+
+// ---- conv ---------------------------------------------------------------------------------
+size_t conv_bwd_ws_bytes(int n_s, int D, int L, int K);
+cudaError_t launch_conv_fwd(const void* sx, const float* c, const float* bias, void* out, void* cs,
+                            int n_s, int D, int L, int K, int io, int silu, cudaStream_t st);
+cudaError_t launch_conv_bwd(const void* sx, const float* c, const float* bias, const void* dout,
+                            void* d_sx, float* d_c, float* d_bias, void* ws, int n_s, int D, int L,
+                            int K, int io, int silu, cudaStream_t st);
+
+// ---- scan ---------------------------------------------------------------------------------
+// Everything a scan launch needs, validated by the caller.  Pointers are device pointers.
+struct ScanProblem {
+  int ns, L, H, P, N, G, HP;
+  int a_per_state, softplus, check_finite;
+  int state_rows, chunk, n_chunks;
+  int io;
+  const float* s0;
+  const int* ids;
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  int* status;  // device status word
+};
+
+// Forward.  y may be NULL (states / checkpoints only), state_out may be NULL, ckpt may be NULL.
+size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms);
+cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
+                            int num_sms, cudaStream_t st);
+
+struct ScanGrads {
+  const void* dy;
+  const float* d_state_out;
+  float* d_s0;
+  void* d_x;
+  void* d_dt;
+  float* d_A;
+  void* d_B;
+  void* d_C;
+  float* d_D;
+  void* d_z;
+  float* d_dt_bias;
+};
+
+// Backward.  ckpt: checkpoints at interval p.chunk written by the forward, or NULL.
+size_t scan_bwd_ws_bytes(const ScanProblem& p, int num_sms);
+cudaError_t launch_scan_bwd(const ScanProblem& p, const float* ckpt, const ScanGrads& g, void* ws,
+                            int num_sms, cudaStream_t st);
+
+}  // namespace ssm

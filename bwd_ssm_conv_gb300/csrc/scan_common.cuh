@@ -1,0 +1,99 @@
+// scan_common.cuh -- layout decisions and small helpers shared by the scan kernels.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace ssm {
+
+constexpr int kScanThreads = 128;              // threads per scan block
+constexpr long kFwdTargetThreadsPerSM = 768;   // below this, time segments add parallelism
+constexpr long kBwdTargetThreadsPerSM = 768;
+constexpr int kMinSegment = 64;                // shortest time segment worth a block
+
+__host__ inline int pow2_ceil(int v) {
+  int r = 1;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+// States per thread (ns, a power of two in {4, 8, 16}) and threads per channel (tpc, a
+// power of two <= 32) so that ns * tpc >= N; states beyond N are padding and stay zero.
+__host__ inline void state_split(int N, int pref_ns, int* ns, int* tpc) {
+  int n = pow2_ceil(N);
+  if (n < 4) n = 4;
+  *ns = n < pref_ns ? n : pref_ns;
+  *tpc = pow2_ceil((N + *ns - 1) / *ns);
+}
+
+// Lanes of the tpc-lane group this lane belongs to (xor-shuffles stay inside it).
+__device__ __forceinline__ unsigned group_mask(int tpc) {
+  if (tpc >= 32) return 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  return ((1u << tpc) - 1u) << (lane & ~(tpc - 1));
+}
+
+// Row of s0 that sequence b starts from, or NULL for a zero state.  An id outside
+// [0, state_rows) is recorded in the status word and read as a zero state.
+__device__ __forceinline__ const float* start_row(const ScanProblem& p, int b) {
+  if (!p.s0) return nullptr;
+  int row = p.ids ? __ldg(p.ids + b) : b;
+  if (row < 0 || row >= p.state_rows) {
+    record_status(p.status, SSM_ERR_INVALID_ARG);
+    return nullptr;
+  }
+  return p.s0 + (long)row * p.HP * p.N;
+}
+
+// NS consecutive values of a B or C row.  FULL: all NS are in range and the address is
+// aligned to min(16, NS * sizeof(IO)) bytes, so vector loads are used.
+template <typename IO, int NS, bool FULL>
+__device__ __forceinline__ void load_row(const IO* ptr, int nvalid, float (&out)[NS]) {
+  if (FULL) {
+    if (sizeof(IO) == 4) {
+#pragma unroll
+      for (int j = 0; j < NS; j += 4) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(ptr + j));
+        out[j] = v.x; out[j + 1] = v.y; out[j + 2] = v.z; out[j + 3] = v.w;
+      }
+    } else if (NS >= 8) {
+#pragma unroll
+      for (int j = 0; j < NS; j += 8) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(ptr + j));
+        const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          float2 f = __bfloat1622float2(q[k]);
+          out[j + 2 * k] = f.x;
+          out[j + 2 * k + 1] = f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NS; j += 4) {
+        uint2 v = __ldg(reinterpret_cast<const uint2*>(ptr + j));
+        const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+          float2 f = __bfloat1622float2(q[k]);
+          out[j + 2 * k] = f.x;
+          out[j + 2 * k + 1] = f.y;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NS; j++) out[j] = (j < nvalid) ? ld(ptr + j) : 0.0f;
+  }
+}
+
+__host__ inline bool rows_vectorizable(const ScanProblem& p, int ns, int tpc) {
+  if (p.N != ns * tpc) return false;
+  const size_t sz = p.io == SSM_BF16 ? 2 : 4;
+  const size_t vb = ns * sz < 16 ? ns * sz : 16;
+  if ((p.N * sz) % vb != 0) return false;
+  if (((uintptr_t)p.B % 16) != 0 || ((uintptr_t)p.C % 16) != 0) return false;
+  return true;
+}
+
+}  // namespace ssm

@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library builds and loads, exports exactly the functions
+include/ssm.h declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_ssm_conv_gb300 import binding
+from bwd_ssm_conv_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 1 << 20  # a non-null, 256-byte-aligned pointer value: never dereferenced by these tests
+
+
+def _declared():
+    names = set()
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ssm_\w+)\s*\(", text,
+                                    re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return binding.lib()
+
+
+def test_library_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert declared >= set(binding.EXPORTED)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_abi_version_and_status_strings(L):
+    assert binding.ssm_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert binding.ssm_status_string(code)
+    assert binding.ssm_status_string(-99) == "unknown status"
+
+
+def _desc(**kw):
+    base = dict(n_seqs=2, n_tok=8, n_head=4, head_dim=1, d_state=16, n_group=1, a_per_state=1,
+                state_rows=0, chunk=0, io=0, flags=0)
+    base.update(kw)
+    return binding.ScanDesc(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_seqs=0), binding.SSM_ERR_INVALID_ARG),
+    (dict(n_tok=-1), binding.SSM_ERR_INVALID_ARG),
+    (dict(n_group=3), binding.SSM_ERR_INVALID_ARG),          # H % G != 0
+    (dict(io=7), binding.SSM_ERR_INVALID_ARG),
+    (dict(flags=64), binding.SSM_ERR_INVALID_ARG),
+    (dict(a_per_state=2), binding.SSM_ERR_INVALID_ARG),
+    (dict(d_state=513), binding.SSM_ERR_UNSUPPORTED),
+    (dict(n_tok=1 << 20, n_head=1 << 12), binding.SSM_ERR_UNSUPPORTED),
+])
+def test_scan_fwd_rejects_bad_descriptors(L, kw, code):
+    d = _desc(**kw)
+    args = [ctypes.byref(d), None, None] + [FAKE] * 5 + [None] * 3 + [FAKE, FAKE, None, FAKE,
+                                                                       1 << 30, None]
+    assert L.ssm_scan_fwd(*args) == code
+    assert L.ssm_scan_workspace_size(ctypes.byref(d), 0) == 0
+
+
+def test_scan_fwd_rejects_null_and_misaligned(L):
+    d = _desc()
+    good = [ctypes.byref(d), None, None] + [FAKE] * 5 + [None] * 3 + [FAKE, FAKE, None, FAKE,
+                                                                       1 << 30, None]
+    for i in (3, 4, 5, 6, 7, 11, 12):  # x, dt, A, B, C, y, state_out
+        args = list(good)
+        args[i] = None
+        assert L.ssm_scan_fwd(*args) == binding.SSM_ERR_INVALID_ARG, i
+    args = list(good)
+    args[3] = FAKE + 2  # x misaligned for fp32
+    assert L.ssm_scan_fwd(*args) == binding.SSM_ERR_INVALID_ARG
+    # s0 without ids needs state_rows >= n_seqs
+    d2 = _desc(state_rows=1)
+    args = list(good)
+    args[0] = ctypes.byref(d2)
+    args[1] = FAKE
+    assert L.ssm_scan_fwd(*args) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_scan_bwd_rejects_bad_arguments(L):
+    d = _desc()
+    base = ([ctypes.byref(d), None, None] + [FAKE] * 5 + [None, None, None, None, FAKE, None,
+                                                          None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                          None, None, None, FAKE, 1 << 30, None])
+    assert len(base) == 26
+    # d_state beyond the backward limit
+    d_big = _desc(d_state=256)
+    args = list(base)
+    args[0] = ctypes.byref(d_big)
+    assert L.ssm_scan_bwd(*args) == binding.SSM_ERR_UNSUPPORTED
+    # d_D without D, d_z without z, d_dt_bias without softplus
+    for i in (20, 21, 22):
+        args = list(base)
+        args[i] = FAKE
+        assert L.ssm_scan_bwd(*args) == binding.SSM_ERR_INVALID_ARG, i
+    # required outputs
+    for i in (12, 15, 16, 17, 18, 19):
+        args = list(base)
+        args[i] = None
+        assert L.ssm_scan_bwd(*args) == binding.SSM_ERR_INVALID_ARG, i
+
+
+def test_conv_rejects_bad_arguments(L):
+    S = binding.SSM_CONV_SILU
+    assert L.ssm_conv_fwd(None, FAKE, None, FAKE, None, 1, 4, 8, 4, 0, S, None) == -1
+    assert L.ssm_conv_fwd(FAKE, FAKE, None, FAKE, None, 1, 0, 8, 4, 0, S, None) == -1
+    assert L.ssm_conv_fwd(FAKE, FAKE, None, FAKE, None, 1, 4, 8, 65, 0, S, None) == -2
+    assert L.ssm_conv_fwd(FAKE, FAKE, None, FAKE, None, 1, 4, 8, 4, 0, 8, None) == -1
+    assert L.ssm_conv_fwd(FAKE + 2, FAKE, None, FAKE, None, 1, 4, 8, 4, 0, S, None) == -1
+    assert L.ssm_conv_workspace_size(1, 4, 8, 4) > 0
+    assert L.ssm_conv_workspace_size(1, 4, 8, 0) == 0
+    # workspace missing / too small
+    assert L.ssm_conv_bwd(FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, 0, 1, 4, 8, 4, 0, S,
+                          None) == -3
+    assert L.ssm_conv_bwd(FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, 16, 1, 4, 8, 4, 0, S,
+                          None) == -3
+
+
+def test_status_rejects_null(L):
+    v = ctypes.c_int(0)
+    assert L.ssm_scan_status(None, ctypes.byref(v), None) == -1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()
