@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the selective-scan hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+    causal conv1d+SiLU forward -> selective scan forward (with per-chunk checkpoints)
+    -> selective scan backward (recompute from checkpoints) -> conv1d backward.
+Metric: tokens/s (sequences x tokens per second) of that fwd+bwd step, and the achieved HBM
+bandwidth of the scan kernels.  Default workload: the training-shaped Mamba-1 layer
+(16 x 2048 tokens, d_inner 1536, d_state 16, d_conv 4, bf16 I/O, fp32 state, z gate and D
+skip, checkpoints every 256 tokens).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl reference]
+With N > 1 it is launched by torch.distributed.run, one process per GPU; each GPU runs an
+independent replica (the path has no cross-GPU exchange), value = all tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from bwd_ssm_conv_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "selective-scan fwd+bwd tokens/s (B·L/s) and achieved HBM GB/s vs 8 TB/s"
+DEFAULT_CONFIG = 4
+SPEC_HBM_GBS = 8000.0
+
+
+# ---- algorithmic bytes per token (what each stage must move at minimum) -------------------
+def alg_bytes(w) -> dict:
+    """Bytes per token each stage must read and write at minimum (activations in the I/O
+    dtype, checkpoints fp32 every `chunk` tokens; parameters and states are negligible)."""
+    io, D, H, N, G = w.io_bytes, w.channels, w.n_head, w.d_state, w.n_group
+    zc = D if w.has_z else 0
+    ck = 4.0 * D * N / w.chunk
+    bc = 2 * G * N * io
+    scan_fwd = (D + H + zc + D) * io + bc + ck                        # x, dt, z in; y out
+    scan_bwd = (D + H + zc + D) * io + bc + ck + (D + H + zc) * io + bc  # + dy in; dx dt dz dB dC
+    conv_fwd = 2 * D * io if w.d_conv else 0
+    conv_bwd = 3 * D * io if w.d_conv else 0
+    return {"conv_fwd": conv_fwd, "scan_fwd": scan_fwd, "scan_bwd": scan_bwd,
+            "conv_bwd": conv_bwd}
+
+
+def _measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---- clocks during the timed region ------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sel = [r for t, r in self.rows if t0 <= t <= t1] or [r for _, r in self.rows]
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in sel:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the step ----------------------------------------------------------------------------
+class Step:
+    """Device buffers for one step of the hot path and the calls that run it."""
+
+    def __init__(self, w, dev, inp):
+        from bwd_ssm_conv_gb300 import binding as B
+        self.B = B
+        self.w = w
+        self.dev = dev
+        d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+        self.d = d
+        ns, L, H, P, N = w.n_seqs, w.n_tok, w.n_head, w.head_dim, w.d_state
+        io = w.torch_io
+        f32 = torch.float32
+        self.x = (torch.empty(ns, L, H * P, dtype=io, device=dev) if w.d_conv
+                  else d["x"].view(ns, L, H * P))
+        self.x4 = self.x.view(ns, L, H, P)
+        self.y = torch.empty(ns, L, H, P, dtype=io, device=dev)
+        self.st = torch.empty(ns, H, P, N, dtype=f32, device=dev)
+        nch = (L + w.chunk - 1) // w.chunk
+        self.ck = torch.empty(ns, nch, H, P, N, dtype=f32, device=dev)
+        shape = B.scan_shape(self.x4, d["dt"], d["A"], d["B"], d["s0"], w.chunk)
+        self.ws_f = torch.empty(B.ssm_scan_workspace_size(shape, False), dtype=torch.uint8,
+                                device=dev)
+        self.ws_b = torch.empty(B.ssm_scan_workspace_size(shape, True), dtype=torch.uint8,
+                                device=dev)
+        self.g = dict(d_s0=torch.empty(ns, H, P, N, dtype=f32, device=dev),
+                      d_x=torch.empty_like(self.x4), d_dt=torch.empty_like(d["dt"]),
+                      d_A=torch.empty_like(d["A"]), d_B=torch.empty_like(d["B"]),
+                      d_C=torch.empty_like(d["C"]),
+                      d_D=torch.empty_like(d["D"]) if d["D"] is not None else None,
+                      d_z=torch.empty_like(d["z"]) if d["z"] is not None else None,
+                      d_dt_bias=None)
+        if w.d_conv:
+            self.ws_c = torch.empty(B.ssm_conv_workspace_size(ns, H * P, L, w.d_conv),
+                                    dtype=torch.uint8, device=dev)
+            self.d_sx = torch.empty_like(d["sx"])
+            self.d_c = torch.empty_like(d["c"])
+
+    def stages(self):
+        B, w, d = self.B, self.w, self.d
+        out = []
+        if w.d_conv:
+            out.append(("conv_fwd", lambda: B.ssm_conv_fwd(d["sx"], d["c"], None, silu=True,
+                                                           out=self.x)))
+        out.append(("scan_fwd", lambda: B.ssm_scan_fwd(
+            self.x4, d["dt"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"], s0=d["s0"],
+            chunk=w.chunk, ws=self.ws_f, out=(self.y, self.st, self.ck))))
+        if not w.fwd_only:
+            out.append(("scan_bwd", lambda: B.ssm_scan_bwd(
+                self.x4, d["dt"], d["A"], d["B"], d["C"], d["dy"], D=d["D"], z=d["z"],
+                s0=d["s0"], ckpt=self.ck, d_state_out=d["d_state_out"], chunk=w.chunk,
+                ws=self.ws_b, out=self.g)))
+            if w.d_conv:
+                out.append(("conv_bwd", lambda: B.ssm_conv_bwd(
+                    d["sx"], d["c"], self.g["d_x"].view(w.n_seqs, w.n_tok, w.channels), None,
+                    silu=True, ws=self.ws_c, out=(self.d_sx, self.d_c, None))))
+        return out
+
+    def outputs(self):
+        """The step's results a caller reads back (for the end-to-end leg)."""
+        if self.w.fwd_only:
+            return [self.y, self.st]
+        res = [self.y, self.st, self.g["d_x"] if not self.w.d_conv else self.d_sx,
+               self.g["d_dt"], self.g["d_A"], self.g["d_B"], self.g["d_C"]]
+        for k in ("d_D", "d_z"):
+            if self.g[k] is not None:
+                res.append(self.g[k])
+        if self.w.d_conv:
+            res.append(self.d_c)
+        return res
+
+    def inputs(self):
+        d = self.d
+        keys = ["sx", "c"] if self.w.d_conv else ["x"]
+        keys += ["dt", "A", "B", "C", "D", "z", "s0", "dy", "d_state_out"]
+        return [d[k] for k in keys if d.get(k) is not None]
+
+
+def l2_flush_buffer(dev):
+    props = torch.cuda.get_device_properties(dev)
+    return torch.empty(2 * props.L2_cache_size // 4 + 1, dtype=torch.float32, device=dev)
+
+
+def time_device(step, steps, warmup, flush):
+    """Per-step CUDA-event times (ms) of the whole step and of each stage, on the stream the
+    kernels are launched on; L2 flushed before every step (outside the timed events)."""
+    stream = torch.cuda.current_stream()
+    stages = step.stages()
+    for _ in range(warmup):
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(steps)]
+    from bwd_ssm_conv_gb300 import binding as B
+    launches0 = B.ssm_kernel_launches()
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            evs[i][j + 1].record(stream)
+    launches = B.ssm_kernel_launches() - launches0
+    torch.cuda.synchronize()
+    total = [e[0].elapsed_time(e[-1]) for e in evs]
+    per_stage = {name: [e[j].elapsed_time(e[j + 1]) for e in evs]
+                 for j, (name, _) in enumerate(stages)}
+    return total, per_stage, launches
+
+
+def time_e2e(step, steps, warmup):
+    """Same step through the public API with host buffers: every step copies its inputs from
+    pinned host memory and reads its results back."""
+    host_in = [t.detach().cpu().pin_memory() for t in step.inputs()]
+    dev_in = step.inputs()
+    outs = step.outputs()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    stages = step.stages()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        for _, fn in stages:
+            fn()
+        for d, h in zip(outs, host_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ---- the oracle on the host (CPU baseline and the reference arm) ---------------------------
+def oracle_sample(w, channels, seqs=1, seed=None):
+    """Runs the oracle's whole step on `seqs` sequences x all tokens x `channels` channels of
+    the workload; returns (seconds, channel-tokens processed)."""
+    import oracle
+    inp = make_inputs(w.with_(n_seqs=seqs, n_head=channels), seed=seed)
+    t0 = time.perf_counter()
+    dims = oracle.ScanDims(seqs, w.n_tok, channels, w.head_dim, w.d_state, n_group=w.n_group,
+                           a_per_state=0 if w.scalar_a else 1, chunk=w.chunk)
+    if w.d_conv:
+        x = oracle.conv_fwd(inp["sx"], inp["c"], None, silu=True)
+        x = x.reshape(seqs, w.n_tok, channels, w.head_dim)
+    else:
+        x = inp["x"]
+    _, _, ck = oracle.scan_fwd(dims, x=x, dt=inp["dt"], A=inp["A"], B=inp["B"], C=inp["C"],
+                               D=inp["D"], z=inp["z"], s0=inp["s0"])
+    if not w.fwd_only:
+        g = oracle.scan_bwd(dims, x=x, dt=inp["dt"], A=inp["A"], B=inp["B"], C=inp["C"],
+                            dy=inp["dy"], D=inp["D"], z=inp["z"], ckpt=ck)
+        if w.d_conv:
+            oracle.conv_bwd(inp["sx"], inp["c"], g["d_x"].reshape(seqs, w.n_tok, channels),
+                            silu=True)
+    return time.perf_counter() - t0, seqs * w.n_tok * channels
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """Oracle tokens/s at the workload's full width, from a bounded channel sample."""
+    t, ct = oracle_sample(w, channels=4 * w.head_dim if w.head_dim > 1 else 4)
+    per_ct = t / ct
+    ch = max(1, min(w.n_head, int(budget_s / (per_ct * w.n_tok))))
+    t, ct = oracle_sample(w, channels=ch)
+    per_ct = t / ct
+    tokens_per_s = 1.0 / (per_ct * w.n_head)  # full width: every channel of every token
+    return {"value": tokens_per_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 sequence x {w.n_tok} tokens x {ch} of {w.n_head} channels of the same "
+                      f"workload, full step (conv fwd, scan fwd, scan bwd, conv bwd), "
+                      f"{t:.1f} s single-threaded f64; scaled to all channels"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    # size each step so that warmup + steps finish in about two minutes
+    t, ct = oracle_sample(w, channels=2)
+    per_ct = t / ct
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    ch = max(1, min(w.n_head, int(budget / (per_ct * w.n_tok))))
+    for _ in range(args.warmup):
+        oracle_sample(w, channels=ch)
+    times = [oracle_sample(w, channels=ch)[0] for _ in range(args.steps)]
+    t_mean = sum(times) / len(times)
+    value = (ch * w.n_tok / t_mean) / w.n_head
+    sample = (f"each step: 1 sequence x {w.n_tok} tokens x {ch} of {w.n_head} channels, full "
+              f"step, single-threaded f64 oracle; tokens/s scaled to all channels")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * w.n_seqs * w.n_tok / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n_seqs": w.n_seqs, "seq_len": w.n_tok,
+                       "d_inner": w.channels, "d_state": w.d_state, "chunk": w.chunk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bwd_ssm_conv_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if dist is not None:
+        dist.barrier()
+
+    inp = make_inputs(w, grad_seed_state=False)
+    step = Step(w, dev, inp)
+    flush = l2_flush_buffer(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    total, per_stage, launches = time_device(step, args.steps, args.warmup, flush)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    ms = sum(total) / len(total)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+
+    e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 20)), 2)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    tokens = w.n_seqs * w.n_tok
+    value = world * tokens / (ms * 1e-3)
+    peaks, peak_src = _measured_peaks()
+    ab = alg_bytes(w)
+    stage_ms = {k: sum(v) / len(v) for k, v in per_stage.items()}
+    dom = max(stage_ms, key=stage_ms.get)
+    dom_bytes = ab[dom] * tokens
+    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
+    stage_gbs = {k: ab[k] * tokens / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.io == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "n_seqs": w.n_seqs, "seq_len": w.n_tok,
+                   "d_inner": w.channels, "head_dim": w.head_dim, "d_state": w.d_state,
+                   "d_conv": w.d_conv, "chunk": w.chunk, "state_dtype": "f32",
+                   "parallelism": f"replicas{world}", "l2": "flushed before every step"},
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stage_hbm_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
+        "stage_frac_of_8tbs": {k: round(v / SPEC_HBM_GBS, 4) for k, v in stage_gbs.items()},
+        "roofline": {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src,
+                     "traffic": None, "algorithmic_bytes_per_launch": dom_bytes},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

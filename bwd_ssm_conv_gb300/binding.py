@@ -23,7 +23,7 @@ SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE = 1, 2, 4
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
             "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_status", "ssm_status_string",
-            "ssm_abi_version")
+            "ssm_abi_version", "ssm_kernel_launches")
 
 
 class SsmError(RuntimeError):
@@ -65,6 +65,7 @@ def lib():
         L.ssm_status_string.argtypes = [_i]
         L.ssm_status_string.restype = ctypes.c_char_p
         L.ssm_abi_version.restype = _i
+        L.ssm_kernel_launches.restype = ctypes.c_ulonglong
         _lib = L
     return _lib
 
@@ -275,6 +276,10 @@ def ssm_status_string(code: int) -> str:
 
 def ssm_abi_version() -> int:
     return int(lib().ssm_abi_version())
+
+
+def ssm_kernel_launches() -> int:
+    return int(lib().ssm_kernel_launches())
 
 
 # ---- ggml packing (ggmlR test-ssm-rwkv.R) --------------------------------------------------

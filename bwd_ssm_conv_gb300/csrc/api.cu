@@ -8,6 +8,13 @@
 #include "kernels.cuh"
 #include "ssm.h"
 
+#include <atomic>
+
+namespace ssm {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace ssm
+
 namespace {
 
 using ssm::ScanGrads;
@@ -82,6 +89,10 @@ int check_act(const void* ptr, int io) { return aligned(ptr, io_size(io)); }
 extern "C" {
 
 int ssm_abi_version(void) { return SSM_ABI_VERSION; }
+
+unsigned long long ssm_kernel_launches(void) {
+  return ssm::g_launches.load(std::memory_order_relaxed);
+}
 
 const char* ssm_status_string(int s) {
   switch (s) {

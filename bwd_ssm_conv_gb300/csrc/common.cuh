@@ -50,6 +50,9 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 }
 
 constexpr size_t kStatusBytes = 256;
+
+// Number of kernels this library has enqueued in the process (ssm_kernel_launches).
+void count_launches(int n);
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace ssm

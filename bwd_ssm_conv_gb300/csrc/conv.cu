@@ -178,12 +178,12 @@ static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias,
   dim3 grid((D + kConvTD - 1) / kConvTD, (L + kConvTT - 1) / kConvTT, n_s);
   size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
   conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (IO*)out, D, L, K,
-                                                        silu);
+                                                        silu), count_launches(1);
   if (cs && K > 1) {
     long total = (long)n_s * D * (K - 1);
     int blocks = (int)((total + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    conv_state_kernel<IO><<<blocks, 256, 0, st>>>((const IO*)sx, (IO*)cs, n_s, D, L, K);
+    conv_state_kernel<IO><<<blocks, 256, 0, st>>>((const IO*)sx, (IO*)cs, n_s, D, L, K), count_launches(1);
   }
   return cudaGetLastError();
 }
@@ -199,11 +199,11 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
                                  kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
   float* part = (float*)ws;
   conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (const IO*)dout,
-                                                        (IO*)d_sx, part, D, L, K, silu);
+                                                        (IO*)d_sx, part, D, L, K, silu), count_launches(1);
   long total = (long)D * (K + 1);
   int blocks = (int)((total + 255) / 256);
   if (blocks > 4096) blocks = 4096;
-  conv_reduce_kernel<<<blocks, 256, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K);
+  conv_reduce_kernel<<<blocks, 256, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K), count_launches(1);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,7 @@ __device__ __forceinline__ float delta_of(const ScanProblem& p, const IO* dt, lo
 template <typename IO, bool SCALAR_A, bool FULL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_bwd_kernel(const BwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;  // accurate decay form for fp32 I/O
   extern __shared__ float4 smem4[];
   const ScanProblem& p = a.p;
   const Lane l = lane_of(a);
@@ -155,10 +156,10 @@ scan_bwd_kernel(const BwdArgs a) {
         float Bv[kBwdNS];
         load_row<IO, kBwdNS, FULL>(Bm + tok * p.G * N + gbase, N - l.n0, Bv);
         const float dx = dl * xv;
-        const float as = SCALAR_A ? ex2(dl * A2[0]) : 0.0f;
+        const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
 #pragma unroll
         for (int j = 0; j < kBwdNS; j++)
-          hs[j] = fmaf(SCALAR_A ? as : ex2(dl * A2[j]), hs[j], dx * Bv[j]);
+          hs[j] = decay_step<ACC>(SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
       }
     }
     // ---- level 2: per sub-chunk, last to first --------------------------------------------
@@ -180,16 +181,16 @@ scan_bwd_kernel(const BwdArgs a) {
           float Bv[kBwdNS];
           load_row<IO, kBwdNS, FULL>(Bm + tok * p.G * N + gbase, N - l.n0, Bv);
           const float dx = dl * xv;
-          const float as = SCALAR_A ? ex2(dl * A2[0]) : 0.0f;
+          const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
 #pragma unroll
           for (int j = 0; j < kBwdNS; j++) {
-            aa[i][j] = SCALAR_A ? as : ex2(dl * A2[j]);
-            hh[i + 1][j] = fmaf(aa[i][j], hh[i][j], dx * Bv[j]);
+            aa[i][j] = SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]);
+            hh[i + 1][j] = decay_step<ACC>(aa[i][j], hh[i][j], dx * Bv[j]);
           }
           dls[i] = dl; xs[i] = xv; pres[i] = pre;
         } else {
 #pragma unroll
-          for (int j = 0; j < kBwdNS; j++) { aa[i][j] = 1.0f; hh[i + 1][j] = hh[i][j]; }
+          for (int j = 0; j < kBwdNS; j++) { aa[i][j] = ACC ? 0.0f : 1.0f; hh[i + 1][j] = hh[i][j]; }
           dls[i] = 0.0f; xs[i] = 0.0f; pres[i] = 0.0f;
         }
       }
@@ -220,7 +221,7 @@ scan_bwd_kernel(const BwdArgs a) {
             dCp[j] = gy * hh[i + 1][j];
             sB = fmaf(dh, Bv[j], sB);
             dBp[j] = dh * dlx;
-            const float cn = aa[i][j] * dh;
+            const float cn = decay_apply<ACC>(aa[i][j], dh);
             const float w = cn * hh[i][j];
             sAw = fmaf(An[j], w, sAw);
             dA_acc[j] = fmaf(dls[i], w, dA_acc[j]);
@@ -291,6 +292,7 @@ scan_bwd_kernel(const BwdArgs a) {
 template <typename IO, bool SCALAR_A, bool FULL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_bwd_local_kernel(const BwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;
   const ScanProblem& p = a.p;
   const Lane l = lane_of(a);
   const int N = p.N;
@@ -322,10 +324,10 @@ scan_bwd_local_kernel(const BwdArgs a) {
     load_row<IO, kBwdNS, FULL>(Cm + tok * p.G * N + gbase, N - l.n0, Cv);
     float gy = l.valid ? ld(dy + tok * p.HP + l.ch) : 0.0f;
     if (z) gy *= siluf_(l.valid ? ld(z + tok * p.HP + l.ch) : 0.0f);
-    const float as = SCALAR_A ? ex2(dl * A2[0]) : 0.0f;
+    const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
 #pragma unroll
     for (int j = 0; j < kBwdNS; j++)
-      c[j] = (SCALAR_A ? as : ex2(dl * A2[j])) * fmaf(gy, Cv[j], c[j]);
+      c[j] = decay_apply<ACC>(SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]), fmaf(gy, Cv[j], c[j]));
     sumd += dl;
   }
   if (l.valid) {
@@ -530,8 +532,8 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, size_t smem, cudaStream_t st) 
   const ScanProblem& p = a.p;
   if (a.S > 1) {
     dim3 g1(p.G * a.bpg, a.S - 1, p.ns);
-    scan_bwd_local_kernel<IO, SCALAR_A, FULL><<<g1, kScanThreads, 0, st>>>(a);
-    scan_bwd_carry_kernel<<<blocks_for((long)p.ns * p.HP * p.N), 256, 0, st>>>(a);
+    scan_bwd_local_kernel<IO, SCALAR_A, FULL><<<g1, kScanThreads, 0, st>>>(a), count_launches(1);
+    scan_bwd_carry_kernel<<<blocks_for((long)p.ns * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
   }
   auto kern = scan_bwd_kernel<IO, SCALAR_A, FULL>;
   if (smem > 48 * 1024) {
@@ -540,16 +542,16 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, size_t smem, cudaStream_t st) 
     if (e != cudaSuccess) return e;
   }
   dim3 g2(p.G * a.bpg, a.S, p.ns);
-  kern<<<g2, kScanThreads, smem, st>>>(a);
-  reduce_bc_kernel<IO><<<blocks_for((long)p.ns * p.L * p.G * 2 * p.N), 256, 0, st>>>(a);
+  kern<<<g2, kScanThreads, smem, st>>>(a), count_launches(1);
+  reduce_bc_kernel<IO><<<blocks_for((long)p.ns * p.L * p.G * 2 * p.N), 256, 0, st>>>(a), count_launches(1);
   const long nparams = (long)(p.a_per_state ? p.H * p.N : p.H) + p.HP + p.H;
-  reduce_params_kernel<<<blocks_for(nparams), 256, 0, st>>>(a);
+  reduce_params_kernel<<<blocks_for(nparams), 256, 0, st>>>(a), count_launches(1);
   if (p.P > 1) {
-    reduce_ddt_kernel<IO><<<blocks_for((long)p.ns * p.L * p.H), 256, 0, st>>>(a);
-    if (p.softplus && a.g.d_dt_bias) reduce_dtb_kernel<IO><<<blocks_for(p.H), 256, 0, st>>>(a);
+    reduce_ddt_kernel<IO><<<blocks_for((long)p.ns * p.L * p.H), 256, 0, st>>>(a), count_launches(1);
+    if (p.softplus && a.g.d_dt_bias) reduce_dtb_kernel<IO><<<blocks_for(p.H), 256, 0, st>>>(a), count_launches(1);
   }
   if (a.g.d_s0)
-    reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a);
+    reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
   return cudaGetLastError();
 }
 

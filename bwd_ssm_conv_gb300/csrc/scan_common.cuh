@@ -26,6 +26,34 @@ __host__ inline void state_split(int N, int pref_ns, int* ns, int* tpc) {
   *tpc = pow2_ceil((N + *ns - 1) / *ns);
 }
 
+// ---- the per-step decay ---------------------------------------------------------------
+// Fast form (bf16 I/O): a = 2^(delta A log2 e) by the SFU, h <- a h + u.
+// Accurate form (fp32 I/O): e = exp(delta A) - 1 and h <- h + (e h + u).  When delta |A| is
+// small, a sits just below 1 and fp32 cannot hold 1 - a to better than ~6e-8 / (delta |A|);
+// the SFU result is also biased there (about -0.3 ulp), and both errors compound over the
+// ~1 / (delta |A|) tokens a state remembers.  Carrying e instead keeps each step's error at
+// one fp32 rounding of h.  e comes from the Taylor series x + x^2/2 + x^3/6 + x^4/24
+// (remainder below 1.3e-7 relative for |x| < 1/16) and from 2^(x log2 e) - 1 above that.
+template <bool ACC>
+__device__ __forceinline__ float decay_coef(float dl, float A2) {
+  const float x2 = dl * A2;  // delta A log2(e)
+  if (!ACC) return ex2(x2);
+  const float x = x2 * 0.6931471805599453f;  // delta A
+  const float p = x * fmaf(x, fmaf(x, fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+  const float q = ex2(x2) - 1.0f;
+  return fabsf(x) < 0.0625f ? p : q;
+}
+// h <- a h + u   (fast)   or   h <- h + (e h + u)   (accurate)
+template <bool ACC>
+__device__ __forceinline__ float decay_step(float coef, float h, float u) {
+  return ACC ? h + fmaf(coef, h, u) : fmaf(coef, h, u);
+}
+// a * v   (fast)   or   v + e v   (accurate)
+template <bool ACC>
+__device__ __forceinline__ float decay_apply(float coef, float v) {
+  return ACC ? fmaf(coef, v, v) : coef * v;
+}
+
 // Lanes of the tpc-lane group this lane belongs to (xor-shuffles stay inside it).
 __device__ __forceinline__ unsigned group_mask(int tpc) {
   if (tpc >= 32) return 0xffffffffu;

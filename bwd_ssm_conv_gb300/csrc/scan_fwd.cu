@@ -35,6 +35,7 @@ struct FwdArgs {
 template <typename IO, int NS, bool SCALAR_A, bool LOCAL, bool FULL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_kernel(const FwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;  // accurate decay form for fp32 I/O
   const ScanProblem& p = a.p;
   const int tpc = a.tpc;
   const int tid = threadIdx.x;
@@ -98,11 +99,11 @@ scan_fwd_kernel(const FwdArgs a) {
     load_row<IO, NS, FULL>(Bm + (tok * p.G + g) * N + n0, N - n0, Bv);
     if (!LOCAL) load_row<IO, NS, FULL>(Cm + (tok * p.G + g) * N + n0, N - n0, Cv);
     float acc = 0.0f;
-    const float as = SCALAR_A ? ex2(dl * A2[0]) : 0.0f;
+    const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
 #pragma unroll
     for (int j = 0; j < NS; j++) {
-      const float av = SCALAR_A ? as : ex2(dl * A2[j]);
-      hs[j] = fmaf(av, hs[j], dx * Bv[j]);
+      const float av = SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]);
+      hs[j] = decay_step<ACC>(av, hs[j], dx * Bv[j]);
       if (!LOCAL) acc = fmaf(Cv[j], hs[j], acc);
     }
     if (LOCAL) {
@@ -187,13 +188,13 @@ template <typename IO, int NS, bool SCALAR_A, bool FULL>
 static void launch_fwd_t(const FwdArgs& a, int blocks_x, cudaStream_t st) {
   if (a.S > 1) {
     dim3 g1(blocks_x, a.S - 1, a.p.ns);
-    scan_fwd_kernel<IO, NS, SCALAR_A, true, FULL><<<g1, kScanThreads, 0, st>>>(a);
+    scan_fwd_kernel<IO, NS, SCALAR_A, true, FULL><<<g1, kScanThreads, 0, st>>>(a), count_launches(1);
     const long total = (long)a.p.ns * a.p.HP * a.p.N;
     int nb = (int)((total + 255) / 256);
-    scan_fwd_carry_kernel<<<nb, 256, 0, st>>>(a);
+    scan_fwd_carry_kernel<<<nb, 256, 0, st>>>(a), count_launches(1);
   }
   dim3 g2(blocks_x, a.S, a.p.ns);
-  scan_fwd_kernel<IO, NS, SCALAR_A, false, FULL><<<g2, kScanThreads, 0, st>>>(a);
+  scan_fwd_kernel<IO, NS, SCALAR_A, false, FULL><<<g2, kScanThreads, 0, st>>>(a), count_launches(1);
 }
 
 template <typename IO, int NS>

@@ -166,6 +166,10 @@ const char* ssm_status_string(int status);
 /* SSM_ABI_VERSION of the loaded library. */
 int ssm_abi_version(void);
 
+/* Diagnostic: number of kernels this library has enqueued in this process so far (all
+ * devices, all streams).  Lets a caller count the launches of a region of its program. */
+unsigned long long ssm_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,205 @@
+"""GPU parity of the selective scan (forward and backward) against the f64 oracle.
+
+Small cases span several blocks, several time segments and ragged tails (tokens not a
+multiple of the chunk or of the 8-token sub-chunk, channels not a multiple of the block,
+padded state counts); the benchmark configurations run at full size with the oracle on
+sampled channels; dB / dC at full size use an upstream gradient that is non-zero on the
+sampled channels only, so that the oracle's subset sums are exact.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from bwd_ssm_conv_gb300 import binding
+from bwd_ssm_conv_gb300.workloads import CONFIGS, make_inputs, random_scan_inputs
+from gpu_util import (assert_close, channel_subset, gpu_bwd, gpu_fwd, oracle_bwd, oracle_fwd, tol)
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_s0", "d_dt_bias")
+
+# name, shape (ns, L, H, P, N, G), io, scalar_a, chunk, softplus, with ids
+CASES = [
+    ("cfg0_shape", (1, 64, 16, 1, 4, 1), "f32", False, 16, False, False),
+    ("multiseg_ragged", (2, 1000, 24, 1, 16, 1), "f32", False, 100, False, False),
+    ("padded_groups_ids_softplus", (3, 77, 6, 2, 3, 3), "f32", False, 16, True, True),
+    ("mamba2_form", (2, 300, 4, 8, 32, 2), "f32", True, 64, False, False),
+    ("bf16", (2, 333, 48, 1, 16, 1), "bf16", False, 128, False, False),
+    ("n24_padded", (1, 50, 8, 1, 24, 1), "f32", False, 7, False, False),
+    ("big_chunk_rechunked", (1, 1300, 5, 1, 16, 1), "f32", False, 600, False, False),
+    ("single_token", (2, 1, 3, 1, 16, 1), "f32", False, 256, False, False),
+    ("n128_mamba2", (1, 40, 2, 4, 128, 1), "f32", True, 16, False, False),
+]
+
+
+def _inputs(shape, io, scalar_a, softplus, seed):
+    ns, L, H, P, N, G = shape
+    inp = random_scan_inputs(ns, L, H, P, N, n_group=G, io=io, scalar_a=scalar_a, seed=seed,
+                             dt_raw=softplus, has_z=not scalar_a, has_D=not scalar_a)
+    if softplus:
+        inp["dt_bias"] = torch.linspace(-0.5, 0.5, H).float()
+    return inp
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_scan_forward_parity(case):
+    name, shape, io, scalar_a, chunk, softplus, with_ids = case
+    inp = _inputs(shape, io, scalar_a, softplus, seed=zlib.crc32(name.encode()) % 1000)
+    ids, rows = None, 0
+    if with_ids:
+        rows = shape[0] + 2
+        inp["s0"] = torch.randn(rows, shape[2], shape[3], shape[4]).float()
+        ids = torch.tensor([rows - 1, 0, rows - 1][:shape[0]], dtype=torch.int32)
+    y, st, ck = gpu_fwd(inp, chunk, softplus, ids, rows)
+    yo, so, co = oracle_fwd(inp, chunk, softplus, ids, rows)
+    t = tol(io, grad=False)
+    assert_close("y", y, yo, t)
+    assert_close("state_out", st, so, t)
+    assert_close("ckpt", ck, co, t)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_scan_backward_parity(case):
+    name, shape, io, scalar_a, chunk, softplus, with_ids = case
+    inp = _inputs(shape, io, scalar_a, softplus, seed=zlib.crc32(name.encode()) % 1000 + 1)
+    ids, rows = None, 0
+    if with_ids:
+        rows = shape[0] + 2
+        inp["s0"] = torch.randn(rows, shape[2], shape[3], shape[4]).float()
+        ids = torch.tensor([rows - 1, 0, rows - 1][:shape[0]], dtype=torch.int32)
+    _, _, ck = gpu_fwd(inp, chunk, softplus, ids, rows)
+    g = gpu_bwd(inp, chunk, ckpt=ck, softplus=softplus, ids=ids, state_rows=rows)
+    o = oracle_bwd(inp, chunk, softplus, ids, rows)
+    t = tol(io, grad=True)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], t)
+    assert binding.ssm_scan_status(g["_ws"]) == 0
+
+
+def test_backward_without_checkpoints_recomputes():
+    inp = _inputs((2, 200, 8, 1, 16, 1), "f32", False, False, seed=5)
+    g1 = gpu_bwd(inp, 32, ckpt=None)
+    _, _, ck = gpu_fwd(inp, 32)
+    g2 = gpu_bwd(inp, 32, ckpt=ck)
+    for k in ("d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_s0"):
+        assert torch.equal(g1[k], g2[k]), k
+
+
+def test_backward_is_bitwise_deterministic():
+    inp = _inputs((2, 700, 40, 1, 16, 1), "f32", False, False, seed=6)
+    _, _, ck = gpu_fwd(inp, 64)
+    g1 = gpu_bwd(inp, 64, ckpt=ck)
+    g2 = gpu_bwd(inp, 64, ckpt=ck)
+    for k in ("d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_s0"):
+        assert torch.equal(g1[k], g2[k]), k
+
+
+def test_zero_upstream_gives_zero_gradients():
+    inp = _inputs((2, 90, 8, 1, 16, 1), "f32", False, False, seed=7)
+    inp["dy"] = torch.zeros_like(inp["dy"])
+    g = gpu_bwd(inp, 32, d_state_out=False)
+    for k in ("d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_s0"):
+        assert not torch.any(g[k]), k
+
+
+def test_bad_id_is_reported_not_read():
+    inp = _inputs((2, 20, 4, 1, 16, 1), "f32", False, False, seed=8)
+    inp["s0"] = torch.randn(2, 4, 1, 16)
+    ids = torch.tensor([1, 7], dtype=torch.int32)  # 7 is outside [0, 2)
+    shape = binding.scan_shape(inp["x"], inp["dt"], inp["A"], inp["B"], inp["s0"], 16)
+    ws = torch.empty(binding.ssm_scan_workspace_size(shape, False), dtype=torch.uint8,
+                     device="cuda")
+    d = {k: v.cuda() for k, v in inp.items() if torch.is_tensor(v)}
+    y, _, _ = binding.ssm_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                   s0=d["s0"], ids=ids.cuda(), chunk=16, state_rows=2, ws=ws)
+    assert binding.ssm_scan_status(ws) == binding.SSM_ERR_INVALID_ARG
+    # the bad row reads as a zero initial state
+    inp0 = dict(inp)
+    inp0["s0"] = None
+    y0, _, _ = oracle_fwd(inp0, 16)
+    assert_close("y[seq 1]", y[1], y0[1], 1e-4)
+
+
+def test_ggml_packing_roundtrip():
+    inp = _inputs((2, 5, 3, 2, 4, 1), "f32", True, False, seed=9)
+    y, st, _ = gpu_fwd(inp, 256)
+    packed = binding.pack_scan_result(y, st)
+    assert packed.numel() == inp["x"].numel() + 2 * 3 * 2 * 4
+    assert torch.equal(packed[: y.numel()].view_as(y), y)
+
+
+# ---- full-size benchmark configurations ---------------------------------------------------
+
+def _config_inputs(i):
+    w = CONFIGS[i]
+    inp = make_inputs(w, grad_seed_state=True)
+    if inp["x"] is None:  # the conv prelude produces x; the scan parity needs only its shape
+        g = torch.Generator().manual_seed(w.seed + 7)
+        inp["x"] = torch.randn(w.n_seqs, w.n_tok, w.n_head, w.head_dim, generator=g).to(w.torch_io)
+    return w, inp
+
+
+@pytest.mark.parametrize("i", [1])
+def test_config_full_parity(i):
+    w, inp = _config_inputs(i)
+    y, st, ck = gpu_fwd(inp, w.chunk)
+    yo, so, co = oracle_fwd(inp, w.chunk)
+    assert_close("y", y, yo, tol(w.io, False))
+    assert_close("state_out", st, so, tol(w.io, False))
+    assert_close("ckpt", ck, co, tol(w.io, False))
+    g = gpu_bwd(inp, w.chunk, ckpt=ck)
+    o = oracle_bwd(inp, w.chunk)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], tol(w.io, True))
+
+
+def test_config2_mamba2_forward_sampled_heads():
+    w, inp = _config_inputs(2)
+    y, st, ck = gpu_fwd(inp, w.chunk)
+    heads = [0, 11, 23]
+    sub = dict(inp)
+    for k in ("x", "dt"):
+        sub[k] = inp[k][:, :, heads]
+    sub["A"] = inp["A"][heads]
+    sub["s0"] = inp["s0"][:, heads]
+    sub["D"] = sub["z"] = None
+    yo, so, co = oracle_fwd(sub, w.chunk)
+    assert_close("y", y[:, :, heads], yo, tol(w.io, False))
+    assert_close("state_out", st[:, heads], so, tol(w.io, False))
+    assert_close("ckpt", ck[:, :, heads], co, tol(w.io, False))
+
+
+@pytest.mark.parametrize("i", [3, 4])
+def test_config_full_size_sampled_channels(i):
+    w, inp = _config_inputs(i)
+    D = w.n_head
+    idx = torch.tensor(sorted({0, 1, 31, 32, 127, D // 2, D - 2, D - 1}), dtype=torch.long)
+    y, st, ck = gpu_fwd(inp, w.chunk)
+    sub = channel_subset(inp, idx)
+    yo, so, co = oracle_fwd(sub, w.chunk)
+    assert_close("y", y[:, :, idx], yo, tol(w.io, False))
+    assert_close("state_out", st[:, idx], so, tol(w.io, False))
+    assert_close("ckpt", ck[:, :, idx], co, tol(w.io, False))
+    # dense upstream gradient: every per-channel gradient of the sampled channels
+    g = gpu_bwd(inp, w.chunk, ckpt=ck)
+    o = oracle_bwd(sub, w.chunk)
+    for k in ("d_x", "d_dt", "d_z"):
+        assert_close(k, g[k][:, :, idx], o[k], tol(w.io, True))
+    assert_close("d_A", g["d_A"][idx], o["d_A"], tol(w.io, True))
+    assert_close("d_D", g["d_D"][idx], o["d_D"], tol(w.io, True))
+    assert_close("d_s0", g["d_s0"][:, idx], o["d_s0"], tol(w.io, True))
+    # upstream gradient only on the sampled channels: dB and dC reduce to the subset's sums
+    sparse = dict(inp)
+    mask = torch.zeros(D, dtype=torch.bool)
+    mask[idx] = True
+    sparse["dy"] = torch.where(mask[None, None, :, None], inp["dy"], torch.zeros_like(inp["dy"]))
+    sparse["d_state_out"] = torch.where(mask[None, :, None, None], inp["d_state_out"],
+                                        torch.zeros_like(inp["d_state_out"]))
+    gs = gpu_bwd(sparse, w.chunk, ckpt=ck)
+    os_ = oracle_bwd(channel_subset(sparse, idx), w.chunk)
+    assert_close("d_B", gs["d_B"], os_["d_B"], tol(w.io, True))
+    assert_close("d_C", gs["d_C"], os_["d_C"], tol(w.io, True))
