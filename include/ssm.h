@@ -125,6 +125,24 @@ int ssm_conv_bwd(const void* sx, const float* c, const float* bias, const void* 
                  int n_s, int d_inner, int n_t, int d_conv, int io, unsigned flags,
                  void* stream);
 
+/* Allocation-free variant of ssm_conv_bwd (no counterpart on the source pages).
+ * For callers that cannot allocate device memory -- for example code running where a
+ * cudaMalloc is not allowed because it can synchronise the device or block (a host callback,
+ * a latency-bound serving loop, a plugin interface), or a process whose device memory is held
+ * entirely by another framework's pool.  Same arguments as ssm_conv_bwd without the
+ * workspace: the scratch is a fixed array of SSM_NOALLOC_SCRATCH_BYTES in the library's own
+ * device memory, which every GPU that loads the library holds until the process exits.
+ * Sizes whose scratch (ssm_conv_workspace_size) exceeds it return SSM_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All calls on a
+ * device share the array and it keeps the last call's contents (each call overwrites what it
+ * reads), so calls that overlap on the GPU -- on different streams or threads -- race: keep
+ * them ordered on one stream.  Allocates and frees nothing. */
+#define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
+int ssm_conv_bwd_noalloc(const void* sx, const float* c, const float* bias, const void* dout,
+                         void* d_sx, float* d_c, float* d_bias, int n_s, int d_inner, int n_t,
+                         int d_conv, int io, unsigned flags, void* stream);
+
 /* ---- selective scan ---------------------------------------------------------------------
  * Bytes of scratch ssm_scan_fwd (backward = 0) or ssm_scan_bwd (backward = 1) needs for this
  * descriptor on the current device; 0 if the descriptor is invalid.  Always >= 256 (the
