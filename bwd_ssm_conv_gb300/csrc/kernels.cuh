@@ -35,7 +35,11 @@ struct ScanProblem {
 };
 
 // Forward.  y may be NULL (states / checkpoints only), state_out may be NULL, ckpt may be NULL.
+// launch_scan_fwd takes the TMA-staged path (scan_fwd_tma.cu) when it applies.
 size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms);
+size_t scan_fwd_tma_ws_bytes(const ScanProblem& p, int num_sms);  // 0: path does not apply
+cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out, float* ckpt,
+                                void* ws, int num_sms, cudaStream_t st);
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st);
 

@@ -182,7 +182,10 @@ static FwdPlan plan_fwd(const ScanProblem& p, int num_sms) {
   return q;
 }
 
-size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms) { return plan_fwd(p, num_sms).bytes; }
+size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms) {
+  const size_t a = plan_fwd(p, num_sms).bytes, b = scan_fwd_tma_ws_bytes(p, num_sms);
+  return a > b ? a : b;
+}
 
 template <typename IO, int NS, bool SCALAR_A, bool FULL>
 static void launch_fwd_t(const FwdArgs& a, int blocks_x, cudaStream_t st) {
@@ -221,6 +224,8 @@ static void launch_fwd_io(const FwdArgs& a, int ns_state, int blocks_x, bool ful
 
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st) {
+  const cudaError_t e = launch_scan_fwd_tma(p, y, state_out, ckpt, ws, num_sms, st);
+  if (e != cudaErrorNotSupported) return e;
   const FwdPlan q = plan_fwd(p, num_sms);
   FwdArgs a{};
   a.p = p;

@@ -1,0 +1,364 @@
+// scan_fwd_tma.cu -- forward scan with TMA-staged tiles: the fast path for the Mamba-1
+// layout (head_dim 1; channel rows 16-byte aligned).  Other shapes use scan_fwd.cu.
+//
+// Same arithmetic and segment decomposition as scan_fwd.cu (local aggregate, carry, main),
+// but every block streams its inputs as [tile tokens][block channels] tiles of x, dt, z and
+// [tile tokens][N] tiles of B, C into a ring of shared-memory stages: one elected thread
+// issues 3-D cp.async.bulk.tensor loads that complete on an mbarrier per stage, so the
+// loads of the next tiles overlap the arithmetic of this one.  y leaves the same way, one
+// tile per TMA store.  Segments are whole tiles long, so no tile straddles two segments;
+// the sequence end is clipped by the tensor bounds (loads fill zeros, stores skip).
+#include "common.cuh"
+#include "kernels.cuh"
+#include "scan_common.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+
+constexpr int kFwdStages = 3;
+
+struct FwdTmaArgs {
+  CUtensorMap mx, mdt, mz, my, mb, mc;
+  ScanProblem p;
+  int S, seg_len, tpc, cb, tt;
+  float* state_out;
+  float* ckpt;
+  float* segstart;
+  float* hloc;
+  float* sumdelta;
+  int has_y;
+  uint32_t bytes_main, bytes_local;        // expected transaction bytes per stage
+  uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride, off_y, y_stride, off_bar;
+};
+
+template <typename IO>
+__device__ __forceinline__ float lds1(const IO* p) {
+  if constexpr (sizeof(IO) == 4) return *reinterpret_cast<const float*>(p);
+  else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+}
+
+// NS consecutive values of a shared-memory row (16-byte aligned when NS*sizeof(IO) >= 16).
+template <typename IO, int NS>
+__device__ __forceinline__ void lds_row(const IO* ptr, float (&out)[NS]) {
+  if constexpr (sizeof(IO) == 4) {
+#pragma unroll
+    for (int j = 0; j < NS; j += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ptr + j);
+      out[j] = v.x; out[j + 1] = v.y; out[j + 2] = v.z; out[j + 3] = v.w;
+    }
+  } else if constexpr (NS >= 8) {
+#pragma unroll
+    for (int j = 0; j < NS; j += 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(ptr + j);
+      const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const float2 f = __bfloat1622float2(q[k]);
+        out[j + 2 * k] = f.x; out[j + 2 * k + 1] = f.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NS; j += 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(ptr + j);
+      const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int k = 0; k < 2; k++) {
+        const float2 f = __bfloat1622float2(q[k]);
+        out[j + 2 * k] = f.x; out[j + 2 * k + 1] = f.y;
+      }
+    }
+  }
+}
+
+template <typename IO, int NS, bool LOCAL>
+__global__ void __launch_bounds__(kScanThreads)
+scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const ScanProblem& p = a.p;
+  const int tid = threadIdx.x, tpc = a.tpc, cb = a.cb, tt = a.tt;
+  const int cl = tid / tpc, sg = tid - cl * tpc;
+  const int ch0 = blockIdx.x * cb, ch = ch0 + cl;
+  const int s = blockIdx.y, b = blockIdx.z;
+  const int N = p.N, n0 = sg * NS;
+  const int g = ch0 / (p.H / p.G);
+  const int t_begin = s * a.seg_len, t_end = min(p.L, t_begin + a.seg_len);
+  const int ntiles = (t_end - t_begin + tt - 1) / tt;
+  const uint32_t bytes = LOCAL ? a.bytes_local : a.bytes_main;
+  const bool want_y = !LOCAL && a.has_y;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+
+  if (tid == 0) {
+    for (int i = 0; i < kFwdStages; i++) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int k) {  // tile k -> stage k % kFwdStages (thread 0 only)
+    const int stg = k % kFwdStages;
+    unsigned char* base = smem + stg * a.stage_stride;
+    const int t0 = t_begin + k * tt;
+    mbar_expect_tx(&full[stg], bytes);
+    tma_load_3d(base + a.off_x, &a.mx, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + a.off_dt, &a.mdt, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + a.off_b, &a.mb, g * N, t0, b, &full[stg]);
+    if (!LOCAL) {
+      if (p.z) tma_load_3d(base + a.off_z, &a.mz, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + a.off_c, &a.mc, g * N, t0, b, &full[stg]);
+    }
+  };
+  if (tid == 0)
+    for (int k = 0; k < kFwdStages && k < ntiles; k++) issue(k);
+
+  float A2[NS];
+#pragma unroll
+  for (int j = 0; j < NS; j++) A2[j] = __ldg(p.A + (long)ch * N + n0 + j) * kLog2e;
+  float hs[NS];
+  if (LOCAL) {
+#pragma unroll
+    for (int j = 0; j < NS; j++) hs[j] = 0.0f;
+  } else if (s == 0) {
+    const float* row = start_row(p, b);
+#pragma unroll
+    for (int j = 0; j < NS; j++) hs[j] = row ? __ldg(row + (long)ch * N + n0 + j) : 0.0f;
+  } else {
+    const float* src = a.segstart + (((long)b * a.S + s) * p.HP + ch) * N + n0;
+#pragma unroll
+    for (int j = 0; j < NS; j++) hs[j] = src[j];
+  }
+  const float Dv = p.D ? __ldg(p.D + ch) : 0.0f;
+  const float bias = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch) : 0.0f;
+  const unsigned gmask = group_mask(tpc);
+  float sumd = 0.0f;
+
+  for (int k = 0; k < ntiles; k++) {
+    const int stg = k % kFwdStages;
+    if (want_y && tid == 0) tma_store_wait_read<1>();  // store k-2 has read its y buffer
+    const bool ok = mbar_wait(&full[stg], (uint32_t)(k / kFwdStages) & 1u);
+    if (__syncthreads_or(!ok)) {  // a tile never arrived: report, drain, leave
+      if (tid == 0) {
+        record_status(p.status, SSM_ERR_TIMEOUT);
+        for (int j = k; j < ntiles && j < k + kFwdStages; j++)
+          mbar_wait(&full[j % kFwdStages], (uint32_t)(j / kFwdStages) & 1u);
+        tma_store_wait_all();
+      }
+      return;
+    }
+    const unsigned char* base = smem + stg * a.stage_stride;
+    const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
+    const IO* sdt = reinterpret_cast<const IO*>(base + a.off_dt);
+    const IO* sz = reinterpret_cast<const IO*>(base + a.off_z);
+    const IO* sB = reinterpret_cast<const IO*>(base + a.off_b);
+    const IO* sC = reinterpret_cast<const IO*>(base + a.off_c);
+    IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
+    const int t0 = t_begin + k * tt;
+    const int cnt = min(tt, t_end - t0);
+    for (int i = 0; i < cnt; i++) {
+      const int t = t0 + i;
+      if (!LOCAL && a.ckpt && (t % p.chunk) == 0) {
+        float* dst = a.ckpt + (((long)b * p.n_chunks + t / p.chunk) * p.HP + ch) * N + n0;
+#pragma unroll
+        for (int j = 0; j < NS; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(hs[j], hs[j + 1], hs[j + 2], hs[j + 3]);
+      }
+      float dl = lds1(sdt + i * cb + cl);
+      if (p.softplus) dl = softplusf_(dl + bias);
+      const float xv = lds1(sx + i * cb + cl);
+      const float dx = dl * xv;
+      float Bv[NS];
+      lds_row<IO, NS>(sB + i * N + n0, Bv);
+      if (LOCAL) {
+#pragma unroll
+        for (int j = 0; j < NS; j++) hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
+        sumd += dl;
+      } else {
+        float Cv[NS];
+        lds_row<IO, NS>(sC + i * N + n0, Cv);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NS; j++) {
+          hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
+          acc = fmaf(Cv[j], hs[j], acc);
+        }
+        for (int off = tpc >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(gmask, acc, off);
+        if (want_y && sg == 0) {
+          float yv = fmaf(Dv, xv, acc);
+          if (p.z) yv *= siluf_(lds1(sz + i * cb + cl));
+          if (p.check_finite && !isfinite(yv)) record_status(p.status, SSM_ERR_NONFINITE);
+          if constexpr (sizeof(IO) == 4) sy[i * cb + cl] = yv;
+          else sy[i * cb + cl] = __float2bfloat16_rn(yv);
+        }
+      }
+    }
+    if (want_y) fence_async_shared();
+    __syncthreads();  // stage stg fully read, y tile complete
+    if (tid == 0) {
+      if (want_y) {
+        tma_store_3d(&a.my, sy, ch0, t0, b);
+        tma_store_commit();
+      }
+      if (k + kFwdStages < ntiles) issue(k + kFwdStages);
+    }
+  }
+  if (want_y && tid == 0) tma_store_wait_all();
+
+  if (LOCAL) {
+    float* dst = a.hloc + (((long)b * a.S + s) * p.HP + ch) * N + n0;
+#pragma unroll
+    for (int j = 0; j < NS; j++) dst[j] = hs[j];
+    if (sg == 0) a.sumdelta[((long)b * a.S + s) * p.HP + ch] = sumd;
+  } else if (s == a.S - 1 && a.state_out) {
+    float* dst = a.state_out + ((long)b * p.HP + ch) * N + n0;
+#pragma unroll
+    for (int j = 0; j < NS; j++) dst[j] = hs[j];
+  }
+}
+
+// Same composition as scan_fwd.cu's carry kernel (kept separate to keep that file unchanged).
+__global__ void scan_fwd_tma_carry_kernel(const __grid_constant__ FwdTmaArgs a) {
+  const ScanProblem& p = a.p;
+  const long total = (long)p.ns * p.HP * p.N;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    const int n = (int)(i % p.N);
+    const long bc = i / p.N;
+    const int ch = (int)(bc % p.HP), b = (int)(bc / p.HP);
+    const float A2 = __ldg(p.A + (long)ch * p.N + n) * kLog2e;
+    const float* row = start_row(p, b);
+    float hv = row ? __ldg(row + (long)ch * p.N + n) : 0.0f;
+    for (int s = 0; s < a.S; s++) {
+      const long si = ((long)b * a.S + s) * p.HP + ch;
+      a.segstart[si * p.N + n] = hv;
+      if (s + 1 < a.S) hv = fmaf(ex2(A2 * a.sumdelta[si]), hv, a.hloc[si * p.N + n]);
+    }
+  }
+}
+
+// ---- host ------------------------------------------------------------------------------
+struct FwdTmaPlan {
+  bool ok;
+  int ns_state, tpc, cb, tt, S, seg_len;
+  size_t smem, off_segstart, off_hloc, off_sumdelta, bytes;
+};
+
+static bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
+
+static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
+  FwdTmaPlan q{};
+  const int io = p.io == SSM_BF16 ? 2 : 4;
+  if (p.P != 1 || !p.a_per_state || p.N > 256 || (p.N * io) % 16 != 0 || (p.HP * io) % 16 != 0)
+    return q;
+  // largest states-per-thread that still gives two blocks per SM without time segments
+  int ns = 0;
+  for (int cand = 16; cand >= 4; cand >>= 1) {
+    if (p.N % cand != 0) continue;
+    ns = cand;
+    const int cb = kScanThreads / (p.N / cand);
+    if (cb > 0 && (long)p.ns * ((p.HP + cb - 1) / cb) >= 2L * num_sms) break;
+  }
+  if (ns < 4 || p.N / ns > 32) return q;
+  q.ns_state = ns;
+  q.tpc = p.N / ns;
+  if (q.tpc > 32) return q;
+  q.cb = kScanThreads / q.tpc;
+  if ((p.H / p.G) % q.cb != 0 || p.HP % q.cb != 0 || q.cb * io < 16) return q;
+  const int zt = p.z ? 1 : 0;
+  const int per_tok = q.cb * io * (2 + zt) + 2 * p.N * io;
+  q.tt = per_tok * 32 <= 16384 ? 32 : (per_tok * 16 <= 16384 ? 16 : 8);
+  const long base = (long)p.ns * (p.HP / q.cb);
+  long S = (2L * num_sms + base - 1) / base;
+  const long max_s = (p.L + kMinSegment - 1) / kMinSegment;
+  if (S > max_s) S = max_s;
+  if (S < 1) S = 1;
+  int seg = (int)((p.L + S - 1) / S);
+  seg = (seg + q.tt - 1) / q.tt * q.tt;
+  q.seg_len = seg;
+  q.S = (p.L + seg - 1) / seg;
+  size_t off = kStatusBytes;
+  const size_t st_bytes = sizeof(float) * (size_t)p.ns * q.S * p.HP * p.N;
+  if (q.S > 1) {
+    q.off_segstart = off; off = align_up(off + st_bytes, 256);
+    q.off_hloc = off; off = align_up(off + st_bytes, 256);
+    q.off_sumdelta = off; off = align_up(off + sizeof(float) * (size_t)p.ns * q.S * p.HP, 256);
+  }
+  q.bytes = off;
+  q.ok = aligned16(p.x) && aligned16(p.dt) && aligned16(p.B) && aligned16(p.C) &&
+         (!p.z || aligned16(p.z));
+  return q;
+}
+
+size_t scan_fwd_tma_ws_bytes(const ScanProblem& p, int num_sms) {
+  const FwdTmaPlan q = plan_fwd_tma(p, num_sms);
+  return q.ok ? q.bytes : 0;
+}
+
+template <typename IO, int NS>
+static cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
+  auto km = scan_fwd_tma_kernel<IO, NS, false>;
+  auto kl = scan_fwd_tma_kernel<IO, NS, true>;
+  cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int bx = a.p.HP / a.cb;
+  if (a.S > 1) {
+    kl<<<dim3(bx, a.S - 1, a.p.ns), kScanThreads, smem, st>>>(a), count_launches(1);
+    const long total = (long)a.p.ns * a.p.HP * a.p.N;
+    scan_fwd_tma_carry_kernel<<<(int)((total + 255) / 256), 256, 0, st>>>(a), count_launches(1);
+  }
+  km<<<dim3(bx, a.S, a.p.ns), kScanThreads, smem, st>>>(a), count_launches(1);
+  return cudaGetLastError();
+}
+
+// Returns cudaErrorNotSupported (without launching anything) when the fast path does not
+// apply to this problem; the caller then uses the general kernels.
+cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out, float* ckpt,
+                                void* ws, int num_sms, cudaStream_t st) {
+  const FwdTmaPlan q = plan_fwd_tma(p, num_sms);
+  if (!q.ok || (y && !aligned16(y)) || (ckpt && !aligned16(ckpt))) return cudaErrorNotSupported;
+  const int io = p.io == SSM_BF16 ? 2 : 4;
+  FwdTmaArgs a;
+  memset(&a, 0, sizeof(a));
+  a.p = p;
+  a.S = q.S; a.seg_len = q.seg_len; a.tpc = q.tpc; a.cb = q.cb; a.tt = q.tt;
+  a.state_out = state_out; a.ckpt = ckpt; a.has_y = y != nullptr;
+  char* w = (char*)ws;
+  if (q.S > 1) {
+    a.segstart = (float*)(w + q.off_segstart);
+    a.hloc = (float*)(w + q.off_hloc);
+    a.sumdelta = (float*)(w + q.off_sumdelta);
+  }
+  const uint64_t C = p.HP, L = p.L, NSq = p.ns, GN = (uint64_t)p.G * p.N;
+  bool ok = encode_tmap_3d(&a.mx, p.x, io, C, L, NSq, C, C * L, q.cb, q.tt, 1) &&
+            encode_tmap_3d(&a.mdt, p.dt, io, C, L, NSq, C, C * L, q.cb, q.tt, 1) &&
+            encode_tmap_3d(&a.mb, p.B, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1) &&
+            encode_tmap_3d(&a.mc, p.C, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1);
+  if (ok && p.z) ok = encode_tmap_3d(&a.mz, p.z, io, C, L, NSq, C, C * L, q.cb, q.tt, 1);
+  if (ok && y) ok = encode_tmap_3d(&a.my, y, io, C, L, NSq, C, C * L, q.cb, q.tt, 1);
+  if (!ok) return cudaErrorNotSupported;
+  const uint32_t tile = (uint32_t)(q.tt * q.cb * io), row = (uint32_t)(q.tt * p.N * io);
+  auto al = [](uint32_t v) { return (v + 127u) & ~127u; };
+  a.off_x = 0;
+  a.off_dt = al(tile);
+  a.off_z = a.off_dt + al(tile);
+  a.off_b = a.off_z + (p.z ? al(tile) : 0);
+  a.off_c = a.off_b + al(row);
+  a.stage_stride = a.off_c + al(row);
+  a.off_y = kFwdStages * a.stage_stride;
+  a.y_stride = al(tile);
+  a.off_bar = a.off_y + 2 * a.y_stride;
+  const size_t smem = a.off_bar + 64;
+  a.bytes_local = 2 * tile + row;
+  a.bytes_main = (2 + (p.z ? 1 : 0)) * tile + 2 * row;
+  const bool bf = p.io == SSM_BF16;
+  switch (q.ns_state) {
+    case 16: return bf ? launch_fwd_tma_t<__nv_bfloat16, 16>(a, smem, st)
+                       : launch_fwd_tma_t<float, 16>(a, smem, st);
+    case 8: return bf ? launch_fwd_tma_t<__nv_bfloat16, 8>(a, smem, st)
+                      : launch_fwd_tma_t<float, 8>(a, smem, st);
+    default: return bf ? launch_fwd_tma_t<__nv_bfloat16, 4>(a, smem, st)
+                       : launch_fwd_tma_t<float, 4>(a, smem, st);
+  }
+}
+
+}  // namespace ssm

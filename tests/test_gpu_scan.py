@@ -31,6 +31,11 @@ CASES = [
     ("big_chunk_rechunked", (1, 1300, 5, 1, 16, 1), "f32", False, 600, False, False),
     ("single_token", (2, 1, 3, 1, 16, 1), "f32", False, 256, False, False),
     ("n128_mamba2", (1, 40, 2, 4, 128, 1), "f32", True, 16, False, False),
+    # shapes that take the TMA-staged kernels (channels a multiple of 32, d_state 16)
+    ("tma_f32_ragged_multiseg", (2, 300, 64, 1, 16, 1), "f32", False, 64, False, False),
+    ("tma_bf16_softplus", (3, 520, 96, 1, 16, 1), "bf16", False, 128, True, False),
+    ("tma_chunk24_tile8", (1, 200, 32, 1, 16, 1), "f32", False, 24, False, False),
+    ("tma_groups", (2, 100, 64, 1, 16, 2), "bf16", False, 32, False, False),
 ]
 
 
@@ -77,6 +82,27 @@ def test_scan_backward_parity(case):
         if o.get(k) is not None and g.get(k) is not None:
             assert_close(k, g[k], o[k], t)
     assert binding.ssm_scan_status(g["_ws"]) == 0
+
+
+def test_misaligned_inputs_fall_back_to_general_kernels():
+    inp = _inputs((2, 150, 64, 1, 16, 1), "f32", False, False, seed=11)
+    # x one element past a 16-byte boundary: the TMA paths cannot take it
+    buf = torch.empty(inp["x"].numel() + 1)
+    buf[1:] = inp["x"].reshape(-1)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    xbuf = buf.cuda()
+    x_mis = xbuf[1:].view_as(inp["x"])
+    assert x_mis.data_ptr() % 16 != 0
+    y, st, ck = binding.ssm_scan_fwd(x_mis, d["dt"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                     s0=d["s0"], chunk=32)
+    yo, so, co = oracle_fwd(inp, 32)
+    assert_close("y", y, yo, 1e-4)
+    assert_close("ckpt", ck, co, 1e-4)
+    g = binding.ssm_scan_bwd(x_mis, d["dt"], d["A"], d["B"], d["C"], d["dy"], D=d["D"], z=d["z"],
+                             s0=d["s0"], ckpt=ck, d_state_out=d["d_state_out"], chunk=32)
+    o = oracle_bwd(inp, 32)
+    for k in ("d_x", "d_dt", "d_A", "d_B", "d_C", "d_z"):
+        assert_close(k, g[k], o[k], 1e-3)
 
 
 def test_backward_without_checkpoints_recomputes():
