@@ -16,6 +16,7 @@
 namespace ssm {
 
 constexpr int kFwdStages = 3;
+constexpr int kFwdTile = 16;  // tokens per staged tile
 
 struct FwdTmaArgs {
   CUtensorMap mx, mdt, mz, my, mb, mc;
@@ -28,7 +29,8 @@ struct FwdTmaArgs {
   float* sumdelta;
   int has_y;
   uint32_t bytes_main, bytes_local;        // expected transaction bytes per stage
-  uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride, off_y, y_stride, off_bar;
+  uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride;  // inside a stage
+  uint32_t off_dl, off_dx, off_bf, off_cf, off_acc, off_par, off_y, y_stride, off_bar;
 };
 
 template <typename IO>
@@ -75,29 +77,38 @@ template <typename IO, int NS, bool LOCAL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;
+  constexpr int TT = kFwdTile;
   extern __shared__ __align__(128) unsigned char smem[];
   const ScanProblem& p = a.p;
-  const int tid = threadIdx.x, tpc = a.tpc, cb = a.cb, tt = a.tt;
+  const int tid = threadIdx.x, tpc = a.tpc, cb = a.cb;
   const int cl = tid / tpc, sg = tid - cl * tpc;
   const int ch0 = blockIdx.x * cb, ch = ch0 + cl;
   const int s = blockIdx.y, b = blockIdx.z;
   const int N = p.N, n0 = sg * NS;
   const int g = ch0 / (p.H / p.G);
   const int t_begin = s * a.seg_len, t_end = min(p.L, t_begin + a.seg_len);
-  const int ntiles = (t_end - t_begin + tt - 1) / tt;
+  const int ntiles = (t_end - t_begin + TT - 1) / TT;
   const uint32_t bytes = LOCAL ? a.bytes_local : a.bytes_main;
   const bool want_y = !LOCAL && a.has_y;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+  float* sDL = reinterpret_cast<float*>(smem + a.off_dl);    // [TT][cb] delta
+  float* sDX = reinterpret_cast<float*>(smem + a.off_dx);    // [TT][cb] delta * x
+  float* sACC = reinterpret_cast<float*>(smem + a.off_acc);  // [TT][cb * tpc] partial C . h
+  float* sPar = reinterpret_cast<float*>(smem + a.off_par);  // [cb] D, [cb] dt_bias
 
   if (tid == 0) {
     for (int i = 0; i < kFwdStages; i++) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
+  for (int c = tid; c < cb; c += kScanThreads) {
+    sPar[c] = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
+    sPar[cb + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
+  }
   __syncthreads();
   auto issue = [&](int k) {  // tile k -> stage k % kFwdStages (thread 0 only)
     const int stg = k % kFwdStages;
     unsigned char* base = smem + stg * a.stage_stride;
-    const int t0 = t_begin + k * tt;
+    const int t0 = t_begin + k * TT;
     mbar_expect_tx(&full[stg], bytes);
     tma_load_3d(base + a.off_x, &a.mx, ch0, t0, b, &full[stg]);
     tma_load_3d(base + a.off_dt, &a.mdt, ch0, t0, b, &full[stg]);
@@ -126,10 +137,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
 #pragma unroll
     for (int j = 0; j < NS; j++) hs[j] = src[j];
   }
-  const float Dv = p.D ? __ldg(p.D + ch) : 0.0f;
-  const float bias = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch) : 0.0f;
-  const unsigned gmask = group_mask(tpc);
   float sumd = 0.0f;
+  int next_ck = (t_begin + p.chunk - 1) / p.chunk * p.chunk;  // next checkpoint token
 
   for (int k = 0; k < ntiles; k++) {
     const int stg = k % kFwdStages;
@@ -144,61 +153,106 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
       return;
     }
-    const unsigned char* base = smem + stg * a.stage_stride;
+    unsigned char* base = smem + stg * a.stage_stride;
     const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
     const IO* sdt = reinterpret_cast<const IO*>(base + a.off_dt);
     const IO* sz = reinterpret_cast<const IO*>(base + a.off_z);
-    const IO* sB = reinterpret_cast<const IO*>(base + a.off_b);
-    const IO* sC = reinterpret_cast<const IO*>(base + a.off_c);
-    IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
-    const int t0 = t_begin + k * tt;
-    const int cnt = min(tt, t_end - t0);
+    const int t0 = t_begin + k * TT;
+    const int cnt = min(TT, t_end - t0);
+
+    // ---- prepass, once per (token, channel): delta, delta x; B, C to fp32 --------------------
+    for (int idx = tid; idx < TT * cb; idx += kScanThreads) {
+      const int i = idx / cb, c = idx - i * cb;
+      float dl = lds1(sdt + idx);
+      if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
+      sDL[idx] = dl;
+      sDX[idx] = dl * lds1(sx + idx);
+      (void)i;
+    }
+    const float* sBf;
+    const float* sCf;
+    if constexpr (sizeof(IO) == 4) {
+      sBf = reinterpret_cast<const float*>(base + a.off_b);
+      sCf = reinterpret_cast<const float*>(base + a.off_c);
+    } else {
+      float* wB = reinterpret_cast<float*>(smem + a.off_bf);
+      float* wC = reinterpret_cast<float*>(smem + a.off_cf);
+      const IO* rB = reinterpret_cast<const IO*>(base + a.off_b);
+      const IO* rC = reinterpret_cast<const IO*>(base + a.off_c);
+      for (int idx = tid; idx < TT * N; idx += kScanThreads) {
+        wB[idx] = lds1(rB + idx);
+        if (!LOCAL) wC[idx] = lds1(rC + idx);
+      }
+      sBf = wB;
+      sCf = wC;
+    }
+    __syncthreads();
+
+    // ---- the recurrence: per thread, its channel's NS states over the tile ------------------
+#pragma unroll 2
     for (int i = 0; i < cnt; i++) {
       const int t = t0 + i;
-      if (!LOCAL && a.ckpt && (t % p.chunk) == 0) {
-        float* dst = a.ckpt + (((long)b * p.n_chunks + t / p.chunk) * p.HP + ch) * N + n0;
+      if (!LOCAL && t == next_ck) {
+        if (a.ckpt) {
+          float* dst = a.ckpt + (((long)b * p.n_chunks + t / p.chunk) * p.HP + ch) * N + n0;
 #pragma unroll
-        for (int j = 0; j < NS; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(hs[j], hs[j + 1], hs[j + 2], hs[j + 3]);
+          for (int j = 0; j < NS; j += 4)
+            *reinterpret_cast<float4*>(dst + j) = make_float4(hs[j], hs[j + 1], hs[j + 2], hs[j + 3]);
+        }
+        next_ck += p.chunk;
       }
-      float dl = lds1(sdt + i * cb + cl);
-      if (p.softplus) dl = softplusf_(dl + bias);
-      const float xv = lds1(sx + i * cb + cl);
-      const float dx = dl * xv;
+      const float dl = sDL[i * cb + cl];
+      const float dx = sDX[i * cb + cl];
       float Bv[NS];
-      lds_row<IO, NS>(sB + i * N + n0, Bv);
+#pragma unroll
+      for (int j = 0; j < NS; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
+        Bv[j] = v.x; Bv[j + 1] = v.y; Bv[j + 2] = v.z; Bv[j + 3] = v.w;
+      }
       if (LOCAL) {
 #pragma unroll
-        for (int j = 0; j < NS; j++) hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
+        for (int j = 0; j < NS; j++)
+          hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
         sumd += dl;
       } else {
         float Cv[NS];
-        lds_row<IO, NS>(sC + i * N + n0, Cv);
+#pragma unroll
+        for (int j = 0; j < NS; j += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
+          Cv[j] = v.x; Cv[j + 1] = v.y; Cv[j + 2] = v.z; Cv[j + 3] = v.w;
+        }
         float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < NS; j++) {
           hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
           acc = fmaf(Cv[j], hs[j], acc);
         }
-        for (int off = tpc >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(gmask, acc, off);
-        if (want_y && sg == 0) {
-          float yv = fmaf(Dv, xv, acc);
-          if (p.z) yv *= siluf_(lds1(sz + i * cb + cl));
-          if (p.check_finite && !isfinite(yv)) record_status(p.status, SSM_ERR_NONFINITE);
-          if constexpr (sizeof(IO) == 4) sy[i * cb + cl] = yv;
-          else sy[i * cb + cl] = __float2bfloat16_rn(yv);
-        }
+        sACC[i * cb * tpc + tid] = acc;
       }
     }
-    if (want_y) fence_async_shared();
-    __syncthreads();  // stage stg fully read, y tile complete
-    if (tid == 0) {
-      if (want_y) {
+    __syncthreads();
+
+    // ---- epilogue, once per (token, channel): y = (C . h + D x) silu(z) -> TMA store -----------
+    if (want_y) {
+      IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
+      for (int idx = tid; idx < cnt * cb; idx += kScanThreads) {
+        const int i = idx / cb, c = idx - i * cb;
+        float acc = 0.0f;
+        for (int q = 0; q < tpc; q++) acc += sACC[(i * cb + c) * tpc + q];
+        float yv = fmaf(sPar[c], lds1(sx + idx), acc);
+        if (p.z) yv *= siluf_(lds1(sz + idx));
+        if (p.check_finite && !isfinite(yv)) record_status(p.status, SSM_ERR_NONFINITE);
+        if constexpr (sizeof(IO) == 4) sy[idx] = yv;
+        else sy[idx] = __float2bfloat16_rn(yv);
+      }
+      fence_async_shared();
+      __syncthreads();  // y tile complete; stage stg fully read
+      if (tid == 0) {
         tma_store_3d(&a.my, sy, ch0, t0, b);
         tma_store_commit();
       }
-      if (k + kFwdStages < ntiles) issue(k + kFwdStages);
     }
+    if (tid == 0 && k + kFwdStages < ntiles) issue(k + kFwdStages);
   }
   if (want_y && tid == 0) tma_store_wait_all();
 
@@ -264,7 +318,8 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   if ((p.H / p.G) % q.cb != 0 || p.HP % q.cb != 0 || q.cb * io < 16) return q;
   const int zt = p.z ? 1 : 0;
   const int per_tok = q.cb * io * (2 + zt) + 2 * p.N * io;
-  q.tt = per_tok * 32 <= 16384 ? 32 : (per_tok * 16 <= 16384 ? 16 : 8);
+  (void)per_tok;
+  q.tt = kFwdTile;
   const long base = (long)p.ns * (p.HP / q.cb);
   long S = (2L * num_sms + base - 1) / base;
   const long max_s = (p.L + kMinSegment - 1) / kMinSegment;
@@ -344,7 +399,14 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_b = a.off_z + (p.z ? al(tile) : 0);
   a.off_c = a.off_b + al(row);
   a.stage_stride = a.off_c + al(row);
-  a.off_y = kFwdStages * a.stage_stride;
+  const uint32_t f_tile = (uint32_t)(q.tt * q.cb * 4), f_row = (uint32_t)(q.tt * p.N * 4);
+  a.off_dl = kFwdStages * a.stage_stride;
+  a.off_dx = a.off_dl + al(f_tile);
+  a.off_bf = a.off_dx + al(f_tile);
+  a.off_cf = a.off_bf + al(f_row);
+  a.off_acc = a.off_cf + al(f_row);
+  a.off_par = a.off_acc + al((uint32_t)(q.tt * kScanThreads * 4));
+  a.off_y = a.off_par + al((uint32_t)(2 * q.cb * 4));
   a.y_stride = al(tile);
   a.off_bar = a.off_y + 2 * a.y_stride;
   const size_t smem = a.off_bar + 64;
