@@ -43,6 +43,39 @@ __device__ __forceinline__ float softplus_gradf_(float v) {
   return v > 20.0f ? 1.0f : sigmoidf_(v);
 }
 
+// ---- packed fp32 pairs (fma/mul/add .rn.f32x2): one instruction for two lanes' worth ------
+// On GB300 these run at the same FMA-pipe rate as two scalar ops but take one issue slot.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// 2^v for both halves (two SFU operations).
+__device__ __forceinline__ f2_t f2_ex2(f2_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return f2_pack(ex2(lo), ex2(hi));
+}
+
 // ---- device status word (first 4 bytes of every scan workspace) ---------------------
 // Holds 0 or the first error a kernel recorded.  Only ever written with atomicCAS from 0.
 __device__ __forceinline__ void record_status(int* status, int code) {

@@ -24,64 +24,9 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "scan_common.cuh"
-#include "tma.cuh"
+#include "scan_bwd.cuh"
 
 namespace ssm {
-
-constexpr int kBwdNS = 4;          // states per thread
-constexpr int kTsub = 8;           // tokens of state history held in registers
-constexpr int kMaxBwdChunk = 512;  // larger checkpoint intervals are re-checkpointed at 256
-constexpr int kDefaultChunk = 256;
-
-struct BwdArgs {
-  ScanProblem p;
-  ScanGrads g;
-  const float* ckpt;  // checkpoints at interval chunk_b
-  int chunk_b, nch_b;
-  int S, seg_chunks;  // segments of whole chunks
-  int tpc, bpg, gc;   // threads per channel, blocks per group, channels per group
-  float* dhloc;       // [ns][S][HP][N]
-  float* segend;      // [ns][S][HP][N]
-  float* sumd;        // [ns][S][HP]
-  float* part_bc;     // [ns*L][G][bpg][2][N]
-  float* dA_part;     // [ns][S][HP][N]
-  float* dD_part;     // [ns][S][HP]
-  float* dtb_part;    // [ns][S][HP]
-  float* ddt_part;    // [ns*L][HP]   (head_dim > 1 only)
-  float* dh0;         // [ns][HP][N]
-};
-
-struct Lane {
-  int tpc, cl, sg, g, blk, cig, ch, h, n0;
-  bool valid;
-};
-
-__device__ __forceinline__ Lane lane_of(const BwdArgs& a) {
-  Lane l;
-  l.tpc = a.tpc;
-  l.cl = threadIdx.x / l.tpc;
-  l.sg = threadIdx.x - l.cl * l.tpc;
-  l.g = blockIdx.x / a.bpg;
-  l.blk = blockIdx.x - l.g * a.bpg;
-  l.cig = l.blk * (kScanThreads / l.tpc) + l.cl;
-  l.valid = l.cig < a.gc;
-  l.ch = l.g * a.gc + (l.valid ? l.cig : 0);
-  l.h = l.ch / a.p.P;
-  l.n0 = l.sg * kBwdNS;
-  return l;
-}
-
-template <typename IO>
-__device__ __forceinline__ float delta_of(const ScanProblem& p, const IO* dt, long tok, int h,
-                                          float bias, float* pre) {
-  const float raw = ld(dt + tok * p.H + h);
-  if (p.softplus) {
-    *pre = raw + bias;
-    return softplusf_(*pre);
-  }
-  *pre = raw;
-  return raw;
-}
 
 template <typename IO, bool SCALAR_A, bool FULL>
 __global__ void __launch_bounds__(kScanThreads)
@@ -467,342 +412,7 @@ __global__ void reduce_ds0_kernel(const BwdArgs a) {
   }
 }
 
-// ---- TMA-staged main kernel: Mamba-1 layout, d_state 16 ----------------------------------
-// Same arithmetic and workspace outputs as scan_bwd_kernel, with its inputs streamed as
-// [tile][32 channels] tiles (x, dt, z, dy) and [tile][16] tiles (B, C) through a ring of
-// shared-memory stages filled by cp.async.bulk.tensor, and dx, dz, ddt leaving as TMA-stored
-// tiles.  Per chunk the schedule is: level-1 tiles forward (x, dt, B), then level-2 tiles in
-// reverse (all inputs).  Sub-chunk start states go to a per-block region of global scratch
-// (they are re-read by the same thread shortly after, from L2).  The dB/dC sums over the 8
-// channels of a warp use a transposed butterfly: each of the 3 levels halves the values a
-// lane holds, so the 8 partials (4 dB, 4 dC) of 8 lanes become 1 finished sum per lane in
-// 7 shuffles instead of 24.
-constexpr int kBwdStages = 3;
-
-struct BwdTma {
-  CUtensorMap mx, mdt, mz, mdy, mb, mc, mdx, mdz, mddt;
-  int tt;  // tile tokens: divides chunk_b, multiple of kTsub
-  uint32_t bytes_l1, bytes_l2;
-  uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
-  uint32_t off_out, out_tile, out_stride, off_red, off_bar;
-  float4* bnd;  // global scratch: [blocks][chunk_b / kTsub][threads]
-};
-
-// v holds 8 partials; lanes that differ in bits 2..4 hold other channels.  Returns the sum over
-// those 8 lanes of the partial with original index (lane >> 2) & 7.
-__device__ __forceinline__ float reduce8_transposed(float (&v)[8], int lane) {
-  {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  }
-  {
-    const bool up = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-      const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-  }
-  const bool up = lane & 4;
-  const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-  return keep + __shfl_xor_sync(0xffffffffu, send, 4);
-}
-
-template <typename IO>
-__device__ __forceinline__ float lds_f(const IO* p) {
-  if constexpr (sizeof(IO) == 4) return *reinterpret_cast<const float*>(p);
-  else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
-}
-template <typename IO>
-__device__ __forceinline__ void sts_f(IO* p, float v) {
-  if constexpr (sizeof(IO) == 4) *reinterpret_cast<float*>(p) = v;
-  else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
-}
-template <typename IO>
-__device__ __forceinline__ void lds4(const IO* p, float (&o)[4]) {
-  if constexpr (sizeof(IO) == 4) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-  } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    const __nv_bfloat162* q = reinterpret_cast<const __nv_bfloat162*>(&v);
-    const float2 a0 = __bfloat1622float2(q[0]), a1 = __bfloat1622float2(q[1]);
-    o[0] = a0.x; o[1] = a0.y; o[2] = a1.x; o[3] = a1.y;
-  }
-}
-
-template <typename IO>
-__global__ void __launch_bounds__(kScanThreads)
-scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
-  constexpr bool ACC = sizeof(IO) == 4;
-  constexpr int kWarps = kScanThreads / 32;
-  constexpr int CB = kScanThreads / 4;  // 32 channels, 4 threads x 4 states each
-  extern __shared__ __align__(128) unsigned char smem[];
-  const ScanProblem& p = a.p;
-  const Lane l = lane_of(a);
-  const int N = p.N;  // 16
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cl = l.cl, ch = l.ch, ch0 = ch - cl;
-  const int s = blockIdx.y, b = blockIdx.z;
-  const int tt = m.tt;
-  const int sub_per_tile = tt / kTsub;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  float* red = reinterpret_cast<float*>(smem + m.off_red);  // [tt][warps][2N]
-  const int nsub_max = a.chunk_b / kTsub;
-  float4* bnd = m.bnd + ((long)(b * a.S + s) * gridDim.x + blockIdx.x) * nsub_max * kScanThreads;
-  const int c_first = s * a.seg_chunks;
-  const int c_last = min(a.nch_b, c_first + a.seg_chunks) - 1;
-
-  // The tile schedule: per chunk (last to first), level-1 tiles ascending then level-2 tiles
-  // descending.  Producer and consumers walk it with their own cursors.
-  struct Pos { int ck, lvl, j, nt; };
-  auto ntiles = [&](int ck) {
-    const int t0 = ck * a.chunk_b, t1 = min(p.L, t0 + a.chunk_b);
-    return (t1 - t0 + tt - 1) / tt;
-  };
-  auto first = [&]() { Pos q; q.ck = c_last; q.lvl = 0; q.j = 0; q.nt = ntiles(c_last); return q; };
-  auto advance = [&](Pos& q) {
-    if (q.lvl == 0) {
-      if (++q.j == q.nt) { q.lvl = 1; q.j = q.nt - 1; }
-    } else if (--q.j < 0) {
-      q.ck--; q.lvl = 0; q.j = 0;
-      if (q.ck >= c_first) q.nt = ntiles(q.ck);
-    }
-  };
-
-  if (tid == 0) {
-    for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  Pos pp = first();
-  int issued = 0;
-  auto issue = [&]() {  // thread 0 only
-    const int stg = issued % kBwdStages;
-    unsigned char* base = smem + stg * m.stage_stride;
-    const int t0 = pp.ck * a.chunk_b + pp.j * tt;
-    if (pp.lvl == 0) {
-      mbar_expect_tx(&full[stg], m.bytes_l1);
-      tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
-    } else {
-      mbar_expect_tx(&full[stg], m.bytes_l2);
-      tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_dy, &m.mdy, ch0, t0, b, &full[stg]);
-      if (p.z) tma_load_3d(base + m.off_z, &m.mz, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_c, &m.mc, l.g * N, t0, b, &full[stg]);
-    }
-    issued++;
-    advance(pp);
-  };
-  if (tid == 0)
-    for (int k = 0; k < kBwdStages && pp.ck >= c_first; k++) issue();
-
-  float An[kBwdNS], A2[kBwdNS], carry[kBwdNS];
-  {
-    const long si = ((long)b * a.S + s) * p.HP + ch;
-#pragma unroll
-    for (int j = 0; j < kBwdNS; j++) {
-      An[j] = __ldg(p.A + (long)ch * N + l.n0 + j);
-      A2[j] = An[j] * kLog2e;
-      if (a.S > 1) carry[j] = a.segend[si * N + l.n0 + j];
-      else carry[j] = a.g.d_state_out ? __ldg(a.g.d_state_out + ((long)b * p.HP + ch) * N + l.n0 + j) : 0.0f;
-    }
-  }
-  float dA_acc[kBwdNS] = {0.f, 0.f, 0.f, 0.f};
-  float dD_acc = 0.0f, dtb_acc = 0.0f;
-  const float Dv = p.D ? __ldg(p.D + ch) : 0.0f;
-  const float bias = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch) : 0.0f;
-  float hs[kBwdNS] = {0.f, 0.f, 0.f, 0.f};
-  int n_l2 = 0;
-
-  int q = 0;
-  for (Pos cs = first(); cs.ck >= c_first; advance(cs), q++) {
-    const int stg = q % kBwdStages;
-    if (cs.lvl == 1 && tid == 0) tma_store_wait_read<1>();  // out buffer (n_l2 & 1) is free
-    const bool ok = mbar_wait(&full[stg], (uint32_t)(q / kBwdStages) & 1u);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        record_status(p.status, SSM_ERR_TIMEOUT);
-        for (int j = q; j < issued; j++) mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
-        tma_store_wait_all();
-      }
-      return;
-    }
-    const unsigned char* base = smem + stg * m.stage_stride;
-    const IO* sx = reinterpret_cast<const IO*>(base + m.off_x);
-    const IO* sdt = reinterpret_cast<const IO*>(base + m.off_dt);
-    const IO* sz = reinterpret_cast<const IO*>(base + m.off_z);
-    const IO* sdy = reinterpret_cast<const IO*>(base + m.off_dy);
-    const IO* sB = reinterpret_cast<const IO*>(base + m.off_b);
-    const IO* sC = reinterpret_cast<const IO*>(base + m.off_c);
-    const int t0c = cs.ck * a.chunk_b, t1c = min(p.L, t0c + a.chunk_b);
-    const int t0 = t0c + cs.j * tt;
-    const int cnt = min(tt, t1c - t0);
-    const int nsub = (cnt + kTsub - 1) / kTsub;
-
-    if (cs.lvl == 0) {
-      // ---- level 1: walk the tile forward, keeping every sub-chunk's start state ----------
-      if (cs.j == 0) {
-        const float* src = a.ckpt + (((long)b * a.nch_b + cs.ck) * p.HP + ch) * N + l.n0;
-#pragma unroll
-        for (int j = 0; j < kBwdNS; j++) hs[j] = src[j];
-      }
-      for (int k = 0; k < nsub; k++) {
-        bnd[(cs.j * sub_per_tile + k) * kScanThreads + tid] = make_float4(hs[0], hs[1], hs[2], hs[3]);
-        const int i1 = min(cnt, (k + 1) * kTsub);
-        for (int i = k * kTsub; i < i1; i++) {
-          float dl = lds_f(sdt + i * CB + cl);
-          if (p.softplus) dl = softplusf_(dl + bias);
-          const float dx = dl * lds_f(sx + i * CB + cl);
-          float Bv[kBwdNS];
-          lds4(sB + i * N + l.n0, Bv);
-#pragma unroll
-          for (int j = 0; j < kBwdNS; j++)
-            hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
-        }
-      }
-      __syncthreads();  // stage fully read
-      if (tid == 0 && pp.ck >= c_first) issue();
-      continue;
-    }
-
-    // ---- level 2: sub-chunks last to first: recompute 8 tokens, then the adjoint over them --
-    IO* out = reinterpret_cast<IO*>(smem + m.off_out + (n_l2 & 1) * m.out_stride);
-    IO* odx = out;
-    IO* odz = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + m.out_tile);
-    IO* oddt = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + 2 * m.out_tile);
-    for (int k = nsub - 1; k >= 0; k--) {
-      const int i0 = k * kTsub;
-      const int c8 = min(kTsub, cnt - i0);
-      float hh[kTsub + 1][kBwdNS], aa[kTsub][kBwdNS], dls[kTsub], xs[kTsub], pres[kTsub];
-      {
-        const float4 v = bnd[(cs.j * sub_per_tile + k) * kScanThreads + tid];
-        hh[0][0] = v.x; hh[0][1] = v.y; hh[0][2] = v.z; hh[0][3] = v.w;
-      }
-#pragma unroll
-      for (int r = 0; r < kTsub; r++) {
-        if (r < c8) {
-          const int i = i0 + r;
-          const float raw = lds_f(sdt + i * CB + cl);
-          const float pre = raw + bias;
-          const float dl = p.softplus ? softplusf_(pre) : raw;
-          const float xv = lds_f(sx + i * CB + cl);
-          float Bv[kBwdNS];
-          lds4(sB + i * N + l.n0, Bv);
-          const float dx = dl * xv;
-#pragma unroll
-          for (int j = 0; j < kBwdNS; j++) {
-            aa[r][j] = decay_coef<ACC>(dl, A2[j]);
-            hh[r + 1][j] = decay_step<ACC>(aa[r][j], hh[r][j], dx * Bv[j]);
-          }
-          dls[r] = dl; xs[r] = xv; pres[r] = pre;
-        } else {
-#pragma unroll
-          for (int j = 0; j < kBwdNS; j++) { aa[r][j] = ACC ? 0.0f : 1.0f; hh[r + 1][j] = hh[r][j]; }
-          dls[r] = 0.0f; xs[r] = 0.0f; pres[r] = 0.0f;
-        }
-      }
-#pragma unroll
-      for (int r = kTsub - 1; r >= 0; r--) {
-        if (r < c8) {  // uniform over the block
-          const int i = i0 + r;
-          float Bv[kBwdNS], Cv[kBwdNS];
-          lds4(sB + i * N + l.n0, Bv);
-          lds4(sC + i * N + l.n0, Cv);
-          const float dyv = lds_f(sdy + i * CB + cl);
-          float gy = dyv, ypre = 0.0f, zv = 0.0f;
-          if (p.z) {
-            float part = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kBwdNS; j++) part = fmaf(Cv[j], hh[r + 1][j], part);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            ypre = fmaf(Dv, xs[r], part);
-            zv = lds_f(sz + i * CB + cl);
-            gy = dyv * siluf_(zv);
-          }
-          const float dlx = dls[r] * xs[r];
-          float sB = 0.0f, sAw = 0.0f, v8[8];
-#pragma unroll
-          for (int j = 0; j < kBwdNS; j++) {
-            const float dh = fmaf(gy, Cv[j], carry[j]);
-            v8[4 + j] = gy * hh[r + 1][j];          // dC partial
-            sB = fmaf(dh, Bv[j], sB);
-            v8[j] = dh * dlx;                       // dB partial
-            const float cn = decay_apply<ACC>(aa[r][j], dh);
-            const float w = cn * hh[r][j];
-            sAw = fmaf(An[j], w, sAw);
-            dA_acc[j] = fmaf(dls[r], w, dA_acc[j]);
-            carry[j] = cn;
-          }
-          sB += __shfl_xor_sync(0xffffffffu, sB, 1);
-          sAw += __shfl_xor_sync(0xffffffffu, sAw, 1);
-          sB += __shfl_xor_sync(0xffffffffu, sB, 2);
-          sAw += __shfl_xor_sync(0xffffffffu, sAw, 2);
-          const float dxv = fmaf(gy, Dv, dls[r] * sB);
-          const float ddl = fmaf(xs[r], sB, sAw);
-          const float ddt = p.softplus ? ddl * softplus_gradf_(pres[r]) : ddl;
-          dD_acc = fmaf(gy, xs[r], dD_acc);
-          if (l.sg == 0) {
-            sts_f(odx + i * CB + cl, dxv);
-            if (p.z) sts_f(odz + i * CB + cl, dyv * ypre * silu_gradf_(zv));
-            sts_f(oddt + i * CB + cl, ddt);
-            dtb_acc += ddt;
-          }
-          const float tot = reduce8_transposed(v8, lane);
-          const int o = (lane >> 2) & 7;  // 0..3: dB of state n0+o, 4..7: dC of state n0+o-4
-          red[(i * kWarps + warp) * 2 * N + (o >> 2) * N + l.n0 + (o & 3)] = tot;
-        }
-      }
-    }
-    fence_async_shared();
-    __syncthreads();  // stage read, out tiles and red complete
-    for (int idx = tid; idx < cnt * 2 * N; idx += kScanThreads) {
-      const int i = idx / (2 * N), r = idx - i * 2 * N;
-      float v = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
-      const long tok = (long)b * p.L + t0 + i;
-      a.part_bc[((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r] = v;
-    }
-    if (tid == 0) {
-      tma_store_3d(&m.mdx, odx, ch0, t0, b);
-      if (p.z && a.g.d_z) tma_store_3d(&m.mdz, odz, ch0, t0, b);
-      tma_store_3d(&m.mddt, oddt, ch0, t0, b);
-      tma_store_commit();
-      if (pp.ck >= c_first) issue();
-    }
-    n_l2++;
-  }
-  if (tid == 0) tma_store_wait_all();
-
-  const long si = ((long)b * a.S + s) * p.HP + ch;
-#pragma unroll
-  for (int j = 0; j < kBwdNS; j++) {
-    a.dA_part[si * N + l.n0 + j] = dA_acc[j];
-    if (s == 0) a.dh0[((long)b * p.HP + ch) * N + l.n0 + j] = carry[j];
-  }
-  if (l.sg == 0) {
-    a.dD_part[si] = dD_acc;
-    a.dtb_part[si] = dtb_acc;
-  }
-}
-
 // ---- host side -------------------------------------------------------------------------
-struct BwdPlan {
-  int tpc, gc, bpg, chunk_b, nch_b, S, seg_chunks;
-  int tma_tt;  // tile tokens of the TMA-staged path; 0 when the shape does not allow it
-  size_t off_fwd, fwd_bytes, off_ckpt, off_dhloc, off_segend, off_sumd, off_part_bc, off_dA,
-      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, bytes, smem;
-};
 
 static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   BwdPlan q{};
@@ -841,10 +451,7 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.off_dtb = take(segch);
   q.off_ddt = take(p.P > 1 ? F * (size_t)p.ns * p.L * p.HP : 0);
   q.off_dh0 = take(F * (size_t)p.ns * p.HP * p.N);
-  const int io = p.io == SSM_BF16 ? 2 : 4;
-  if (p.P == 1 && p.a_per_state && p.N == 16 && q.tpc == 4 && (p.HP * io) % 16 == 0 &&
-      q.gc % (kScanThreads / 4) == 0 && q.chunk_b % kTsub == 0)
-    q.tma_tt = q.chunk_b % 32 == 0 ? 32 : (q.chunk_b % 16 == 0 ? 16 : 8);
+  q.tma_tt = bwd_tma_tile(p, q.chunk_b, q.tpc, q.gc);
   if (q.tma_tt) {
     const size_t blocks = (size_t)p.G * q.bpg * q.S * p.ns;
     q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsub) * kScanThreads);
@@ -866,29 +473,29 @@ static int blocks_for(long total) {
 }
 
 template <typename IO, bool SCALAR_A, bool FULL>
-static cudaError_t launch_bwd_t(const BwdArgs& a, size_t smem, const BwdTma* m, size_t tma_smem,
-                                cudaStream_t st) {
+static cudaError_t launch_bwd_t(const BwdArgs& a, const BwdPlan& q, char* w, cudaStream_t st) {
   const ScanProblem& p = a.p;
   if (a.S > 1) {
-    dim3 g1(p.G * a.bpg, a.S - 1, p.ns);
-    scan_bwd_local_kernel<IO, SCALAR_A, FULL><<<g1, kScanThreads, 0, st>>>(a), count_launches(1);
+    cudaError_t e = q.tma_tt ? launch_bwd_tma_local(a, q, w, st) : cudaErrorNotSupported;
+    if (e == cudaErrorNotSupported) {
+      dim3 g1(p.G * a.bpg, a.S - 1, p.ns);
+      scan_bwd_local_kernel<IO, SCALAR_A, FULL><<<g1, kScanThreads, 0, st>>>(a), count_launches(1);
+    } else if (e != cudaSuccess) {
+      return e;
+    }
     scan_bwd_carry_kernel<<<blocks_for((long)p.ns * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
   }
-  dim3 g2(p.G * a.bpg, a.S, p.ns);
-  if (m) {
-    auto kt = scan_bwd_tma_kernel<IO>;
-    cudaError_t e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tma_smem);
-    if (e != cudaSuccess) return e;
-    kt<<<g2, kScanThreads, tma_smem, st>>>(*m, a), count_launches(1);
-  } else {
+  cudaError_t e = q.tma_tt ? launch_bwd_tma_main(a, q, w, st) : cudaErrorNotSupported;
+  if (e == cudaErrorNotSupported) {
     auto kern = scan_bwd_kernel<IO, SCALAR_A, FULL>;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    if (q.smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q.smem);
       if (e != cudaSuccess) return e;
     }
-    kern<<<g2, kScanThreads, smem, st>>>(a), count_launches(1);
+    dim3 g2(p.G * a.bpg, a.S, p.ns);
+    kern<<<g2, kScanThreads, q.smem, st>>>(a), count_launches(1);
+  } else if (e != cudaSuccess) {
+    return e;
   }
   reduce_bc_kernel<IO><<<blocks_for((long)p.ns * p.L * p.G * 2 * p.N), 256, 0, st>>>(a), count_launches(1);
   const long nparams = (long)(p.a_per_state ? p.H * p.N : p.H) + p.HP + p.H;
@@ -903,58 +510,11 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, size_t smem, const BwdTma* m, 
 }
 
 template <typename IO>
-static cudaError_t launch_bwd_io(const BwdArgs& a, size_t smem, bool full, const BwdTma* m,
-                                 size_t tma_smem, cudaStream_t st) {
+static cudaError_t launch_bwd_io(const BwdArgs& a, const BwdPlan& q, bool full, char* w,
+                                 cudaStream_t st) {
   if (!a.p.a_per_state)
-    return full ? launch_bwd_t<IO, true, true>(a, smem, nullptr, 0, st)
-                : launch_bwd_t<IO, true, false>(a, smem, nullptr, 0, st);
-  return full ? launch_bwd_t<IO, false, true>(a, smem, m, tma_smem, st)
-              : launch_bwd_t<IO, false, false>(a, smem, nullptr, 0, st);
-}
-
-static bool al16(const void* v) { return ((uintptr_t)v & 15) == 0; }
-
-// Tensor maps and shared-memory layout of the TMA-staged backward; false if not applicable.
-static bool setup_bwd_tma(const ScanProblem& p, const ScanGrads& g, const BwdPlan& q, char* w,
-                          BwdTma* m, size_t* smem) {
-  if (!q.tma_tt) return false;
-  if (!al16(p.x) || !al16(p.dt) || !al16(p.B) || !al16(p.C) || !al16(g.dy) || !al16(g.d_x) ||
-      !al16(g.d_dt) || (p.z && !al16(p.z)) || (g.d_z && !al16(g.d_z)))
-    return false;
-  const int io = p.io == SSM_BF16 ? 2 : 4;
-  const int tt = q.tma_tt, cb = kScanThreads / 4;
-  const uint64_t C = p.HP, L = p.L, NSq = p.ns, GN = (uint64_t)p.G * p.N;
-  memset(m, 0, sizeof(*m));
-  bool ok = encode_tmap_3d(&m->mx, p.x, io, C, L, NSq, C, C * L, cb, tt, 1) &&
-            encode_tmap_3d(&m->mdt, p.dt, io, C, L, NSq, C, C * L, cb, tt, 1) &&
-            encode_tmap_3d(&m->mdy, g.dy, io, C, L, NSq, C, C * L, cb, tt, 1) &&
-            encode_tmap_3d(&m->mb, p.B, io, GN, L, NSq, GN, GN * L, p.N, tt, 1) &&
-            encode_tmap_3d(&m->mc, p.C, io, GN, L, NSq, GN, GN * L, p.N, tt, 1) &&
-            encode_tmap_3d(&m->mdx, g.d_x, io, C, L, NSq, C, C * L, cb, tt, 1) &&
-            encode_tmap_3d(&m->mddt, g.d_dt, io, C, L, NSq, C, C * L, cb, tt, 1);
-  if (ok && p.z) ok = encode_tmap_3d(&m->mz, p.z, io, C, L, NSq, C, C * L, cb, tt, 1);
-  if (ok && g.d_z) ok = encode_tmap_3d(&m->mdz, g.d_z, io, C, L, NSq, C, C * L, cb, tt, 1);
-  if (!ok) return false;
-  auto al = [](uint32_t v) { return (v + 127u) & ~127u; };
-  const uint32_t tile = (uint32_t)(tt * cb * io), row = (uint32_t)(tt * p.N * io);
-  m->tt = tt;
-  m->off_x = 0;
-  m->off_dt = al(tile);
-  m->off_z = m->off_dt + al(tile);
-  m->off_dy = m->off_z + al(tile);
-  m->off_b = m->off_dy + al(tile);
-  m->off_c = m->off_b + al(row);
-  m->stage_stride = m->off_c + al(row);
-  m->off_out = kBwdStages * m->stage_stride;
-  m->out_tile = al(tile);
-  m->out_stride = 3 * m->out_tile;
-  m->off_red = m->off_out + 2 * m->out_stride;
-  m->off_bar = m->off_red + al((uint32_t)(sizeof(float) * tt * (kScanThreads / 32) * 2 * p.N));
-  m->bytes_l1 = 2 * tile + row;
-  m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
-  m->bnd = reinterpret_cast<float4*>(w + q.off_bnd);
-  *smem = m->off_bar + 64;
-  return true;
+    return full ? launch_bwd_t<IO, true, true>(a, q, w, st) : launch_bwd_t<IO, true, false>(a, q, w, st);
+  return full ? launch_bwd_t<IO, false, true>(a, q, w, st) : launch_bwd_t<IO, false, false>(a, q, w, st);
 }
 
 cudaError_t launch_scan_bwd(const ScanProblem& p, const float* ckpt, const ScanGrads& g, void* ws,
@@ -991,12 +551,8 @@ cudaError_t launch_scan_bwd(const ScanProblem& p, const float* ckpt, const ScanG
   a.ddt_part = (float*)(w + q.off_ddt);
   a.dh0 = (float*)(w + q.off_dh0);
   const bool full = rows_vectorizable(p, kBwdNS, q.tpc);
-  BwdTma m;
-  size_t tma_smem = 0;
-  const bool tma = setup_bwd_tma(p, g, q, w, &m, &tma_smem);
-  return p.io == SSM_BF16
-             ? launch_bwd_io<__nv_bfloat16>(a, q.smem, full, tma ? &m : nullptr, tma_smem, st)
-             : launch_bwd_io<float>(a, q.smem, full, tma ? &m : nullptr, tma_smem, st);
+  return p.io == SSM_BF16 ? launch_bwd_io<__nv_bfloat16>(a, q, full, w, st)
+                          : launch_bwd_io<float>(a, q, full, w, st);
 }
 
 }  // namespace ssm

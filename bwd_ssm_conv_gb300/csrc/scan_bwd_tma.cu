@@ -1,0 +1,614 @@
+// scan_bwd_tma.cu -- TMA-staged backward scan for the Mamba-1 layout with d_state 16
+// (head_dim 1, rows 16-byte aligned, checkpoint interval a multiple of 16).
+//
+// Same arithmetic and workspace outputs as the general kernels in scan_bwd.cu.  A block =
+// 128 threads = 32 channels x 16 states (4 threads of 4 states per channel), one sequence,
+// one time segment.  Inputs arrive as [16 tokens][32 channels] tiles (x, dt, z, dy) and
+// [16 tokens][16] tiles (B, C) through a 3-stage ring filled by cp.async.bulk.tensor; dx,
+// dz, ddt leave as TMA-stored tiles.  Per tile, work that depends only on (token, channel)
+// -- delta, the gate, dy silu'(z), softplus' -- is done once by the whole block in a
+// prepass, so the per-state loops carry only the recurrence (packed f32x2 arithmetic);
+// the per-channel sums over states go through shared memory to an epilogue that writes
+// dx, dz and ddt, and the dB/dC sums over channels use a transposed warp butterfly.
+//
+// Per chunk (last to first): level 1 walks the chunk's tiles forward from the checkpoint,
+// saving the state at every 8-token sub-chunk start (global scratch, re-read from L2);
+// level 2 walks the tiles in reverse, recomputes each sub-chunk's 8 states and decays in
+// registers and runs the adjoint over them.
+#include "scan_bwd.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+
+constexpr int kBwdStages = 3;
+constexpr int kBwdTile = 16;                  // tokens per staged tile (two sub-chunks)
+constexpr int kCB = kScanThreads / 4;         // channels per block
+constexpr int kWarps = kScanThreads / 32;
+
+struct BwdTma {
+  CUtensorMap mx, mdt, mz, mdy, mb, mc, mdx, mdz, mddt;
+  uint32_t bytes_l1, bytes_l2, bytes_loc;
+  uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
+  uint32_t off_p, off_spg, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
+  uint32_t off_par, off_acc, off_bar, smem;
+  float4* bnd;
+};
+
+int bwd_tma_tile(const ScanProblem& p, int chunk_b, int tpc, int gc) {
+  const int io = p.io == SSM_BF16 ? 2 : 4;
+  if (p.P == 1 && p.a_per_state && p.N == 16 && tpc == 4 && (p.HP * io) % 16 == 0 &&
+      gc % kCB == 0 && chunk_b % kBwdTile == 0)
+    return kBwdTile;
+  return 0;
+}
+
+template <typename IO>
+__device__ __forceinline__ float lds_f(const IO* p) {
+  if constexpr (sizeof(IO) == 4) return *reinterpret_cast<const float*>(p);
+  else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+}
+template <typename IO>
+__device__ __forceinline__ void sts_f(IO* p, float v) {
+  if constexpr (sizeof(IO) == 4) *reinterpret_cast<float*>(p) = v;
+  else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+}
+
+// Packed decay for a pair of states: the coefficient and the two uses of it (see
+// scan_common.cuh for the fast and the accurate forms).
+template <bool ACC>
+__device__ __forceinline__ f2_t decay2(f2_t dl2, f2_t A2p) {
+  if constexpr (!ACC) return f2_ex2(f2_mul(dl2, A2p));
+  float dl, d2, a0, a1;
+  f2_unpack(dl2, dl, d2);
+  f2_unpack(A2p, a0, a1);
+  return f2_pack(decay_coef<true>(dl, a0), decay_coef<true>(dl, a1));
+}
+template <bool ACC>
+__device__ __forceinline__ f2_t step2(f2_t coef, f2_t h, f2_t u) {
+  return ACC ? f2_add(h, f2_fma(coef, h, u)) : f2_fma(coef, h, u);
+}
+template <bool ACC>
+__device__ __forceinline__ f2_t apply2(f2_t coef, f2_t v) {
+  return ACC ? f2_fma(coef, v, v) : f2_mul(coef, v);
+}
+__device__ __forceinline__ float f2_sum(f2_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return lo + hi;
+}
+
+// v holds 8 partials; lanes that differ in bits 2..4 hold other channels.  Returns the sum over
+// those 8 lanes of the partial with original index (lane >> 2) & 7.
+__device__ __forceinline__ float reduce8_transposed(float (&v)[8], int lane) {
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  const bool up = lane & 4;
+  const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 4);
+}
+
+// B (and C) of a tile as fp32: the staged tile itself for fp32 I/O, else converted once.
+template <typename IO>
+__device__ __forceinline__ const float* tile_rows_f32(const unsigned char* stage_rows, float* conv,
+                                                      int count) {
+  if constexpr (sizeof(IO) == 4) {
+    (void)conv; (void)count;
+    return reinterpret_cast<const float*>(stage_rows);
+  } else {
+    const IO* src = reinterpret_cast<const IO*>(stage_rows);
+    for (int idx = threadIdx.x; idx < count; idx += kScanThreads) conv[idx] = lds_f(src + idx);
+    return conv;
+  }
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kScanThreads)
+scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;
+  constexpr int TT = kBwdTile, CB = kCB, N = 16;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const ScanProblem& p = a.p;
+  const Lane l = lane_of(a);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
+  const int s = blockIdx.y, b = blockIdx.z;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
+  float4* sP = reinterpret_cast<float4*>(smem + m.off_p);        // [TT][CB] (delta, x, gy, dyg)
+  float* sSPG = reinterpret_cast<float*>(smem + m.off_spg);      // [TT][CB] softplus'(pre)
+  float4* sPart = reinterpret_cast<float4*>(smem + m.off_part);  // [TT][threads] (sB, sAw, ypre)
+  float* red = reinterpret_cast<float*>(smem + m.off_red);       // [TT][warps][2N]
+  float* sPar = reinterpret_cast<float*>(smem + m.off_par);      // D[CB], dt_bias[CB]
+  float* sAcc = reinterpret_cast<float*>(smem + m.off_acc);      // [warps][CB][2]
+  const int nsub_max = a.chunk_b / kTsub;
+  float4* bnd = m.bnd + ((long)(b * a.S + s) * gridDim.x + blockIdx.x) * nsub_max * kScanThreads;
+  const int c_first = s * a.seg_chunks;
+  const int c_last = min(a.nch_b, c_first + a.seg_chunks) - 1;
+
+  // Tile schedule: per chunk (last to first), level-1 tiles ascending then level-2 tiles
+  // descending.  Thread 0 (producer) and every thread (consumer) walk it with own cursors.
+  struct Pos { int ck, lvl, j, nt; };
+  auto ntiles = [&](int ck) {
+    const int t0 = ck * a.chunk_b, t1 = min(p.L, t0 + a.chunk_b);
+    return (t1 - t0 + TT - 1) / TT;
+  };
+  auto first = [&]() { Pos q; q.ck = c_last; q.lvl = 0; q.j = 0; q.nt = ntiles(c_last); return q; };
+  auto advance = [&](Pos& q) {
+    if (q.lvl == 0) {
+      if (++q.j == q.nt) { q.lvl = 1; q.j = q.nt - 1; }
+    } else if (--q.j < 0) {
+      q.ck--; q.lvl = 0; q.j = 0;
+      if (q.ck >= c_first) q.nt = ntiles(q.ck);
+    }
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  for (int c = tid; c < CB; c += kScanThreads) {
+    sPar[c] = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
+    sPar[CB + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
+  }
+  __syncthreads();
+  Pos pp = first();
+  int issued = 0;
+  auto issue = [&]() {  // thread 0 only
+    const int stg = issued % kBwdStages;
+    unsigned char* base = smem + stg * m.stage_stride;
+    const int t0 = pp.ck * a.chunk_b + pp.j * TT;
+    if (pp.lvl == 0) {
+      mbar_expect_tx(&full[stg], m.bytes_l1);
+      tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
+    } else {
+      mbar_expect_tx(&full[stg], m.bytes_l2);
+      tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_dy, &m.mdy, ch0, t0, b, &full[stg]);
+      if (p.z) tma_load_3d(base + m.off_z, &m.mz, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
+      tma_load_3d(base + m.off_c, &m.mc, l.g * N, t0, b, &full[stg]);
+    }
+    issued++;
+    advance(pp);
+  };
+  if (tid == 0)
+    for (int k = 0; k < kBwdStages && pp.ck >= c_first; k++) issue();
+
+  f2_t A2p[2], Anp[2], carry2[2], dA2[2] = {0ull, 0ull}, hp[2] = {0ull, 0ull};
+  {
+    const long si = ((long)b * a.S + s) * p.HP + ch;
+    float cv[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      if (a.S > 1) cv[j] = a.segend[si * N + n0 + j];
+      else cv[j] = a.g.d_state_out ? __ldg(a.g.d_state_out + ((long)b * p.HP + ch) * N + n0 + j) : 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      const float a0 = __ldg(p.A + (long)ch * N + n0 + 2 * q), a1 = __ldg(p.A + (long)ch * N + n0 + 2 * q + 1);
+      Anp[q] = f2_pack(a0, a1);
+      A2p[q] = f2_pack(a0 * kLog2e, a1 * kLog2e);
+      carry2[q] = f2_pack(cv[2 * q], cv[2 * q + 1]);
+    }
+  }
+  float dD_acc = 0.0f, dtb_acc = 0.0f;  // of channel tid % CB, over this thread's epilogue items
+  int n_l2 = 0;
+
+  int qpos = 0;
+  for (Pos cs = first(); cs.ck >= c_first; advance(cs), qpos++) {
+    const int stg = qpos % kBwdStages;
+    if (cs.lvl == 1 && tid == 0) tma_store_wait_read<1>();  // out buffer (n_l2 & 1) is free
+    const bool ok = mbar_wait(&full[stg], (uint32_t)(qpos / kBwdStages) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        record_status(p.status, SSM_ERR_TIMEOUT);
+        for (int j = qpos; j < issued; j++) mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
+        tma_store_wait_all();
+      }
+      return;
+    }
+    const unsigned char* base = smem + stg * m.stage_stride;
+    const IO* sx = reinterpret_cast<const IO*>(base + m.off_x);
+    const IO* sdt = reinterpret_cast<const IO*>(base + m.off_dt);
+    const IO* sz = reinterpret_cast<const IO*>(base + m.off_z);
+    const IO* sdy = reinterpret_cast<const IO*>(base + m.off_dy);
+    const int t0c = cs.ck * a.chunk_b, t1c = min(p.L, t0c + a.chunk_b);
+    const int t0 = t0c + cs.j * TT;
+    const int cnt = min(TT, t1c - t0);
+
+    // ---- prepass, once per (token, channel) -----------------------------------------------
+    for (int idx = tid; idx < TT * CB; idx += kScanThreads) {
+      const int c = idx % CB;
+      const float raw = lds_f(sdt + idx);
+      const float pre = raw + sPar[CB + c];
+      const float dl = p.softplus ? softplusf_(pre) : raw;
+      const float xv = lds_f(sx + idx);
+      float gy = 0.0f, dyg = 0.0f;
+      if (cs.lvl == 1) {
+        const float dyv = lds_f(sdy + idx);
+        gy = dyv;
+        if (p.z) {
+          const float zv = lds_f(sz + idx), sgm = sigmoidf_(zv);
+          gy = dyv * zv * sgm;
+          dyg = dyv * sgm * (1.0f + zv * (1.0f - sgm));
+        }
+        if (p.softplus) sSPG[idx] = softplus_gradf_(pre);
+      }
+      sP[idx] = make_float4(dl, xv, gy, dyg);
+    }
+    const float* sBf = tile_rows_f32<IO>(base + m.off_b, reinterpret_cast<float*>(smem + m.off_bf), TT * N);
+    const float* sCf = cs.lvl == 1
+        ? tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N)
+        : nullptr;
+    __syncthreads();
+
+    if (cs.lvl == 0) {
+      // ---- level 1: walk the tile forward, keeping every sub-chunk's start state ----------
+      if (cs.j == 0) {
+        const float* src = a.ckpt + (((long)b * a.nch_b + cs.ck) * p.HP + ch) * N + n0;
+        hp[0] = f2_pack(src[0], src[1]);
+        hp[1] = f2_pack(src[2], src[3]);
+      }
+#pragma unroll
+      for (int i = 0; i < TT; i++) {
+        if (i < cnt) {
+          if (i % kTsub == 0) {
+            float h0, h1, h2, h3;
+            f2_unpack(hp[0], h0, h1);
+            f2_unpack(hp[1], h2, h3);
+            bnd[(cs.j * (TT / kTsub) + i / kTsub) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
+          }
+          const float4 p4 = sP[i * CB + cl];
+          const f2_t dl2 = f2_pack(p4.x, p4.x);
+          const float dx = p4.x * p4.y;
+          const f2_t dx2 = f2_pack(dx, dx);
+          const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
+          hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
+          hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+        }
+      }
+      __syncthreads();  // stage fully read
+      if (tid == 0 && pp.ck >= c_first) issue();
+      continue;
+    }
+
+    // ---- level 2: sub-chunks last to first: recompute 8 states, then the adjoint ------------
+    const int nsub = (cnt + kTsub - 1) / kTsub;
+    for (int k = nsub - 1; k >= 0; k--) {
+      const int i0 = k * kTsub;
+      const int c8 = min(kTsub, cnt - i0);
+      f2_t hh[kTsub + 1][2], aa[kTsub][2];
+      {
+        const float4 v = bnd[(cs.j * (TT / kTsub) + k) * kScanThreads + tid];
+        hh[0][0] = f2_pack(v.x, v.y);
+        hh[0][1] = f2_pack(v.z, v.w);
+      }
+#pragma unroll
+      for (int r = 0; r < kTsub; r++) {
+        if (r < c8) {
+          const float4 p4 = sP[(i0 + r) * CB + cl];
+          const f2_t dl2 = f2_pack(p4.x, p4.x);
+          const float dx = p4.x * p4.y;
+          const f2_t dx2 = f2_pack(dx, dx);
+          const float4 bv = *reinterpret_cast<const float4*>(sBf + (i0 + r) * N + n0);
+          aa[r][0] = decay2<ACC>(dl2, A2p[0]);
+          aa[r][1] = decay2<ACC>(dl2, A2p[1]);
+          hh[r + 1][0] = step2<ACC>(aa[r][0], hh[r][0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
+          hh[r + 1][1] = step2<ACC>(aa[r][1], hh[r][1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+        } else {
+          aa[r][0] = aa[r][1] = 0ull;
+          hh[r + 1][0] = hh[r][0];
+          hh[r + 1][1] = hh[r][1];
+        }
+      }
+#pragma unroll
+      for (int r = kTsub - 1; r >= 0; r--) {
+        if (r < c8) {  // uniform over the block
+          const int i = i0 + r;
+          const float4 p4 = sP[i * CB + cl];
+          const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.z, p4.z);
+          const float dlx = p4.x * p4.y;
+          const f2_t dlx2 = f2_pack(dlx, dlx);
+          const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
+          const float4 cv = *reinterpret_cast<const float4*>(sCf + i * N + n0);
+          const f2_t B2[2] = {f2_pack(bv.x, bv.y), f2_pack(bv.z, bv.w)};
+          const f2_t C2[2] = {f2_pack(cv.x, cv.y), f2_pack(cv.z, cv.w)};
+          f2_t sB2 = 0ull, sAw2 = 0ull, yp2 = 0ull, dB2[2], dC2[2];
+#pragma unroll
+          for (int q = 0; q < 2; q++) {
+            const f2_t dh2 = f2_fma(gy2, C2[q], carry2[q]);
+            dC2[q] = f2_mul(gy2, hh[r + 1][q]);
+            sB2 = f2_fma(dh2, B2[q], sB2);
+            dB2[q] = f2_mul(dh2, dlx2);
+            const f2_t cn2 = apply2<ACC>(aa[r][q], dh2);
+            const f2_t w2 = f2_mul(cn2, hh[r][q]);
+            sAw2 = f2_fma(Anp[q], w2, sAw2);
+            dA2[q] = f2_fma(dl2, w2, dA2[q]);
+            yp2 = f2_fma(C2[q], hh[r + 1][q], yp2);
+            carry2[q] = cn2;
+          }
+          sPart[i * kScanThreads + tid] = make_float4(f2_sum(sB2), f2_sum(sAw2), f2_sum(yp2), 0.0f);
+          float v8[8];
+          f2_unpack(dB2[0], v8[0], v8[1]);
+          f2_unpack(dB2[1], v8[2], v8[3]);
+          f2_unpack(dC2[0], v8[4], v8[5]);
+          f2_unpack(dC2[1], v8[6], v8[7]);
+          const float tot = reduce8_transposed(v8, lane);
+          const int o = (lane >> 2) & 7;  // 0..3: dB of state n0+o, 4..7: dC of state n0+o-4
+          red[(i * kWarps + warp) * 2 * N + (o >> 2) * N + n0 + (o & 3)] = tot;
+        }
+      }
+    }
+    __syncthreads();  // sPart and red complete
+
+    // ---- epilogue, once per (token, channel): dx, dz, ddt; dD and d dt_bias partials --------
+    IO* out = reinterpret_cast<IO*>(smem + m.off_out + (n_l2 & 1) * m.out_stride);
+    IO* odx = out;
+    IO* odz = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + m.out_tile);
+    IO* oddt = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + 2 * m.out_tile);
+    for (int idx = tid; idx < cnt * CB; idx += kScanThreads) {
+      const int i = idx / CB, c = idx - i * CB;  // c == tid % CB for every item of this thread
+      const float4* pp4 = sPart + i * kScanThreads + c * 4;
+      const float4 q0 = pp4[0], q1 = pp4[1], q2 = pp4[2], q3 = pp4[3];
+      const float sBt = (q0.x + q1.x) + (q2.x + q3.x);
+      const float sAwt = (q0.y + q1.y) + (q2.y + q3.y);
+      const float ypt = (q0.z + q1.z) + (q2.z + q3.z);
+      const float4 p4 = sP[idx];
+      const float D = sPar[c];
+      const float ddl = fmaf(p4.y, sBt, sAwt);
+      const float ddt = p.softplus ? ddl * sSPG[idx] : ddl;
+      sts_f(odx + idx, fmaf(p4.z, D, p4.x * sBt));
+      sts_f(odz + idx, p4.w * fmaf(D, p4.y, ypt));
+      sts_f(oddt + idx, ddt);
+      dD_acc = fmaf(p4.z, p4.y, dD_acc);
+      dtb_acc += ddt;
+    }
+    for (int idx = tid; idx < cnt * 2 * N; idx += kScanThreads) {
+      const int i = idx / (2 * N), r = idx - i * 2 * N;
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
+      const long tok = (long)b * p.L + t0 + i;
+      a.part_bc[((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r] = v;
+    }
+    fence_async_shared();
+    __syncthreads();  // out tiles complete; stage fully read
+    if (tid == 0) {
+      tma_store_3d(&m.mdx, odx, ch0, t0, b);
+      if (p.z && a.g.d_z) tma_store_3d(&m.mdz, odz, ch0, t0, b);
+      tma_store_3d(&m.mddt, oddt, ch0, t0, b);
+      tma_store_commit();
+      if (pp.ck >= c_first) issue();
+    }
+    n_l2++;
+  }
+  if (tid == 0) tma_store_wait_all();
+
+  const long si = ((long)b * a.S + s) * p.HP + ch;
+#pragma unroll
+  for (int q = 0; q < 2; q++) {
+    f2_unpack(dA2[q], a.dA_part[si * N + n0 + 2 * q], a.dA_part[si * N + n0 + 2 * q + 1]);
+    if (s == 0)
+      f2_unpack(carry2[q], a.dh0[((long)b * p.HP + ch) * N + n0 + 2 * q],
+                a.dh0[((long)b * p.HP + ch) * N + n0 + 2 * q + 1]);
+  }
+  sAcc[(warp * CB + (tid % CB)) * 2] = dD_acc;
+  sAcc[(warp * CB + (tid % CB)) * 2 + 1] = dtb_acc;
+  __syncthreads();
+  if (tid < CB) {
+    float vD = 0.0f, vT = 0.0f;
+    for (int w = 0; w < kWarps; w++) {
+      vD += sAcc[(w * CB + tid) * 2];
+      vT += sAcc[(w * CB + tid) * 2 + 1];
+    }
+    const long sc = ((long)b * a.S + s) * p.HP + ch0 + tid;
+    a.dD_part[sc] = vD;
+    a.dtb_part[sc] = vT;
+  }
+}
+
+// Local adjoint of segments 1..S-1 (zero adjoint at the segment end), tiles in reverse.
+template <typename IO>
+__global__ void __launch_bounds__(kScanThreads)
+scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;
+  constexpr int TT = kBwdTile, CB = kCB, N = 16;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const ScanProblem& p = a.p;
+  const Lane l = lane_of(a);
+  const int tid = threadIdx.x;
+  const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
+  const int s = blockIdx.y + 1, b = blockIdx.z;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
+  float4* sP = reinterpret_cast<float4*>(smem + m.off_p);
+  float* sPar = reinterpret_cast<float*>(smem + m.off_par);
+  const int t_begin = s * a.seg_chunks * a.chunk_b;
+  const int t_end = min(p.L, t_begin + a.seg_chunks * a.chunk_b);
+  const int nt = (t_end - t_begin + TT - 1) / TT;
+
+  if (tid == 0) {
+    for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  for (int c = tid; c < CB; c += kScanThreads)
+    sPar[CB + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
+  __syncthreads();
+  auto issue = [&](int k) {  // tile nt-1-k (reverse order) -> stage k % stages
+    const int stg = k % kBwdStages;
+    unsigned char* base = smem + stg * m.stage_stride;
+    const int t0 = t_begin + (nt - 1 - k) * TT;
+    mbar_expect_tx(&full[stg], m.bytes_loc);
+    tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + m.off_dy, &m.mdy, ch0, t0, b, &full[stg]);
+    if (p.z) tma_load_3d(base + m.off_z, &m.mz, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + m.off_c, &m.mc, l.g * N, t0, b, &full[stg]);
+  };
+  if (tid == 0)
+    for (int k = 0; k < kBwdStages && k < nt; k++) issue(k);
+
+  f2_t A2p[2], c2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int q = 0; q < 2; q++)
+    A2p[q] = f2_pack(__ldg(p.A + (long)ch * N + n0 + 2 * q) * kLog2e,
+                     __ldg(p.A + (long)ch * N + n0 + 2 * q + 1) * kLog2e);
+  float sumd = 0.0f;
+  for (int k = 0; k < nt; k++) {
+    const int stg = k % kBwdStages;
+    const bool ok = mbar_wait(&full[stg], (uint32_t)(k / kBwdStages) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        record_status(p.status, SSM_ERR_TIMEOUT);
+        for (int j = k; j < nt && j < k + kBwdStages; j++)
+          mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
+      }
+      return;
+    }
+    const unsigned char* base = smem + stg * m.stage_stride;
+    const IO* sdt = reinterpret_cast<const IO*>(base + m.off_dt);
+    const IO* sz = reinterpret_cast<const IO*>(base + m.off_z);
+    const IO* sdy = reinterpret_cast<const IO*>(base + m.off_dy);
+    const int t0 = t_begin + (nt - 1 - k) * TT;
+    const int cnt = min(TT, t_end - t0);
+    for (int idx = tid; idx < TT * CB; idx += kScanThreads) {
+      const int c = idx % CB;
+      const float raw = lds_f(sdt + idx);
+      const float dl = p.softplus ? softplusf_(raw + sPar[CB + c]) : raw;
+      float gy = lds_f(sdy + idx);
+      if (p.z) gy *= siluf_(lds_f(sz + idx));
+      sP[idx] = make_float4(dl, 0.0f, gy, 0.0f);
+    }
+    const float* sCf = tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N);
+    __syncthreads();
+#pragma unroll
+    for (int r = TT - 1; r >= 0; r--) {
+      if (r < cnt) {
+        const float4 p4 = sP[r * CB + cl];
+        const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.z, p4.z);
+        const float4 cv = *reinterpret_cast<const float4*>(sCf + r * N + n0);
+        c2[0] = apply2<ACC>(decay2<ACC>(dl2, A2p[0]), f2_fma(gy2, f2_pack(cv.x, cv.y), c2[0]));
+        c2[1] = apply2<ACC>(decay2<ACC>(dl2, A2p[1]), f2_fma(gy2, f2_pack(cv.z, cv.w), c2[1]));
+        sumd += p4.x;
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && k + kBwdStages < nt) issue(k + kBwdStages);
+  }
+  const long si = ((long)b * a.S + s) * p.HP + ch;
+#pragma unroll
+  for (int q = 0; q < 2; q++)
+    f2_unpack(c2[q], a.dhloc[si * N + n0 + 2 * q], a.dhloc[si * N + n0 + 2 * q + 1]);
+  if (l.sg == 0) a.sumd[si] = sumd;
+}
+
+// ---- host --------------------------------------------------------------------------------
+static bool al16(const void* v) { return ((uintptr_t)v & 15) == 0; }
+
+static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m) {
+  const ScanProblem& p = a.p;
+  const ScanGrads& g = a.g;
+  if (!q.tma_tt) return false;
+  if (!al16(p.x) || !al16(p.dt) || !al16(p.B) || !al16(p.C) || !al16(g.dy) || !al16(g.d_x) ||
+      !al16(g.d_dt) || (p.z && !al16(p.z)) || (g.d_z && !al16(g.d_z)))
+    return false;
+  const int io = p.io == SSM_BF16 ? 2 : 4;
+  const int TT = kBwdTile, cb = kCB;
+  const uint64_t C = p.HP, L = p.L, NSq = p.ns, GN = (uint64_t)p.G * p.N;
+  memset(m, 0, sizeof(*m));
+  bool ok = encode_tmap_3d(&m->mx, p.x, io, C, L, NSq, C, C * L, cb, TT, 1) &&
+            encode_tmap_3d(&m->mdt, p.dt, io, C, L, NSq, C, C * L, cb, TT, 1) &&
+            encode_tmap_3d(&m->mdy, g.dy, io, C, L, NSq, C, C * L, cb, TT, 1) &&
+            encode_tmap_3d(&m->mb, p.B, io, GN, L, NSq, GN, GN * L, p.N, TT, 1) &&
+            encode_tmap_3d(&m->mc, p.C, io, GN, L, NSq, GN, GN * L, p.N, TT, 1) &&
+            encode_tmap_3d(&m->mdx, g.d_x, io, C, L, NSq, C, C * L, cb, TT, 1) &&
+            encode_tmap_3d(&m->mddt, g.d_dt, io, C, L, NSq, C, C * L, cb, TT, 1);
+  if (ok && p.z) ok = encode_tmap_3d(&m->mz, p.z, io, C, L, NSq, C, C * L, cb, TT, 1);
+  if (ok && g.d_z) ok = encode_tmap_3d(&m->mdz, g.d_z, io, C, L, NSq, C, C * L, cb, TT, 1);
+  if (!ok) return false;
+  auto al = [](uint32_t v) { return (v + 127u) & ~127u; };
+  const uint32_t tile = (uint32_t)(TT * cb * io), row = (uint32_t)(TT * p.N * io);
+  m->off_x = 0;
+  m->off_dt = al(tile);
+  m->off_z = m->off_dt + al(tile);
+  m->off_dy = m->off_z + al(tile);
+  m->off_b = m->off_dy + al(tile);
+  m->off_c = m->off_b + al(row);
+  m->stage_stride = m->off_c + al(row);
+  uint32_t off = kBwdStages * m->stage_stride;
+  auto take = [&](uint32_t bytes) { uint32_t o = off; off = al(off + bytes); return o; };
+  m->off_p = take(TT * cb * 16);
+  m->off_spg = take(TT * cb * 4);
+  m->off_bf = take(TT * p.N * 4);
+  m->off_cf = take(TT * p.N * 4);
+  m->off_part = take(TT * kScanThreads * 16);
+  m->off_red = take(TT * kWarps * 2 * p.N * 4);
+  m->out_tile = al(tile);
+  m->out_stride = 3 * m->out_tile;
+  m->off_out = take(2 * m->out_stride);
+  m->off_par = take(2 * cb * 4);
+  m->off_acc = take(kWarps * cb * 2 * 4);
+  m->off_bar = take(64);
+  m->smem = off;
+  m->bytes_l1 = 2 * tile + row;
+  m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
+  m->bytes_loc = (2 + (p.z ? 1 : 0)) * tile + row;
+  m->bnd = reinterpret_cast<float4*>(w + q.off_bnd);
+  return true;
+}
+
+cudaError_t launch_bwd_tma_main(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st) {
+  BwdTma m;
+  if (!setup_bwd_tma(a, q, ws, &m)) return cudaErrorNotSupported;
+  const ScanProblem& p = a.p;
+  dim3 grid(p.G * a.bpg, a.S, p.ns);
+  cudaError_t e;
+  if (p.io == SSM_BF16) {
+    auto k = scan_bwd_tma_kernel<__nv_bfloat16>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  } else {
+    auto k = scan_bwd_tma_kernel<float>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st) {
+  BwdTma m;
+  if (!setup_bwd_tma(a, q, ws, &m)) return cudaErrorNotSupported;
+  const ScanProblem& p = a.p;
+  dim3 grid(p.G * a.bpg, a.S - 1, p.ns);
+  cudaError_t e;
+  if (p.io == SSM_BF16) {
+    auto k = scan_bwd_tma_local_kernel<__nv_bfloat16>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  } else {
+    auto k = scan_bwd_tma_local_kernel<float>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

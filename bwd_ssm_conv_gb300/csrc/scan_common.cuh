@@ -8,7 +8,7 @@ namespace ssm {
 
 constexpr int kScanThreads = 128;              // threads per scan block
 constexpr long kFwdTargetThreadsPerSM = 768;   // below this, time segments add parallelism
-constexpr long kBwdTargetThreadsPerSM = 768;
+constexpr long kBwdTargetThreadsPerSM = 512;
 constexpr int kMinSegment = 64;                // shortest time segment worth a block
 
 __host__ inline int pow2_ceil(int v) {

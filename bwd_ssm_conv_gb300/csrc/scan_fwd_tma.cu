@@ -1,5 +1,6 @@
 // scan_fwd_tma.cu -- forward scan with TMA-staged tiles: the fast path for the Mamba-1
-// layout (head_dim 1; channel rows 16-byte aligned).  Other shapes use scan_fwd.cu.
+// layout with bf16 I/O (head_dim 1; channel rows 16-byte aligned; checkpoint interval a
+// multiple of the 16-token tile).  Other shapes and fp32 I/O use scan_fwd.cu.
 //
 // Same arithmetic and segment decomposition as scan_fwd.cu (local aggregate, carry, main),
 // but every block streams its inputs as [tile tokens][block channels] tiles of x, dt, z and
@@ -91,8 +92,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   const uint32_t bytes = LOCAL ? a.bytes_local : a.bytes_main;
   const bool want_y = !LOCAL && a.has_y;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
-  float* sDL = reinterpret_cast<float*>(smem + a.off_dl);    // [TT][cb] delta
-  float* sDX = reinterpret_cast<float*>(smem + a.off_dx);    // [TT][cb] delta * x
+  float4* sDD = reinterpret_cast<float4*>(smem + a.off_dl);  // [TT][cb] (delta, delta, dx, dx)
   float* sACC = reinterpret_cast<float*>(smem + a.off_acc);  // [TT][cb * tpc] partial C . h
   float* sPar = reinterpret_cast<float*>(smem + a.off_par);  // [cb] D, [cb] dt_bias
 
@@ -121,24 +121,21 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   if (tid == 0)
     for (int k = 0; k < kFwdStages && k < ntiles; k++) issue(k);
 
-  float A2[NS];
+  static_assert(!ACC, "the TMA forward path runs the fast decay form (bf16 I/O)");
+  f2_t A2p[NS / 2], hp[NS / 2];
+  {
+    const float* row = nullptr;
+    if (!LOCAL) row = s == 0 ? start_row(p, b) : a.segstart + (((long)b * a.S + s) * p.HP) * N;
 #pragma unroll
-  for (int j = 0; j < NS; j++) A2[j] = __ldg(p.A + (long)ch * N + n0 + j) * kLog2e;
-  float hs[NS];
-  if (LOCAL) {
-#pragma unroll
-    for (int j = 0; j < NS; j++) hs[j] = 0.0f;
-  } else if (s == 0) {
-    const float* row = start_row(p, b);
-#pragma unroll
-    for (int j = 0; j < NS; j++) hs[j] = row ? __ldg(row + (long)ch * N + n0 + j) : 0.0f;
-  } else {
-    const float* src = a.segstart + (((long)b * a.S + s) * p.HP + ch) * N + n0;
-#pragma unroll
-    for (int j = 0; j < NS; j++) hs[j] = src[j];
+    for (int j = 0; j < NS / 2; j++) {
+      A2p[j] = f2_pack(__ldg(p.A + (long)ch * N + n0 + 2 * j) * kLog2e,
+                       __ldg(p.A + (long)ch * N + n0 + 2 * j + 1) * kLog2e);
+      const float h0 = row ? row[(long)ch * N + n0 + 2 * j] : 0.0f;
+      const float h1 = row ? row[(long)ch * N + n0 + 2 * j + 1] : 0.0f;
+      hp[j] = f2_pack(h0, h1);
+    }
   }
   float sumd = 0.0f;
-  int next_ck = (t_begin + p.chunk - 1) / p.chunk * p.chunk;  // next checkpoint token
 
   for (int k = 0; k < ntiles; k++) {
     const int stg = k % kFwdStages;
@@ -165,8 +162,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       const int i = idx / cb, c = idx - i * cb;
       float dl = lds1(sdt + idx);
       if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
-      sDL[idx] = dl;
-      sDX[idx] = dl * lds1(sx + idx);
+      const float dx = dl * lds1(sx + idx);
+      sDD[idx] = make_float4(dl, dl, dx, dx);
       (void)i;
     }
     const float* sBf;
@@ -189,45 +186,48 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     __syncthreads();
 
     // ---- the recurrence: per thread, its channel's NS states over the tile ------------------
-#pragma unroll 2
-    for (int i = 0; i < cnt; i++) {
-      const int t = t0 + i;
-      if (!LOCAL && t == next_ck) {
-        if (a.ckpt) {
-          float* dst = a.ckpt + (((long)b * p.n_chunks + t / p.chunk) * p.HP + ch) * N + n0;
+    if (!LOCAL && a.ckpt && t0 % p.chunk == 0) {  // checkpoints fall on tile starts
+      float* dst = a.ckpt + (((long)b * p.n_chunks + t0 / p.chunk) * p.HP + ch) * N + n0;
 #pragma unroll
-          for (int j = 0; j < NS; j += 4)
-            *reinterpret_cast<float4*>(dst + j) = make_float4(hs[j], hs[j + 1], hs[j + 2], hs[j + 3]);
-        }
-        next_ck += p.chunk;
+      for (int j = 0; j < NS / 2; j += 2) {
+        float x0, x1, x2, x3;
+        f2_unpack(hp[j], x0, x1);
+        f2_unpack(hp[j + 1], x2, x3);
+        *reinterpret_cast<float4*>(dst + 2 * j) = make_float4(x0, x1, x2, x3);
       }
-      const float dl = sDL[i * cb + cl];
-      const float dx = sDX[i * cb + cl];
-      float Bv[NS];
+    }
 #pragma unroll
-      for (int j = 0; j < NS; j += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
-        Bv[j] = v.x; Bv[j + 1] = v.y; Bv[j + 2] = v.z; Bv[j + 3] = v.w;
-      }
-      if (LOCAL) {
-#pragma unroll
-        for (int j = 0; j < NS; j++)
-          hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
-        sumd += dl;
-      } else {
-        float Cv[NS];
+    for (int i = 0; i < TT; i++) {
+      if (i < cnt) {
+        const float4 dd = sDD[i * cb + cl];
+        const f2_t dl2 = f2_pack(dd.x, dd.y), dx2 = f2_pack(dd.z, dd.w);
+        f2_t B2[NS / 2];
 #pragma unroll
         for (int j = 0; j < NS; j += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
-          Cv[j] = v.x; Cv[j + 1] = v.y; Cv[j + 2] = v.z; Cv[j + 3] = v.w;
+          const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
+          B2[j / 2] = f2_pack(v.x, v.y);
+          B2[j / 2 + 1] = f2_pack(v.z, v.w);
         }
-        float acc = 0.0f;
+        if (LOCAL) {
 #pragma unroll
-        for (int j = 0; j < NS; j++) {
-          hs[j] = decay_step<ACC>(decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
-          acc = fmaf(Cv[j], hs[j], acc);
+          for (int j = 0; j < NS / 2; j++)
+            hp[j] = f2_fma(f2_ex2(f2_mul(dl2, A2p[j])), hp[j], f2_mul(dx2, B2[j]));
+          sumd += dd.x;
+        } else {
+          f2_t acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+          for (int j = 0; j < NS; j += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
+            const int q = j / 2;
+            hp[q] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q])), hp[q], f2_mul(dx2, B2[q]));
+            hp[q + 1] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q + 1])), hp[q + 1], f2_mul(dx2, B2[q + 1]));
+            acc0 = f2_fma(f2_pack(v.x, v.y), hp[q], acc0);
+            acc1 = f2_fma(f2_pack(v.z, v.w), hp[q + 1], acc1);
+          }
+          float lo, hi;
+          f2_unpack(f2_add(acc0, acc1), lo, hi);
+          sACC[i * cb * tpc + tid] = lo + hi;
         }
-        sACC[i * cb * tpc + tid] = acc;
       }
     }
     __syncthreads();
@@ -256,15 +256,16 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   }
   if (want_y && tid == 0) tma_store_wait_all();
 
+  float* dst = nullptr;
   if (LOCAL) {
-    float* dst = a.hloc + (((long)b * a.S + s) * p.HP + ch) * N + n0;
-#pragma unroll
-    for (int j = 0; j < NS; j++) dst[j] = hs[j];
+    dst = a.hloc + (((long)b * a.S + s) * p.HP + ch) * N + n0;
     if (sg == 0) a.sumdelta[((long)b * a.S + s) * p.HP + ch] = sumd;
   } else if (s == a.S - 1 && a.state_out) {
-    float* dst = a.state_out + ((long)b * p.HP + ch) * N + n0;
+    dst = a.state_out + ((long)b * p.HP + ch) * N + n0;
+  }
+  if (dst) {
 #pragma unroll
-    for (int j = 0; j < NS; j++) dst[j] = hs[j];
+    for (int j = 0; j < NS / 2; j++) f2_unpack(hp[j], dst[2 * j], dst[2 * j + 1]);
   }
 }
 
@@ -300,7 +301,8 @@ static bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
 static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   FwdTmaPlan q{};
   const int io = p.io == SSM_BF16 ? 2 : 4;
-  if (p.P != 1 || !p.a_per_state || p.N > 256 || (p.N * io) % 16 != 0 || (p.HP * io) % 16 != 0)
+  if (p.io != SSM_BF16 || p.P != 1 || !p.a_per_state || p.N > 256 || (p.N * io) % 16 != 0 ||
+      (p.HP * io) % 16 != 0 || p.chunk % kFwdTile != 0)
     return q;
   // largest states-per-thread that still gives two blocks per SM without time segments
   int ns = 0;
@@ -400,9 +402,9 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_c = a.off_b + al(row);
   a.stage_stride = a.off_c + al(row);
   const uint32_t f_tile = (uint32_t)(q.tt * q.cb * 4), f_row = (uint32_t)(q.tt * p.N * 4);
-  a.off_dl = kFwdStages * a.stage_stride;
-  a.off_dx = a.off_dl + al(f_tile);
-  a.off_bf = a.off_dx + al(f_tile);
+  a.off_dl = kFwdStages * a.stage_stride;         // float4 (delta, delta, dx, dx) per item
+  a.off_dx = a.off_dl + al(4 * f_tile);
+  a.off_bf = a.off_dx;
   a.off_cf = a.off_bf + al(f_row);
   a.off_acc = a.off_cf + al(f_row);
   a.off_par = a.off_acc + al((uint32_t)(q.tt * kScanThreads * 4));
@@ -412,14 +414,10 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   const size_t smem = a.off_bar + 64;
   a.bytes_local = 2 * tile + row;
   a.bytes_main = (2 + (p.z ? 1 : 0)) * tile + 2 * row;
-  const bool bf = p.io == SSM_BF16;
   switch (q.ns_state) {
-    case 16: return bf ? launch_fwd_tma_t<__nv_bfloat16, 16>(a, smem, st)
-                       : launch_fwd_tma_t<float, 16>(a, smem, st);
-    case 8: return bf ? launch_fwd_tma_t<__nv_bfloat16, 8>(a, smem, st)
-                      : launch_fwd_tma_t<float, 8>(a, smem, st);
-    default: return bf ? launch_fwd_tma_t<__nv_bfloat16, 4>(a, smem, st)
-                       : launch_fwd_tma_t<float, 4>(a, smem, st);
+    case 16: return launch_fwd_tma_t<__nv_bfloat16, 16>(a, smem, st);
+    case 8: return launch_fwd_tma_t<__nv_bfloat16, 8>(a, smem, st);
+    default: return launch_fwd_tma_t<__nv_bfloat16, 4>(a, smem, st);
   }
 }
 
