@@ -53,6 +53,17 @@ def alg_bytes(w) -> dict:
             "conv_bwd": conv_bwd}
 
 
+# Algorithmic FP32 flops per (token, channel, state) element of the scan kernels (an FMA counts
+# 2, a multiply 1; the SFU exponentials are counted separately).
+#   forward:  delta*A (1), (delta x)*B (1), h = a h + u (2), y += C h (2)                    = 6
+#   backward: two forward recomputes (4 each, without C h) + the adjoint: dh = gy C + carry (2),
+#             dC += gy h (1), sum dh B (2), dB = dh delta x (1), carry = a dh (1),
+#             w = carry h_prev (1), sum A w (2), dA += delta w (2), y_pre += C h (2)      = 22
+SCAN_FLOPS = {"scan_fwd": 6, "scan_bwd": 22}
+FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (packed f32x2
+                          # issues half the instructions at the same lane rate)
+
+
 def _measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -191,6 +202,20 @@ class Step:
         keys = ["sx", "c"] if self.w.d_conv else ["x"]
         keys += ["dt", "A", "B", "C", "D", "z", "s0", "dy", "d_state_out"]
         return [d[k] for k in keys if d.get(k) is not None]
+
+
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of a per-rank value over all ranks (the slowest replica sets the job's time)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every rank processes tokens_per_rank per step; weak scaling."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
 
 
 def l2_flush_buffer(dev):
@@ -369,25 +394,19 @@ def main():
     total, per_stage, launches = time_device(step, args.steps, args.warmup, flush)
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
-    ms = sum(total) / len(total)
+    ms = reduce_max(sum(total) / len(total), dist, dev)
     if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
 
     e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 20)), 2)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dist, dev)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
     tokens = w.n_seqs * w.n_tok
-    value = world * tokens / (ms * 1e-3)
+    value = job_throughput(tokens, world, ms)
     peaks, peak_src = _measured_peaks()
     ab = alg_bytes(w)
     stage_ms = {k: sum(v) / len(v) for k, v in per_stage.items()}
@@ -395,6 +414,27 @@ def main():
     dom_bytes = ab[dom] * tokens
     achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
     stage_gbs = {k: ab[k] * tokens / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
+    props = torch.cuda.get_device_properties(dev)
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    fp32_peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12  # TFLOP/s
+    if dom in SCAN_FLOPS:
+        # The scan kernels are bound by FP32 arithmetic, not HBM: per element the backward needs
+        # ~22 flops for ~0.9 bytes, far above the GB300 ridge (~12 flops/byte).
+        elems = tokens * w.channels * w.d_state
+        flops = SCAN_FLOPS[dom] * elems
+        ach_tf = flops / (stage_ms[dom] * 1e-3) / 1e12
+        roofline = {"kernel": f"ssm_{dom}", "bound": "alu", "achieved": ach_tf,
+                    "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach_tf / fp32_peak,
+                    "peak_source": f"derived: SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz",
+                    "traffic": None, "algorithmic_flops_per_launch": flops,
+                    "hbm": {"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src,
+                            "algorithmic_bytes_per_launch": dom_bytes}}
+    else:
+        roofline = {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "peak_source": peak_src, "traffic": None,
+                    "algorithmic_bytes_per_launch": dom_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -407,13 +447,10 @@ def main():
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_hbm_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
         "stage_frac_of_8tbs": {k: round(v / SPEC_HBM_GBS, 4) for k, v in stage_gbs.items()},
-        "roofline": {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src,
-                     "traffic": None, "algorithmic_bytes_per_launch": dom_bytes},
+        "roofline": roofline,
         "gpu_launches": int(launches),
         "clocks": clocks,
-        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
     if not args.no_cpu_baseline and world == 1:

@@ -151,17 +151,28 @@ conv_bwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   }
 }
 
-__global__ void conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ d_c,
-                                   float* __restrict__ d_bias, int n_s, int nt, int D, int K) {
+// d_c[d][k] and d_bias[d] = sum over (sequence, tile) partials.  A block = 32 outputs x 8
+// slices of the (sequence, tile) range; slices combine in shared memory in a fixed order.
+constexpr int kRedOut = 32, kRedSlices = 8;
+__global__ void __launch_bounds__(kRedOut * kRedSlices)
+conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ d_c,
+                   float* __restrict__ d_bias, int n_s, int nt, int D, int K) {
+  __shared__ float sred[kRedSlices][kRedOut];
   const long total = (long)D * (K + 1);
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
-       i += (long)gridDim.x * blockDim.x) {
-    int d = (int)(i / (K + 1)), k = (int)(i - (long)d * (K + 1));
-    float acc = 0.0f;
-    for (int b = 0; b < n_s; b++)
-      for (int j = 0; j < nt; j++) acc += part[(((long)b * nt + j) * D + d) * (K + 1) + k];
-    if (k < K) d_c[(long)d * K + k] = acc;
-    else if (d_bias) d_bias[d] = acc;
+  const int lo = threadIdx.x % kRedOut, sl = threadIdx.x / kRedOut;
+  const long o = (long)blockIdx.x * kRedOut + lo;
+  const long terms = (long)n_s * nt;
+  float acc = 0.0f;
+  if (o < total)
+    for (long j = sl; j < terms; j += kRedSlices) acc += part[j * total + o];
+  sred[sl][lo] = acc;
+  __syncthreads();
+  if (sl == 0 && o < total) {
+    float v = 0.0f;
+    for (int q = 0; q < kRedSlices; q++) v += sred[q][lo];
+    const int d = (int)(o / (K + 1)), k = (int)(o - (long)d * (K + 1));
+    if (k < K) d_c[(long)d * K + k] = v;
+    else if (d_bias) d_bias[d] = v;
   }
 }
 
@@ -200,10 +211,10 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
   float* part = (float*)ws;
   conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (const IO*)dout,
                                                         (IO*)d_sx, part, D, L, K, silu), count_launches(1);
-  long total = (long)D * (K + 1);
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 4096) blocks = 4096;
-  conv_reduce_kernel<<<blocks, 256, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K), count_launches(1);
+  const long total = (long)D * (K + 1);
+  const int blocks = (int)((total + kRedOut - 1) / kRedOut);
+  conv_reduce_kernel<<<blocks, kRedOut * kRedSlices, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K),
+      count_launches(1);
   return cudaGetLastError();
 }
 

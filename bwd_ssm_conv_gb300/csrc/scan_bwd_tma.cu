@@ -129,7 +129,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
   float4* sP = reinterpret_cast<float4*>(smem + m.off_p);        // [TT][CB] (delta, x, gy, dyg)
   float* sSPG = reinterpret_cast<float*>(smem + m.off_spg);      // [TT][CB] softplus'(pre)
-  float4* sPart = reinterpret_cast<float4*>(smem + m.off_part);  // [TT][threads] (sB, sAw, ypre)
+  float* sPB = reinterpret_cast<float*>(smem + m.off_part);      // [TT][threads] sum_n dh B
+  float* sPA = sPB + TT * kScanThreads;                           // [TT][threads] sum_n A w
+  float* sPY = sPA + TT * kScanThreads;                           // [TT][threads] sum_n C h
   float* red = reinterpret_cast<float*>(smem + m.off_red);       // [TT][warps][2N]
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);      // D[CB], dt_bias[CB]
   float* sAcc = reinterpret_cast<float*>(smem + m.off_acc);      // [warps][CB][2]
@@ -343,7 +345,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
             yp2 = f2_fma(C2[q], hh[r + 1][q], yp2);
             carry2[q] = cn2;
           }
-          sPart[i * kScanThreads + tid] = make_float4(f2_sum(sB2), f2_sum(sAw2), f2_sum(yp2), 0.0f);
+          sPB[i * kScanThreads + tid] = f2_sum(sB2);
+          sPA[i * kScanThreads + tid] = f2_sum(sAw2);
+          sPY[i * kScanThreads + tid] = f2_sum(yp2);
           float v8[8];
           f2_unpack(dB2[0], v8[0], v8[1]);
           f2_unpack(dB2[1], v8[2], v8[3]);
@@ -364,11 +368,13 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     IO* oddt = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + 2 * m.out_tile);
     for (int idx = tid; idx < cnt * CB; idx += kScanThreads) {
       const int i = idx / CB, c = idx - i * CB;  // c == tid % CB for every item of this thread
-      const float4* pp4 = sPart + i * kScanThreads + c * 4;
-      const float4 q0 = pp4[0], q1 = pp4[1], q2 = pp4[2], q3 = pp4[3];
-      const float sBt = (q0.x + q1.x) + (q2.x + q3.x);
-      const float sAwt = (q0.y + q1.y) + (q2.y + q3.y);
-      const float ypt = (q0.z + q1.z) + (q2.z + q3.z);
+      const int pi = i * kScanThreads + c * 4;  // the 4 threads of channel c, 16 bytes per lane
+      const float4 vb = *reinterpret_cast<const float4*>(sPB + pi);
+      const float4 va = *reinterpret_cast<const float4*>(sPA + pi);
+      const float4 vy = *reinterpret_cast<const float4*>(sPY + pi);
+      const float sBt = (vb.x + vb.y) + (vb.z + vb.w);
+      const float sAwt = (va.x + va.y) + (va.z + va.w);
+      const float ypt = (vy.x + vy.y) + (vy.z + vy.w);
       const float4 p4 = sP[idx];
       const float D = sPar[c];
       const float ddl = fmaf(p4.y, sBt, sAwt);
@@ -555,7 +561,7 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->off_spg = take(TT * cb * 4);
   m->off_bf = take(TT * p.N * 4);
   m->off_cf = take(TT * p.N * 4);
-  m->off_part = take(TT * kScanThreads * 16);
+  m->off_part = take(3 * TT * kScanThreads * 4);
   m->off_red = take(TT * kWarps * 2 * p.N * 4);
   m->out_tile = al(tile);
   m->out_stride = 3 * m->out_tile;

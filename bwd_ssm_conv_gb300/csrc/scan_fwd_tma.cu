@@ -304,13 +304,14 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   if (p.io != SSM_BF16 || p.P != 1 || !p.a_per_state || p.N > 256 || (p.N * io) % 16 != 0 ||
       (p.HP * io) % 16 != 0 || p.chunk % kFwdTile != 0)
     return q;
-  // largest states-per-thread that still gives two blocks per SM without time segments
+  // largest states-per-thread that still gives four blocks per SM without time segments
+  // (the recurrence is latency-bound: more warps per SM beat fewer instructions per state)
   int ns = 0;
   for (int cand = 16; cand >= 4; cand >>= 1) {
     if (p.N % cand != 0) continue;
     ns = cand;
     const int cb = kScanThreads / (p.N / cand);
-    if (cb > 0 && (long)p.ns * ((p.HP + cb - 1) / cb) >= 2L * num_sms) break;
+    if (cb > 0 && (long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) break;
   }
   if (ns < 4 || p.N / ns > 32) return q;
   q.ns_state = ns;
