@@ -283,6 +283,14 @@ def time_e2e(step, steps, warmup):
 
 
 # ---- the oracle on the host (CPU baseline and the reference arm) ---------------------------
+def config_of(w, world: int) -> dict:
+    """The workload description both arms print."""
+    return {"workload": w.name, "n_seqs": w.n_seqs, "seq_len": w.n_tok, "d_inner": w.channels,
+            "head_dim": w.head_dim, "d_state": w.d_state, "d_conv": w.d_conv, "chunk": w.chunk,
+            "state_dtype": "f32", "parallelism": f"replicas{world}",
+            "l2": "flushed before every step"}
+
+
 def oracle_sample(w, channels, seqs=1, seed=None):
     """Runs the oracle's whole step on `seqs` sequences x all tokens x `channels` channels of
     the workload; returns (seconds, channel-tokens processed)."""
@@ -308,17 +316,22 @@ def oracle_sample(w, channels, seqs=1, seed=None):
 
 
 def cpu_baseline(w, budget_s=12.0):
-    """Oracle tokens/s at the workload's full width, from a bounded channel sample."""
+    """Oracle tokens/s at the workload's full width, from a bounded sample of the workload:
+    whole sequences of all channels when they fit the budget, else a channel subset."""
     t, ct = oracle_sample(w, channels=4 * w.head_dim if w.head_dim > 1 else 4)
     per_ct = t / ct
-    ch = max(1, min(w.n_head, int(budget_s / (per_ct * w.n_tok))))
-    t, ct = oracle_sample(w, channels=ch)
-    per_ct = t / ct
-    tokens_per_s = 1.0 / (per_ct * w.n_head)  # full width: every channel of every token
+    full_seq = per_ct * w.n_tok * w.n_head  # seconds for one sequence, all channels
+    if full_seq <= budget_s:
+        seqs = max(1, min(w.n_seqs, int(budget_s / full_seq)))
+        ch = w.n_head
+    else:
+        seqs, ch = 1, max(1, int(budget_s / (per_ct * w.n_tok)))
+    t, ct = oracle_sample(w, channels=ch, seqs=seqs)
+    tokens_per_s = ct / t / w.n_head  # every channel of every token
     return {"value": tokens_per_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"1 sequence x {w.n_tok} tokens x {ch} of {w.n_head} channels of the same "
-                      f"workload, full step (conv fwd, scan fwd, scan bwd, conv bwd), "
-                      f"{t:.1f} s single-threaded f64; scaled to all channels"}
+            "sample": f"{seqs} of {w.n_seqs} sequences x {w.n_tok} tokens x {ch} of {w.n_head} "
+                      f"channels of the same workload, full step (conv fwd, scan fwd, scan bwd, "
+                      f"conv bwd), {t:.1f} s single-threaded f64; scaled to all channels"}
 
 
 def run_reference(args, w):
@@ -341,8 +354,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * w.n_seqs * w.n_tok / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "n_seqs": w.n_seqs, "seq_len": w.n_tok,
-                       "d_inner": w.channels, "d_state": w.d_state, "chunk": w.chunk},
+            "config": config_of(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -440,10 +452,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.io == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "n_seqs": w.n_seqs, "seq_len": w.n_tok,
-                   "d_inner": w.channels, "head_dim": w.head_dim, "d_state": w.d_state,
-                   "d_conv": w.d_conv, "chunk": w.chunk, "state_dtype": "f32",
-                   "parallelism": f"replicas{world}", "l2": "flushed before every step"},
+        "config": config_of(w, world),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_hbm_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
         "stage_frac_of_8tbs": {k: round(v / SPEC_HBM_GBS, 4) for k, v in stage_gbs.items()},
