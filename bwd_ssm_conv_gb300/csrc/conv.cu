@@ -151,6 +151,138 @@ conv_bwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   }
 }
 
+
+// ---- d_conv <= 4: compile-time taps and division-free index math -------------------------
+// Loads walk rows with whole warps (lane = column), so no per-element division is needed; the
+// tap loops unroll.  Same tiles, results and partial layout as the general kernels above.
+template <typename IO, int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv_fwd_k_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                  const float* __restrict__ bias, IO* __restrict__ out, int D, int L, int silu) {
+  constexpr int R = kConvTT + K - 1, Rp = R | 1;
+  constexpr int kWarpsC = kConvThreads / 32;
+  __shared__ float s[kConvTD * Rp];
+  const int d0 = blockIdx.x * kConvTD, t0 = blockIdx.y * kConvTT, b = blockIdx.z;
+  const long W = (long)L + K - 1;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int r = wid; r < kConvTD; r += kWarpsC) {
+    const int d = d0 + r;
+    const IO* row = sx + ((long)b * D + d) * W + t0;
+    const long lim = W - t0;  // columns left in this row
+#pragma unroll
+    for (int col = lane; col < R; col += 32)
+      s[r * Rp + col] = (d < D && col < lim) ? ld(row + col) : 0.0f;
+  }
+  const int d = d0 + lane;
+  float w[K];
+#pragma unroll
+  for (int k = 0; k < K; k++) w[k] = d < D ? __ldg(c + (long)d * K + k) : 0.0f;
+  const float bv = (bias && d < D) ? __ldg(bias + d) : 0.0f;
+  __syncthreads();
+  if (d >= D) return;
+  const int tmax = min(kConvTT, L - t0);
+  for (int tt = wid; tt < tmax; tt += kWarpsC) {
+    float acc = bv;
+#pragma unroll
+    for (int k = 0; k < K; k++) acc = fmaf(s[lane * Rp + tt + k], w[k], acc);
+    st(out + ((long)b * L + t0 + tt) * D + d, silu ? siluf_(acc) : acc);
+  }
+}
+
+template <typename IO, int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv_bwd_k_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                  const float* __restrict__ bias, const IO* __restrict__ dout,
+                  IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int silu) {
+  constexpr int NS_ = kConvTT + 2 * K - 2, Rs = NS_ | 1;  // sx columns i0-K+1 .. i0+TT+K-2
+  constexpr int NG = kConvTT + K - 1, Rg = NG | 1;        // gp tokens  i0-K+1 .. i0+TT-1
+  constexpr int kWarpsC = kConvThreads / 32;
+  __shared__ float sxs[kConvTD * Rs];
+  __shared__ float gps[kConvTD * Rg];
+  const int d0 = blockIdx.x * kConvTD, i0 = blockIdx.y * kConvTT, b = blockIdx.z;
+  const long W = (long)L + K - 1;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int base = i0 - K + 1;
+  for (int r = wid; r < kConvTD; r += kWarpsC) {  // sx: rows along time
+    const int d = d0 + r;
+    const IO* row = sx + ((long)b * D + d) * W;
+#pragma unroll
+    for (int j = lane; j < NS_; j += 32) {
+      const long col = (long)base + j;
+      sxs[r * Rs + j] = (d < D && col >= 0 && col < W) ? ld(row + col) : 0.0f;
+    }
+  }
+  {  // dout: channel-fastest rows per token; lane = channel
+    const int d = d0 + lane;
+    for (int tl = wid; tl < NG; tl += kWarpsC) {
+      const long t = (long)base + tl;
+      gps[lane * Rg + tl] = (d < D && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+    }
+  }
+  // each warp owns channel rows r = wid, wid + 8, ...: its taps in registers
+  __syncthreads();
+  if (silu) {  // gp = dout * silu'(pre), pre recomputed with the forward's tap order
+    for (int r = wid; r < kConvTD; r += kWarpsC) {
+      const int d = d0 + r;
+      if (d >= D) continue;
+      float w[K];
+#pragma unroll
+      for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
+      const float bv = bias ? __ldg(bias + d) : 0.0f;
+#pragma unroll
+      for (int tl = lane; tl < NG; tl += 32) {
+        const long t = (long)base + tl;
+        if (t < 0 || t >= L) continue;
+        float pre = bv;
+#pragma unroll
+        for (int k = 0; k < K; k++) pre = fmaf(sxs[r * Rs + tl + k], w[k], pre);
+        gps[r * Rg + tl] *= silu_gradf_(pre);
+      }
+    }
+    __syncthreads();
+  }
+  const int nt = gridDim.y;
+  for (int r = wid; r < kConvTD; r += kWarpsC) {
+    const int d = d0 + r;
+    if (d >= D) continue;
+    float w[K];
+#pragma unroll
+    for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
+    // d_sx columns [i0, i0+TT): lanes along time -> coalesced row stores
+#pragma unroll
+    for (int il = lane; il < kConvTT; il += 32) {
+      const long i = (long)i0 + il;
+      if (i < W) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; k++) acc = fmaf(gps[r * Rg + il + K - 1 - k], w[k], acc);
+        st(d_sx + ((long)b * D + d) * W + i, acc);
+      }
+    }
+    // partial d_c[d][k] and d_bias[d] over the tokens this tile owns: lanes over tokens, then
+    // a fixed-order warp sum
+    float pk[K + 1];
+#pragma unroll
+    for (int k = 0; k <= K; k++) pk[k] = 0.0f;
+#pragma unroll
+    for (int tl = lane; tl < kConvTT; tl += 32) {
+      if ((long)i0 + tl < L) {
+        const float g = gps[r * Rg + tl + K - 1];
+#pragma unroll
+        for (int k = 0; k < K; k++) pk[k] = fmaf(g, sxs[r * Rs + tl + K - 1 + k], pk[k]);
+        pk[K] += g;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k <= K; k++) {
+      float v = pk[k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) part[(((long)b * nt + blockIdx.y) * D + d) * (K + 1) + k] = v;
+    }
+  }
+}
+
 // d_c[d][k] and d_bias[d] = sum over (sequence, tile) partials.  A block = 32 outputs x 8
 // slices of the (sequence, tile) range; slices combine in shared memory in a fixed order.
 constexpr int kRedOut = 32, kRedSlices = 8;
@@ -187,9 +319,19 @@ template <typename IO>
 static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias, void* out,
                               void* cs, int n_s, int D, int L, int K, int silu, cudaStream_t st) {
   dim3 grid((D + kConvTD - 1) / kConvTD, (L + kConvTT - 1) / kConvTT, n_s);
-  size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
-  conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (IO*)out, D, L, K,
-                                                        silu), count_launches(1);
+  const IO* x = (const IO*)sx;
+  IO* o = (IO*)out;
+  switch (K) {
+    case 1: conv_fwd_k_kernel<IO, 1><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 2: conv_fwd_k_kernel<IO, 2><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 3: conv_fwd_k_kernel<IO, 3><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 4: conv_fwd_k_kernel<IO, 4><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    default: {
+      size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
+      conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, o, D, L, K, silu);
+    }
+  }
+  count_launches(1);
   if (cs && K > 1) {
     long total = (long)n_s * D * (K - 1);
     int blocks = (int)((total + 255) / 256);
@@ -209,8 +351,18 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
   size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + 2 * K - 2) +
                                  kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
   float* part = (float*)ws;
-  conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>((const IO*)sx, c, bias, (const IO*)dout,
-                                                        (IO*)d_sx, part, D, L, K, silu), count_launches(1);
+  const IO* x = (const IO*)sx;
+  const IO* g = (const IO*)dout;
+  IO* dx = (IO*)d_sx;
+  switch (K) {
+    case 1: conv_bwd_k_kernel<IO, 1><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 2: conv_bwd_k_kernel<IO, 2><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 3: conv_bwd_k_kernel<IO, 3><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 4: conv_bwd_k_kernel<IO, 4><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    default:
+      conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, g, dx, part, D, L, K, silu);
+  }
+  count_launches(1);
   const long total = (long)D * (K + 1);
   const int blocks = (int)((total + kRedOut - 1) / kRedOut);
   conv_reduce_kernel<<<blocks, kRedOut * kRedSlices, 0, st>>>(part, d_c, d_bias, n_s, nt, D, K),
