@@ -15,6 +15,8 @@
 // saving the state at every 8-token sub-chunk start (global scratch, re-read from L2);
 // level 2 walks the tiles in reverse, recomputes each sub-chunk's 8 states and decays in
 // registers and runs the adjoint over them.
+#include <type_traits>
+
 #include "scan_bwd.cuh"
 #include "tma.cuh"
 
@@ -267,23 +269,28 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         hp[0] = f2_pack(src[0], src[1]);
         hp[1] = f2_pack(src[2], src[3]);
       }
-#pragma unroll
-      for (int i = 0; i < TT; i++) {
-        if (i < cnt) {
-          if (i % kTsub == 0) {
-            float h0, h1, h2, h3;
-            f2_unpack(hp[0], h0, h1);
-            f2_unpack(hp[1], h2, h3);
-            bnd[(cs.j * (TT / kTsub) + i / kTsub) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
-          }
-          const float4 p4 = sP[i * CB + cl];
-          const f2_t dl2 = f2_pack(p4.x, p4.x);
-          const float dx = p4.x * p4.y;
-          const f2_t dx2 = f2_pack(dx, dx);
-          const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
-          hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
-          hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+      auto token = [&](int i) {
+        if (i % kTsub == 0) {
+          float h0, h1, h2, h3;
+          f2_unpack(hp[0], h0, h1);
+          f2_unpack(hp[1], h2, h3);
+          bnd[(cs.j * (TT / kTsub) + i / kTsub) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
         }
+        const float4 p4 = sP[i * CB + cl];
+        const f2_t dl2 = f2_pack(p4.x, p4.x);
+        const float dx = p4.x * p4.y;
+        const f2_t dx2 = f2_pack(dx, dx);
+        const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
+        hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
+        hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+      };
+      if (cnt == TT) {  // full tile: no per-token branch, so tokens can interleave
+#pragma unroll
+        for (int i = 0; i < TT; i++) token(i);
+      } else {
+#pragma unroll
+        for (int i = 0; i < TT; i++)
+          if (i < cnt) token(i);
       }
       __syncthreads();  // stage fully read
       if (tid == 0 && pp.ck >= c_first) issue();
@@ -291,10 +298,10 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
 
     // ---- level 2: sub-chunks last to first: recompute 8 states, then the adjoint ------------
-    const int nsub = (cnt + kTsub - 1) / kTsub;
-    for (int k = nsub - 1; k >= 0; k--) {
+    // One sub-chunk; FULL (all kTsub tokens present) drops the per-token branches.
+    auto sub_chunk = [&](int k, int c8, auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
       const int i0 = k * kTsub;
-      const int c8 = min(kTsub, cnt - i0);
       f2_t hh[kTsub + 1][2], aa[kTsub][2];
       {
         const float4 v = bnd[(cs.j * (TT / kTsub) + k) * kScanThreads + tid];
@@ -303,7 +310,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       }
 #pragma unroll
       for (int r = 0; r < kTsub; r++) {
-        if (r < c8) {
+        if (FULL || r < c8) {
           const float4 p4 = sP[(i0 + r) * CB + cl];
           const f2_t dl2 = f2_pack(p4.x, p4.x);
           const float dx = p4.x * p4.y;
@@ -321,7 +328,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       }
 #pragma unroll
       for (int r = kTsub - 1; r >= 0; r--) {
-        if (r < c8) {  // uniform over the block
+        if (FULL || r < c8) {  // uniform over the block
           const int i = i0 + r;
           const float4 p4 = sP[i * CB + cl];
           const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.z, p4.z);
@@ -358,6 +365,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
           red[(i * kWarps + warp) * 2 * N + (o >> 2) * N + n0 + (o & 3)] = tot;
         }
       }
+    };
+    const int nsub = (cnt + kTsub - 1) / kTsub;
+    for (int k = nsub - 1; k >= 0; k--) {
+      const int c8 = min(kTsub, cnt - k * kTsub);
+      if (c8 == kTsub) sub_chunk(k, c8, std::true_type{});
+      else sub_chunk(k, c8, std::false_type{});
     }
     __syncthreads();  // sPart and red complete
 

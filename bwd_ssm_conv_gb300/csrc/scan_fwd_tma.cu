@@ -74,14 +74,15 @@ __device__ __forceinline__ void lds_row(const IO* ptr, float (&out)[NS]) {
   }
 }
 
-template <typename IO, int NS, bool LOCAL>
+template <typename IO, int NS, int TPC, bool LOCAL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;
   constexpr int TT = kFwdTile;
   extern __shared__ __align__(128) unsigned char smem[];
   const ScanProblem& p = a.p;
-  const int tid = threadIdx.x, tpc = a.tpc, cb = a.cb;
+  constexpr int tpc = TPC, cb = kScanThreads / TPC;  // compile-time: index math is shifts
+  const int tid = threadIdx.x;
   const int cl = tid / tpc, sg = tid - cl * tpc;
   const int ch0 = blockIdx.x * cb, ch = ch0 + cl;
   const int s = blockIdx.y, b = blockIdx.z;
@@ -196,39 +197,44 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         *reinterpret_cast<float4*>(dst + 2 * j) = make_float4(x0, x1, x2, x3);
       }
     }
+    auto token = [&](int i) {
+      const float4 dd = sDD[i * cb + cl];
+      const f2_t dl2 = f2_pack(dd.x, dd.y), dx2 = f2_pack(dd.z, dd.w);
+      f2_t B2[NS / 2];
 #pragma unroll
-    for (int i = 0; i < TT; i++) {
-      if (i < cnt) {
-        const float4 dd = sDD[i * cb + cl];
-        const f2_t dl2 = f2_pack(dd.x, dd.y), dx2 = f2_pack(dd.z, dd.w);
-        f2_t B2[NS / 2];
+      for (int j = 0; j < NS; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
+        B2[j / 2] = f2_pack(v.x, v.y);
+        B2[j / 2 + 1] = f2_pack(v.z, v.w);
+      }
+      if (LOCAL) {
+#pragma unroll
+        for (int j = 0; j < NS / 2; j++)
+          hp[j] = f2_fma(f2_ex2(f2_mul(dl2, A2p[j])), hp[j], f2_mul(dx2, B2[j]));
+        sumd += dd.x;
+      } else {
+        f2_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
         for (int j = 0; j < NS; j += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
-          B2[j / 2] = f2_pack(v.x, v.y);
-          B2[j / 2 + 1] = f2_pack(v.z, v.w);
+          const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
+          const int q = j / 2;
+          hp[q] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q])), hp[q], f2_mul(dx2, B2[q]));
+          hp[q + 1] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q + 1])), hp[q + 1], f2_mul(dx2, B2[q + 1]));
+          acc0 = f2_fma(f2_pack(v.x, v.y), hp[q], acc0);
+          acc1 = f2_fma(f2_pack(v.z, v.w), hp[q + 1], acc1);
         }
-        if (LOCAL) {
-#pragma unroll
-          for (int j = 0; j < NS / 2; j++)
-            hp[j] = f2_fma(f2_ex2(f2_mul(dl2, A2p[j])), hp[j], f2_mul(dx2, B2[j]));
-          sumd += dd.x;
-        } else {
-          f2_t acc0 = 0ull, acc1 = 0ull;
-#pragma unroll
-          for (int j = 0; j < NS; j += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
-            const int q = j / 2;
-            hp[q] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q])), hp[q], f2_mul(dx2, B2[q]));
-            hp[q + 1] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q + 1])), hp[q + 1], f2_mul(dx2, B2[q + 1]));
-            acc0 = f2_fma(f2_pack(v.x, v.y), hp[q], acc0);
-            acc1 = f2_fma(f2_pack(v.z, v.w), hp[q + 1], acc1);
-          }
-          float lo, hi;
-          f2_unpack(f2_add(acc0, acc1), lo, hi);
-          sACC[i * cb * tpc + tid] = lo + hi;
-        }
+        float lo, hi;
+        f2_unpack(f2_add(acc0, acc1), lo, hi);
+        sACC[i * cb * tpc + tid] = lo + hi;
       }
+    };
+    if (cnt == TT) {  // full tile: no per-token branch, so tokens can interleave
+#pragma unroll
+      for (int i = 0; i < TT; i++) token(i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < TT; i++)
+        if (i < cnt) token(i);
     }
     __syncthreads();
 
@@ -237,8 +243,18 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
       for (int idx = tid; idx < cnt * cb; idx += kScanThreads) {
         const int i = idx / cb, c = idx - i * cb;
-        float acc = 0.0f;
-        for (int q = 0; q < tpc; q++) acc += sACC[(i * cb + c) * tpc + q];
+        const float* pa = sACC + (i * cb + c) * tpc;  // the channel's tpc partials, contiguous
+        float acc;
+        if (tpc == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(pa);
+          acc = (v.x + v.y) + (v.z + v.w);
+        } else if (tpc == 2) {
+          const float2 v = *reinterpret_cast<const float2*>(pa);
+          acc = v.x + v.y;
+        } else {
+          acc = 0.0f;
+          for (int q = 0; q < tpc; q++) acc += pa[q];
+        }
         float yv = fmaf(sPar[c], lds1(sx + idx), acc);
         if (p.z) yv *= siluf_(lds1(sz + idx));
         if (p.check_finite && !isfinite(yv)) record_status(p.status, SSM_ERR_NONFINITE);
@@ -313,7 +329,7 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
     const int cb = kScanThreads / (p.N / cand);
     if (cb > 0 && (long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) break;
   }
-  if (ns < 4 || p.N / ns > 32) return q;
+  if (ns < 4 || p.N / ns > 4) return q;  // instantiated: 1, 2 or 4 threads per channel
   q.ns_state = ns;
   q.tpc = p.N / ns;
   if (q.tpc > 32) return q;
@@ -350,10 +366,10 @@ size_t scan_fwd_tma_ws_bytes(const ScanProblem& p, int num_sms) {
   return q.ok ? q.bytes : 0;
 }
 
-template <typename IO, int NS>
+template <typename IO, int NS, int TPC>
 static cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
-  auto km = scan_fwd_tma_kernel<IO, NS, false>;
-  auto kl = scan_fwd_tma_kernel<IO, NS, true>;
+  auto km = scan_fwd_tma_kernel<IO, NS, TPC, false>;
+  auto kl = scan_fwd_tma_kernel<IO, NS, TPC, true>;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -415,10 +431,16 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   const size_t smem = a.off_bar + 64;
   a.bytes_local = 2 * tile + row;
   a.bytes_main = (2 + (p.z ? 1 : 0)) * tile + 2 * row;
-  switch (q.ns_state) {
-    case 16: return launch_fwd_tma_t<__nv_bfloat16, 16>(a, smem, st);
-    case 8: return launch_fwd_tma_t<__nv_bfloat16, 8>(a, smem, st);
-    default: return launch_fwd_tma_t<__nv_bfloat16, 4>(a, smem, st);
+  // (states per thread, threads per channel) pairs for d_state 16, 32, 64 (others: general path)
+  const int key = q.ns_state * 100 + q.tpc;
+  switch (key) {
+    case 1601: return launch_fwd_tma_t<__nv_bfloat16, 16, 1>(a, smem, st);
+    case 802: return launch_fwd_tma_t<__nv_bfloat16, 8, 2>(a, smem, st);
+    case 404: return launch_fwd_tma_t<__nv_bfloat16, 4, 4>(a, smem, st);
+    case 1602: return launch_fwd_tma_t<__nv_bfloat16, 16, 2>(a, smem, st);
+    case 804: return launch_fwd_tma_t<__nv_bfloat16, 8, 4>(a, smem, st);
+    case 1604: return launch_fwd_tma_t<__nv_bfloat16, 16, 4>(a, smem, st);
+    default: return cudaErrorNotSupported;
   }
 }
 
