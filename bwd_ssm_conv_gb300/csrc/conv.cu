@@ -152,133 +152,240 @@ conv_bwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
 }
 
 
-// ---- d_conv <= 4: compile-time taps and division-free index math -------------------------
-// Loads walk rows with whole warps (lane = column), so no per-element division is needed; the
-// tap loops unroll.  Same tiles, results and partial layout as the general kernels above.
-template <typename IO, int K>
-__global__ void __launch_bounds__(kConvThreads)
-conv_fwd_k_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
-                  const float* __restrict__ bias, IO* __restrict__ out, int D, int L, int silu) {
-  constexpr int R = kConvTT + K - 1, Rp = R | 1;
-  constexpr int kWarpsC = kConvThreads / 32;
-  __shared__ float s[kConvTD * Rp];
-  const int d0 = blockIdx.x * kConvTD, t0 = blockIdx.y * kConvTT, b = blockIdx.z;
-  const long W = (long)L + K - 1;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int r = wid; r < kConvTD; r += kWarpsC) {
-    const int d = d0 + r;
-    const IO* row = sx + ((long)b * D + d) * W + t0;
-    const long lim = W - t0;  // columns left in this row
+// ---- d_conv <= 4: one thread streams 32 tokens of one channel --------------------------
+// A tile = 32 channels (one per lane) x 256 tokens (8 warps x 32).  Each thread walks its 32
+// tokens in order with the taps, the last d_conv inputs and (backward) the last d_conv input
+// gradients in registers, so every tap sum, SiLU (') and d_c term is computed once from
+// registers.  Lanes run along channels, so the channel-fastest out / dout rows are read and
+// written coalesced straight from global memory; the time-fastest sx (and d_sx) rows go
+// through shared memory, moved with aligned 16-byte accesses (row starts have any alignment:
+// a row holds L + d_conv - 1 elements) and scalar ones only at partial groups.
+constexpr int kSeg = 32;                       // tokens per thread
+constexpr int kSegWarps = 8;
+constexpr int kSegThreads = 32 * kSegWarps;
+constexpr int kSegTT = kSeg * kSegWarps;       // tokens per tile
+constexpr int kSegRows = 32;                   // channels per tile
+constexpr int kRowsPerWarp = kSegRows / kSegWarps;
+
+template <typename IO>
+__device__ __forceinline__ void unpack16(const uint4 u, float* v) {
+  if constexpr (sizeof(IO) == 4) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int col = lane; col < R; col += 32)
-      s[r * Rp + col] = (d < D && col < lim) ? ld(row + col) : 0.0f;
+    for (int i = 0; i < 4; i++) {  // bf16 -> fp32 is exact: the bits move up 16 places
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
   }
-  const int d = d0 + lane;
-  float w[K];
+}
+template <typename IO>
+__device__ __forceinline__ uint4 pack16(const float* v) {
+  if constexpr (sizeof(IO) == 4) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[3]));
+  } else {
+    uint32_t w[4];
 #pragma unroll
-  for (int k = 0; k < K; k++) w[k] = d < D ? __ldg(c + (long)d * K + k) : 0.0f;
-  const float bv = (bias && d < D) ? __ldg(bias + d) : 0.0f;
-  __syncthreads();
-  if (d >= D) return;
-  const int tmax = min(kConvTT, L - t0);
-  for (int tt = wid; tt < tmax; tt += kWarpsC) {
-    float acc = bv;
+    for (int i = 0; i < 4; i++) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);  // RNE, as st()
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Copies columns [c0, c0 + NC) of rows d0 + wid + 8q (q < 4) of a time-fastest [..][W] array into
+// s[q'][0..NC) (row stride SP floats) as fp32; zero outside [0, W) and for rows >= D.  16-byte
+// groups aligned in global memory; a group partly outside the row is read element by element.
+template <typename IO, int NC, int SP>
+__device__ __forceinline__ void rows_to_smem(const IO* base, int d0, int D, long c0, long W,
+                                             float* s, int wid, int lane) {
+  constexpr int V = 16 / sizeof(IO);
+  constexpr int NG = (NC + V - 1) / V + 1;  // groups covering NC columns at any alignment
+  for (int idx = lane; idx < kRowsPerWarp * NG; idx += 32) {
+    const int q = idx / NG, gi = idx - q * NG;
+    const int r = wid + q * kSegWarps, d = d0 + r;
+    if (d >= D) continue;
+    const IO* row = base + (long)d * W;
+    const int ph = (int)(((uintptr_t)(row + c0) & 15) / sizeof(IO));
+    const long cs = c0 - ph + (long)gi * V;  // column of the group's first element
+    const int j0 = (int)(cs - c0);           // its index in s
+    if (j0 >= NC) continue;
+    float v[V];
+    if (cs >= 0 && cs + V <= W) {
+      unpack16<IO>(__ldg(reinterpret_cast<const uint4*>(row + cs)), v);
+    } else {
 #pragma unroll
-    for (int k = 0; k < K; k++) acc = fmaf(s[lane * Rp + tt + k], w[k], acc);
-    st(out + ((long)b * L + t0 + tt) * D + d, silu ? siluf_(acc) : acc);
+      for (int e = 0; e < V; e++) v[e] = (cs + e >= 0 && cs + e < W) ? ld(row + cs + e) : 0.0f;
+    }
+    float* dst = s + r * SP + j0;
+    if (j0 >= 0 && j0 + V <= NC) {
+#pragma unroll
+      for (int e = 0; e < V; e++) dst[e] = v[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; e++)
+        if (j0 + e >= 0 && j0 + e < NC) dst[e] = v[e];
+    }
   }
 }
 
 template <typename IO, int K>
-__global__ void __launch_bounds__(kConvThreads)
-conv_bwd_k_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
-                  const float* __restrict__ bias, const IO* __restrict__ dout,
-                  IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int silu) {
-  constexpr int NS_ = kConvTT + 2 * K - 2, Rs = NS_ | 1;  // sx columns i0-K+1 .. i0+TT+K-2
-  constexpr int NG = kConvTT + K - 1, Rg = NG | 1;        // gp tokens  i0-K+1 .. i0+TT-1
-  constexpr int kWarpsC = kConvThreads / 32;
-  __shared__ float sxs[kConvTD * Rs];
-  __shared__ float gps[kConvTD * Rg];
-  const int d0 = blockIdx.x * kConvTD, i0 = blockIdx.y * kConvTT, b = blockIdx.z;
+__global__ void __launch_bounds__(kSegThreads)
+conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                    const float* __restrict__ bias, IO* __restrict__ out, int D, int L, int silu) {
+  constexpr int NC = kSegTT + K - 1, SP = NC | 1;  // odd stride: lanes read distinct banks
+  __shared__ float s[kSegRows * SP];
+  const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
   const long W = (long)L + K - 1;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int base = i0 - K + 1;
-  for (int r = wid; r < kConvTD; r += kWarpsC) {  // sx: rows along time
-    const int d = d0 + r;
-    const IO* row = sx + ((long)b * D + d) * W;
-#pragma unroll
-    for (int j = lane; j < NS_; j += 32) {
-      const long col = (long)base + j;
-      sxs[r * Rs + j] = (d < D && col >= 0 && col < W) ? ld(row + col) : 0.0f;
-    }
-  }
-  {  // dout: channel-fastest rows per token; lane = channel
-    const int d = d0 + lane;
-    for (int tl = wid; tl < NG; tl += kWarpsC) {
-      const long t = (long)base + tl;
-      gps[lane * Rg + tl] = (d < D && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
-    }
-  }
-  // each warp owns channel rows r = wid, wid + 8, ...: its taps in registers
+  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, i0, W, s, wid, lane);
   __syncthreads();
-  if (silu) {  // gp = dout * silu'(pre), pre recomputed with the forward's tap order
-    for (int r = wid; r < kConvTD; r += kWarpsC) {
-      const int d = d0 + r;
-      if (d >= D) continue;
-      float w[K];
+  const int d = d0 + lane, s0 = i0 + wid * kSeg;
+  if (d >= D || s0 >= L) return;
+  float w[K];
 #pragma unroll
-      for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
-      const float bv = bias ? __ldg(bias + d) : 0.0f;
+  for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
+  const float bv = bias ? __ldg(bias + d) : 0.0f;
+  const float* xr = s + lane * SP + wid * kSeg;  // column s0 + u + k at xr[u + k]
+  IO* o = out + ((long)b * L + s0) * D + d;
+  float xw[K];
 #pragma unroll
-      for (int tl = lane; tl < NG; tl += 32) {
-        const long t = (long)base + tl;
-        if (t < 0 || t >= L) continue;
-        float pre = bv;
+  for (int k = 1; k < K; k++) xw[k] = xr[k - 1];
+  const int n = min(kSeg, L - s0);
+  if (n == kSeg) {
 #pragma unroll
-        for (int k = 0; k < K; k++) pre = fmaf(sxs[r * Rs + tl + k], w[k], pre);
-        gps[r * Rg + tl] *= silu_gradf_(pre);
-      }
+    for (int u = 0; u < kSeg; u++) {
+#pragma unroll
+      for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
+      xw[K - 1] = xr[u + K - 1];
+      float acc = bv;
+#pragma unroll
+      for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
+      st(o + (long)u * D, silu ? siluf_(acc) : acc);
     }
-    __syncthreads();
+  } else {
+    for (int u = 0; u < n; u++) {
+#pragma unroll
+      for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
+      xw[K - 1] = xr[u + K - 1];
+      float acc = bv;
+#pragma unroll
+      for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
+      st(o + (long)u * D, silu ? siluf_(acc) : acc);
+    }
   }
-  const int nt = gridDim.y;
-  for (int r = wid; r < kConvTD; r += kWarpsC) {
-    const int d = d0 + r;
-    if (d >= D) continue;
+}
+
+template <typename IO, int K>
+__global__ void __launch_bounds__(kSegThreads, 3)
+conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                    const float* __restrict__ bias, const IO* __restrict__ dout,
+                    IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int silu) {
+  // sx columns i0-K+1 .. i0+TT+K-2 (inputs of tokens i0-K+1 .. i0+TT-1); later reused for the
+  // d_sx tile (columns i0 .. i0+TT-1).
+  constexpr int NC = kSegTT + 2 * K - 2, SP = NC | 1;
+  constexpr int NU = kSeg + K - 1;  // steps per thread: K-1 tokens before the segment, then it
+  __shared__ float s[kSegRows * SP];
+  __shared__ float red[(K + 1) * kSegWarps * 32];
+  const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
+  const long W = (long)L + K - 1;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
+  __syncthreads();
+  const int d = d0 + lane, s0 = i0 + wid * kSeg;
+  const bool active = d < D && s0 < W;
+  float ox[kSeg];
+  float pk[K + 1];
+#pragma unroll
+  for (int k = 0; k <= K; k++) pk[k] = 0.0f;
+  if (active) {
     float w[K];
 #pragma unroll
     for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
-    // d_sx columns [i0, i0+TT): lanes along time -> coalesced row stores
+    const float bv = bias ? __ldg(bias + d) : 0.0f;
+    // dout of tokens s0-K+1+u (zero outside [0, L)), all loads issued up front
+    float dv[NU];
+    const int t_first = s0 - (K - 1);
 #pragma unroll
-    for (int il = lane; il < kConvTT; il += 32) {
-      const long i = (long)i0 + il;
-      if (i < W) {
+    for (int u = 0; u < NU; u++) {
+      const int t = t_first + u;
+      dv[u] = (t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+    }
+    const float* xr = s + lane * SP + wid * kSeg;  // input column t_first + u + k at xr[u + k]
+    float xw[K], gw[K];
+#pragma unroll
+    for (int k = 1; k < K; k++) xw[k] = xr[k - 1];
+#pragma unroll
+    for (int k = 0; k < K; k++) gw[k] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+#pragma unroll
+      for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
+      xw[K - 1] = xr[u + K - 1];
+      float g = dv[u];
+      if (silu) {  // pre recomputed with the forward's tap order
+        float pre = bv;
+#pragma unroll
+        for (int k = 0; k < K; k++) pre = fmaf(xw[k], w[k], pre);
+        g *= silu_gradf_(pre);
+      }
+#pragma unroll
+      for (int k = K - 1; k > 0; k--) gw[k] = gw[k - 1];
+      gw[0] = g;  // gw[k] = gp of token t - k
+      if (u >= K - 1) {  // token t = s0 + u - K + 1 of the segment: d_sx[t], d_c terms
         float acc = 0.0f;
 #pragma unroll
-        for (int k = 0; k < K; k++) acc = fmaf(gps[r * Rg + il + K - 1 - k], w[k], acc);
-        st(d_sx + ((long)b * D + d) * W + i, acc);
-      }
-    }
-    // partial d_c[d][k] and d_bias[d] over the tokens this tile owns: lanes over tokens, then
-    // a fixed-order warp sum
-    float pk[K + 1];
+        for (int k = 0; k < K; k++) acc = fmaf(gw[k], w[k], acc);
+        ox[u - (K - 1)] = acc;
 #pragma unroll
-    for (int k = 0; k <= K; k++) pk[k] = 0.0f;
-#pragma unroll
-    for (int tl = lane; tl < kConvTT; tl += 32) {
-      if ((long)i0 + tl < L) {
-        const float g = gps[r * Rg + tl + K - 1];
-#pragma unroll
-        for (int k = 0; k < K; k++) pk[k] = fmaf(g, sxs[r * Rs + tl + K - 1 + k], pk[k]);
+        for (int k = 0; k < K; k++) pk[k] = fmaf(g, xw[k], pk[k]);  // g = 0 past L
         pk[K] += g;
       }
     }
+  }
 #pragma unroll
-    for (int k = 0; k <= K; k++) {
-      float v = pk[k];
+  for (int k = 0; k <= K; k++) red[(k * kSegWarps + wid) * 32 + lane] = pk[k];
+  __syncthreads();  // every thread is done with the sx tile
+  constexpr int SO = kSegTT | 1;
+  if (active) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) part[(((long)b * nt + blockIdx.y) * D + d) * (K + 1) + k] = v;
+    for (int u = 0; u < kSeg; u++) s[lane * SO + wid * kSeg + u] = ox[u];
+  }
+  const int nt = gridDim.y;
+  if (threadIdx.x < (K + 1) * 32) {  // fixed-order sum over the tile's 8 segments
+    const int k = threadIdx.x >> 5, dd = d0 + lane;
+    float v = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kSegWarps; q++) v += red[(k * kSegWarps + q) * 32 + lane];
+    if (dd < D) part[(((long)b * nt + blockIdx.y) * D + dd) * (K + 1) + k] = v;
+  }
+  __syncthreads();
+  // d_sx rows: columns [i0, min(i0 + TT, W)), 16-byte aligned groups + scalar edges
+  constexpr int V = 16 / sizeof(IO);
+  constexpr int NG = (kSegTT + V - 1) / V + 1;
+  const int n = (int)min((long)kSegTT, W - i0);
+  for (int idx = lane; idx < kRowsPerWarp * NG; idx += 32) {
+    const int q = idx / NG, gi = idx - q * NG;
+    const int r = wid + q * kSegWarps, dd = d0 + r;
+    if (dd >= D) continue;
+    IO* row = d_sx + ((long)b * D + dd) * W + i0;
+    const int ph = (int)(((uintptr_t)row & 15) / sizeof(IO));
+    const int j0 = gi * V - ph;
+    if (j0 >= n) continue;
+    const float* src = s + r * SO + j0;
+    if (j0 >= 0 && j0 + V <= n) {
+      float v[V];
+#pragma unroll
+      for (int e = 0; e < V; e++) v[e] = src[e];
+      *reinterpret_cast<uint4*>(row + j0) = pack16<IO>(v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; e++)
+        if (j0 + e >= 0 && j0 + e < n) st(row + j0 + e, src[e]);
     }
   }
 }
@@ -321,11 +428,12 @@ static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias,
   dim3 grid((D + kConvTD - 1) / kConvTD, (L + kConvTT - 1) / kConvTT, n_s);
   const IO* x = (const IO*)sx;
   IO* o = (IO*)out;
+  const dim3 gseg((D + kSegRows - 1) / kSegRows, (L + kSegTT - 1) / kSegTT, n_s);
   switch (K) {
-    case 1: conv_fwd_k_kernel<IO, 1><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 2: conv_fwd_k_kernel<IO, 2><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 3: conv_fwd_k_kernel<IO, 3><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 4: conv_fwd_k_kernel<IO, 4><<<grid, kConvThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 1: conv_fwd_seg_kernel<IO, 1><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 2: conv_fwd_seg_kernel<IO, 2><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 3: conv_fwd_seg_kernel<IO, 3><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 4: conv_fwd_seg_kernel<IO, 4><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
     default: {
       size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
       conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, o, D, L, K, silu);
@@ -346,7 +454,8 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
                               void* d_sx, float* d_c, float* d_bias, void* ws, int n_s, int D,
                               int L, int K, int silu, cudaStream_t st) {
   long W = (long)L + K - 1;
-  int nt = (int)((W + kConvTT - 1) / kConvTT);
+  const int tt = K <= 4 ? kSegTT : kConvTT;
+  int nt = (int)((W + tt - 1) / tt);
   dim3 grid((D + kConvTD - 1) / kConvTD, nt, n_s);
   size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + 2 * K - 2) +
                                  kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
@@ -355,10 +464,10 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
   const IO* g = (const IO*)dout;
   IO* dx = (IO*)d_sx;
   switch (K) {
-    case 1: conv_bwd_k_kernel<IO, 1><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 2: conv_bwd_k_kernel<IO, 2><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 3: conv_bwd_k_kernel<IO, 3><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 4: conv_bwd_k_kernel<IO, 4><<<grid, kConvThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 1: conv_bwd_seg_kernel<IO, 1><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 2: conv_bwd_seg_kernel<IO, 2><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 3: conv_bwd_seg_kernel<IO, 3><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 4: conv_bwd_seg_kernel<IO, 4><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
     default:
       conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, g, dx, part, D, L, K, silu);
   }

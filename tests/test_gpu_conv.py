@@ -17,6 +17,11 @@ CASES = [
     (2, 64, 200, 7, "bf16", True, True),
     (1, 5, 2, 4, "f32", True, True),        # L < K
     (2, 40, 300, 64, "f32", True, True),    # the largest supported K
+    (3, 45, 513, 4, "bf16", True, True),    # 256-token tiles: 3 tiles, ragged channels
+    (2, 32, 512, 4, "bf16", False, True),   # L a multiple of the tile: a tail tile of K-1 columns
+    (2, 19, 300, 2, "bf16", True, False),   # K = 2 without SiLU
+    (1, 64, 256, 4, "f32", True, True),     # one full tile, fp32
+    (4, 7, 777, 3, "f32", False, True),     # rows of every alignment, several tiles
 ]
 
 
