@@ -30,7 +30,14 @@ __device__ __forceinline__ float ex2(float v) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
-__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + ex2(-v * kLog2e)); }
+// 1/v by the SFU instruction (at most 1 ulp off; 1/inf = 0).
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+// The denominator 1 + 2^(-v log2 e) lies in [1, inf], where the SFU reciprocal needs no fix-up.
+__device__ __forceinline__ float sigmoidf_(float v) { return rcp_approx(1.0f + ex2(-v * kLog2e)); }
 __device__ __forceinline__ float siluf_(float v) { return v * sigmoidf_(v); }
 // d/dv silu(v) = s (1 + v (1 - s)),  s = sigmoid(v)   (silu_grad_from_sigmoid)
 __device__ __forceinline__ float silu_gradf_(float v) {

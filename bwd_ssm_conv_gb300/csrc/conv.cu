@@ -294,10 +294,19 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
   const long W = (long)L + K - 1;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
-  __syncthreads();
   const int d = d0 + lane, s0 = i0 + wid * kSeg;
   const bool active = d < D && s0 < W;
+  // dout of tokens s0-K+1+u (zero outside [0, L)), issued before the sx tile so that both
+  // loads are in flight together
+  float dv[NU];
+  const int t_first = s0 - (K - 1);
+#pragma unroll
+  for (int u = 0; u < NU; u++) {
+    const int t = t_first + u;
+    dv[u] = (active && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+  }
+  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
+  __syncthreads();
   float ox[kSeg];
   float pk[K + 1];
 #pragma unroll
@@ -307,14 +316,6 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
 #pragma unroll
     for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
     const float bv = bias ? __ldg(bias + d) : 0.0f;
-    // dout of tokens s0-K+1+u (zero outside [0, L)), all loads issued up front
-    float dv[NU];
-    const int t_first = s0 - (K - 1);
-#pragma unroll
-    for (int u = 0; u < NU; u++) {
-      const int t = t_first + u;
-      dv[u] = (t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
-    }
     const float* xr = s + lane * SP + wid * kSeg;  // input column t_first + u + k at xr[u + k]
     float xw[K], gw[K];
 #pragma unroll
