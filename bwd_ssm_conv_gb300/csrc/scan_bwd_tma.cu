@@ -9,7 +9,8 @@
 // -- delta, the gate, dy silu'(z), softplus' -- is done once by the whole block in a
 // prepass, so the per-state loops carry only the recurrence (packed f32x2 arithmetic);
 // the per-channel sums over states go through shared memory to an epilogue that writes
-// dx, dz and ddt, and the dB/dC sums over channels use a transposed warp butterfly.
+// dx, dz and ddt, and the dB/dC sums over channels use a warp butterfly whose exchanges need no
+// lane-dependent selects (each thread's states sit in registers in a lane-permuted order).
 //
 // Per chunk (last to first): level 1 walks the chunk's tiles forward from the checkpoint,
 // saving the state at every 8-token sub-chunk start (global scratch, re-read from L2);
@@ -79,30 +80,6 @@ __device__ __forceinline__ float f2_sum(f2_t v) {
   return lo + hi;
 }
 
-// v holds 8 partials; lanes that differ in bits 2..4 hold other channels.  Returns the sum over
-// those 8 lanes of the partial with original index (lane >> 2) & 7.
-__device__ __forceinline__ float reduce8_transposed(float (&v)[8], int lane) {
-  {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  }
-  {
-    const bool up = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-      const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-  }
-  const bool up = lane & 4;
-  const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-  return keep + __shfl_xor_sync(0xffffffffu, send, 4);
-}
-
 // B (and C) of a tile as fp32: the staged tile itself for fp32 I/O, else converted once.
 template <typename IO>
 __device__ __forceinline__ const float* tile_rows_f32(const unsigned char* stage_rows, float* conv,
@@ -117,8 +94,43 @@ __device__ __forceinline__ const float* tile_rows_f32(const unsigned char* stage
   }
 }
 
+// Register slot j of a thread holds state n0 + (j ^ p), p = lane bits 3..4 (see the dB/dC sums
+// below).  B and C of a tile are kept as fp32 in 4 copies, copy p holding within every group of 4
+// states the order (j ^ p), so that each lane reads its slots with one 16-byte load.
 template <typename IO>
-__global__ void __launch_bounds__(kScanThreads)
+__device__ __forceinline__ void tile_rows_perm(const unsigned char* stage_rows, float* dst, int count) {
+  const IO* src = reinterpret_cast<const IO*>(stage_rows);
+  for (int idx = threadIdx.x; idx < count; idx += kScanThreads) {
+    const float v = lds_f(src + idx);
+    const int base = idx & ~3, j = idx & 3;
+#pragma unroll
+    for (int pc = 0; pc < 4; pc++) dst[pc * count + base + (j ^ pc)] = v;
+  }
+}
+
+// Sums the dB and dC products of a token over the 8 channels of a warp (lane bits 2..4).  Slot j
+// holds state n0 + (j ^ p) with p = lane bits 3..4, so at the exchanges over bit 4 (slots 2,3 go
+// out, 0,1 stay) and bit 3 (slot 1 out, slot 0 stays) the partner always sends the states this lane
+// keeps: no lane-dependent selects.  The last exchange (bit 2) is a plain sum.  Returns the totals
+// (dB, dC) of state n0 + p, identical on the lane pair that differs in bit 2.
+__device__ __forceinline__ f2_t reduce_bc_warp(f2_t dB01, f2_t dB23, f2_t dC01, f2_t dC23) {
+  float b2, b3, c2, c3;
+  f2_unpack(dB23, b2, b3);
+  f2_unpack(dC23, c2, c3);
+  const f2_t rb = f2_pack(__shfl_xor_sync(0xffffffffu, b2, 16), __shfl_xor_sync(0xffffffffu, b3, 16));
+  const f2_t rc = f2_pack(__shfl_xor_sync(0xffffffffu, c2, 16), __shfl_xor_sync(0xffffffffu, c3, 16));
+  float wb0, wb1, wc0, wc1;
+  f2_unpack(f2_add(dB01, rb), wb0, wb1);
+  f2_unpack(f2_add(dC01, rc), wc0, wc1);
+  const f2_t x = f2_add(f2_pack(wb0, wc0), f2_pack(__shfl_xor_sync(0xffffffffu, wb1, 8),
+                                                   __shfl_xor_sync(0xffffffffu, wc1, 8)));
+  float xb, xc;
+  f2_unpack(x, xb, xc);
+  return f2_add(x, f2_pack(__shfl_xor_sync(0xffffffffu, xb, 4), __shfl_xor_sync(0xffffffffu, xc, 4)));
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kScanThreads, 3)
 scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;
   constexpr int TT = kBwdTile, CB = kCB, N = 16;
@@ -127,6 +139,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const Lane l = lane_of(a);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
+  const int pm = (lane >> 3) & 3;  // slot j holds state n0 + (j ^ pm)
   const int s = blockIdx.y, b = blockIdx.z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
   float4* sP = reinterpret_cast<float4*>(smem + m.off_p);        // [TT][CB] (delta, x, gy, dyg)
@@ -197,15 +210,17 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   f2_t A2p[2], Anp[2], carry2[2], dA2[2] = {0ull, 0ull}, hp[2] = {0ull, 0ull};
   {
     const long si = ((long)b * a.S + s) * p.HP + ch;
-    float cv[4];
+    float cv[4], av[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-      if (a.S > 1) cv[j] = a.segend[si * N + n0 + j];
-      else cv[j] = a.g.d_state_out ? __ldg(a.g.d_state_out + ((long)b * p.HP + ch) * N + n0 + j) : 0.0f;
+      const int n = n0 + (j ^ pm);
+      if (a.S > 1) cv[j] = a.segend[si * N + n];
+      else cv[j] = a.g.d_state_out ? __ldg(a.g.d_state_out + ((long)b * p.HP + ch) * N + n) : 0.0f;
+      av[j] = __ldg(p.A + (long)ch * N + n);
     }
 #pragma unroll
     for (int q = 0; q < 2; q++) {
-      const float a0 = __ldg(p.A + (long)ch * N + n0 + 2 * q), a1 = __ldg(p.A + (long)ch * N + n0 + 2 * q + 1);
+      const float a0 = av[2 * q], a1 = av[2 * q + 1];
       Anp[q] = f2_pack(a0, a1);
       A2p[q] = f2_pack(a0 * kLog2e, a1 * kLog2e);
       carry2[q] = f2_pack(cv[2 * q], cv[2 * q + 1]);
@@ -256,18 +271,20 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       }
       sP[idx] = make_float4(dl, xv, gy, dyg);
     }
-    const float* sBf = tile_rows_f32<IO>(base + m.off_b, reinterpret_cast<float*>(smem + m.off_bf), TT * N);
-    const float* sCf = cs.lvl == 1
-        ? tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N)
-        : nullptr;
+    float* const sBq = reinterpret_cast<float*>(smem + m.off_bf);
+    float* const sCq = reinterpret_cast<float*>(smem + m.off_cf);
+    tile_rows_perm<IO>(base + m.off_b, sBq, TT * N);
+    if (cs.lvl == 1) tile_rows_perm<IO>(base + m.off_c, sCq, TT * N);
+    const float* sBf = sBq + pm * TT * N;  // this lane's copy
+    const float* sCf = sCq + pm * TT * N;
     __syncthreads();
 
     if (cs.lvl == 0) {
       // ---- level 1: walk the tile forward, keeping every sub-chunk's start state ----------
       if (cs.j == 0) {
         const float* src = a.ckpt + (((long)b * a.nch_b + cs.ck) * p.HP + ch) * N + n0;
-        hp[0] = f2_pack(src[0], src[1]);
-        hp[1] = f2_pack(src[2], src[3]);
+        hp[0] = f2_pack(src[0 ^ pm], src[1 ^ pm]);
+        hp[1] = f2_pack(src[2 ^ pm], src[3 ^ pm]);
       }
       auto token = [&](int i) {
         if (i % kTsub == 0) {
@@ -355,14 +372,10 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
           sPB[i * kScanThreads + tid] = f2_sum(sB2);
           sPA[i * kScanThreads + tid] = f2_sum(sAw2);
           sPY[i * kScanThreads + tid] = f2_sum(yp2);
-          float v8[8];
-          f2_unpack(dB2[0], v8[0], v8[1]);
-          f2_unpack(dB2[1], v8[2], v8[3]);
-          f2_unpack(dC2[0], v8[4], v8[5]);
-          f2_unpack(dC2[1], v8[6], v8[7]);
-          const float tot = reduce8_transposed(v8, lane);
-          const int o = (lane >> 2) & 7;  // 0..3: dB of state n0+o, 4..7: dC of state n0+o-4
-          red[(i * kWarps + warp) * 2 * N + (o >> 2) * N + n0 + (o & 3)] = tot;
+          float tb, tc;
+          f2_unpack(reduce_bc_warp(dB2[0], dB2[1], dC2[0], dC2[1]), tb, tc);
+          const int hi = (lane >> 2) & 1;  // of the lane pair: 0 writes dB, 1 writes dC
+          red[(i * kWarps + warp) * 2 * N + hi * N + n0 + pm] = hi ? tc : tb;
         }
       }
     };
@@ -422,10 +435,11 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const long si = ((long)b * a.S + s) * p.HP + ch;
 #pragma unroll
   for (int q = 0; q < 2; q++) {
-    f2_unpack(dA2[q], a.dA_part[si * N + n0 + 2 * q], a.dA_part[si * N + n0 + 2 * q + 1]);
+    const int n_lo = n0 + ((2 * q) ^ pm), n_hi = n0 + ((2 * q + 1) ^ pm);
+    f2_unpack(dA2[q], a.dA_part[si * N + n_lo], a.dA_part[si * N + n_hi]);
     if (s == 0)
-      f2_unpack(carry2[q], a.dh0[((long)b * p.HP + ch) * N + n0 + 2 * q],
-                a.dh0[((long)b * p.HP + ch) * N + n0 + 2 * q + 1]);
+      f2_unpack(carry2[q], a.dh0[((long)b * p.HP + ch) * N + n_lo],
+                a.dh0[((long)b * p.HP + ch) * N + n_hi]);
   }
   sAcc[(warp * CB + (tid % CB)) * 2] = dD_acc;
   sAcc[(warp * CB + (tid % CB)) * 2 + 1] = dtb_acc;
@@ -572,8 +586,8 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   auto take = [&](uint32_t bytes) { uint32_t o = off; off = al(off + bytes); return o; };
   m->off_p = take(TT * cb * 16);
   m->off_spg = take(TT * cb * 4);
-  m->off_bf = take(TT * p.N * 4);
-  m->off_cf = take(TT * p.N * 4);
+  m->off_bf = take(4 * TT * p.N * 4);  // 4 permuted copies (main kernel); copy 0 also serves
+  m->off_cf = take(4 * TT * p.N * 4);  // the local kernel
   m->off_part = take(3 * TT * kScanThreads * 4);
   m->off_red = take(TT * kWarps * 2 * p.N * 4);
   m->out_tile = al(tile);
