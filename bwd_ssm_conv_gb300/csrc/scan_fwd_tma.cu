@@ -74,6 +74,11 @@ __device__ __forceinline__ void lds_row(const IO* ptr, float (&out)[NS]) {
   }
 }
 
+// A bf16 pair (one 32-bit word, low half first) as a packed fp32 pair; exact.
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 template <typename IO, int NS, int TPC, bool LOCAL>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
@@ -93,7 +98,9 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   const uint32_t bytes = LOCAL ? a.bytes_local : a.bytes_main;
   const bool want_y = !LOCAL && a.has_y;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
-  float4* sDD = reinterpret_cast<float4*>(smem + a.off_dl);  // [TT][cb] (delta, delta, dx, dx)
+  float2* sDD = reinterpret_cast<float2*>(smem + a.off_dl);  // [TT][cb] (delta, delta x)
+  // [TT][N/4]: per token and group of 4 states, B then C as 8 bf16 (one 16-byte load per lane)
+  uint4* sBC = reinterpret_cast<uint4*>(smem + a.off_bf);
   float* sACC = reinterpret_cast<float*>(smem + a.off_acc);  // [TT][cb * tpc] partial C . h
   float* sPar = reinterpret_cast<float*>(smem + a.off_par);  // [cb] D, [cb] dt_bias
 
@@ -164,25 +171,16 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       float dl = lds1(sdt + idx);
       if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
       const float dx = dl * lds1(sx + idx);
-      sDD[idx] = make_float4(dl, dl, dx, dx);
+      sDD[idx] = make_float2(dl, dx);
       (void)i;
     }
-    const float* sBf;
-    const float* sCf;
-    if constexpr (sizeof(IO) == 4) {
-      sBf = reinterpret_cast<const float*>(base + a.off_b);
-      sCf = reinterpret_cast<const float*>(base + a.off_c);
-    } else {
-      float* wB = reinterpret_cast<float*>(smem + a.off_bf);
-      float* wC = reinterpret_cast<float*>(smem + a.off_cf);
-      const IO* rB = reinterpret_cast<const IO*>(base + a.off_b);
-      const IO* rC = reinterpret_cast<const IO*>(base + a.off_c);
-      for (int idx = tid; idx < TT * N; idx += kScanThreads) {
-        wB[idx] = lds1(rB + idx);
-        if (!LOCAL) wC[idx] = lds1(rC + idx);
+    {
+      const uint2* rB = reinterpret_cast<const uint2*>(base + a.off_b);
+      const uint2* rC = reinterpret_cast<const uint2*>(base + a.off_c);
+      for (int idx = tid; idx < TT * N / 4; idx += kScanThreads) {
+        const uint2 vb = rB[idx], vc = LOCAL ? make_uint2(0u, 0u) : rC[idx];
+        sBC[idx] = make_uint4(vb.x, vb.y, vc.x, vc.y);
       }
-      sBf = wB;
-      sCf = wC;
     }
     __syncthreads();
 
@@ -198,16 +196,19 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
     }
     auto token = [&](int i) {
-      const float4 dd = sDD[i * cb + cl];
-      const f2_t dl2 = f2_pack(dd.x, dd.y), dx2 = f2_pack(dd.z, dd.w);
-      f2_t B2[NS / 2];
+      const float2 dd = sDD[i * cb + cl];
+      const f2_t dl2 = f2_pack(dd.x, dd.x), dx2 = f2_pack(dd.y, dd.y);
+      f2_t B2[NS / 2], C2[NS / 2];
 #pragma unroll
       for (int j = 0; j < NS; j += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0 + j);
-        B2[j / 2] = f2_pack(v.x, v.y);
-        B2[j / 2 + 1] = f2_pack(v.z, v.w);
+        const uint4 v = sBC[(i * N + n0 + j) / 4];
+        B2[j / 2] = bf2_to_f2(v.x);
+        B2[j / 2 + 1] = bf2_to_f2(v.y);
+        C2[j / 2] = bf2_to_f2(v.z);
+        C2[j / 2 + 1] = bf2_to_f2(v.w);
       }
       if (LOCAL) {
+        (void)C2;
 #pragma unroll
         for (int j = 0; j < NS / 2; j++)
           hp[j] = f2_fma(f2_ex2(f2_mul(dl2, A2p[j])), hp[j], f2_mul(dx2, B2[j]));
@@ -216,12 +217,11 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         f2_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
         for (int j = 0; j < NS; j += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(sCf + i * N + n0 + j);
           const int q = j / 2;
           hp[q] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q])), hp[q], f2_mul(dx2, B2[q]));
           hp[q + 1] = f2_fma(f2_ex2(f2_mul(dl2, A2p[q + 1])), hp[q + 1], f2_mul(dx2, B2[q + 1]));
-          acc0 = f2_fma(f2_pack(v.x, v.y), hp[q], acc0);
-          acc1 = f2_fma(f2_pack(v.z, v.w), hp[q + 1], acc1);
+          acc0 = f2_fma(C2[q], hp[q], acc0);
+          acc1 = f2_fma(C2[q + 1], hp[q + 1], acc1);
         }
         float lo, hi;
         f2_unpack(f2_add(acc0, acc1), lo, hi);
@@ -419,11 +419,11 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_c = a.off_b + al(row);
   a.stage_stride = a.off_c + al(row);
   const uint32_t f_tile = (uint32_t)(q.tt * q.cb * 4), f_row = (uint32_t)(q.tt * p.N * 4);
-  a.off_dl = kFwdStages * a.stage_stride;         // float4 (delta, delta, dx, dx) per item
-  a.off_dx = a.off_dl + al(4 * f_tile);
-  a.off_bf = a.off_dx;
-  a.off_cf = a.off_bf + al(f_row);
-  a.off_acc = a.off_cf + al(f_row);
+  a.off_dl = kFwdStages * a.stage_stride;         // float2 (delta, delta x) per item
+  a.off_dx = a.off_dl + al(2 * f_tile);
+  a.off_bf = a.off_dx;                            // interleaved bf16 B, C: TT x N x 2 x 2 bytes
+  a.off_cf = a.off_bf;
+  a.off_acc = a.off_bf + al(f_row);
   a.off_par = a.off_acc + al((uint32_t)(q.tt * kScanThreads * 4));
   a.off_y = a.off_par + al((uint32_t)(2 * q.cb * 4));
   a.y_stride = al(tile);
