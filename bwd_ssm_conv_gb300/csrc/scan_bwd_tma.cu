@@ -32,7 +32,7 @@ struct BwdTma {
   CUtensorMap mx, mdt, mz, mdy, mb, mc, mdx, mdz, mddt;
   uint32_t bytes_l1, bytes_l2, bytes_loc;
   uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
-  uint32_t off_p, off_spg, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
+  uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
   float4* bnd;
 };
@@ -108,6 +108,34 @@ __device__ __forceinline__ void tile_rows_perm(const unsigned char* stage_rows, 
   }
 }
 
+// A bf16 pair (one 32-bit word, low half first) as a packed fp32 pair; exact.
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// Four bf16 (two words) with their order permuted by j -> j ^ pc.
+__device__ __forceinline__ uint2 perm4_bf16(uint2 v, int pc) {
+  if (pc & 1) {
+    v.x = __byte_perm(v.x, 0u, 0x1032);
+    v.y = __byte_perm(v.y, 0u, 0x1032);
+  }
+  return (pc & 2) ? make_uint2(v.y, v.x) : v;
+}
+// bf16 I/O: B and C of a tile as [4 copies][TT][N/4] records of 8 bf16 (B of 4 states, then C
+// of the same 4 states), copy pc in the order (j ^ pc); C is left out on level-1 tiles.
+__device__ __forceinline__ void tile_bc_perm_bf16(const unsigned char* rb, const unsigned char* rc,
+                                                  uint4* dst, int groups, bool with_c) {
+  const uint2* b2 = reinterpret_cast<const uint2*>(rb);
+  const uint2* c2 = reinterpret_cast<const uint2*>(rc);
+  for (int idx = threadIdx.x; idx < groups; idx += kScanThreads) {
+    const uint2 vb = b2[idx], vc = with_c ? c2[idx] : make_uint2(0u, 0u);
+#pragma unroll
+    for (int pc = 0; pc < 4; pc++) {
+      const uint2 pb = perm4_bf16(vb, pc), pcv = perm4_bf16(vc, pc);
+      dst[pc * groups + idx] = make_uint4(pb.x, pb.y, pcv.x, pcv.y);
+    }
+  }
+}
+
 // Sums the dB and dC products of a token over the 8 channels of a warp (lane bits 2..4).  Slot j
 // holds state n0 + (j ^ p) with p = lane bits 3..4, so at the exchanges over bit 4 (slots 2,3 go
 // out, 0,1 stay) and bit 3 (slot 1 out, slot 0 stays) the partner always sends the states this lane
@@ -142,8 +170,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int pm = (lane >> 3) & 3;  // slot j holds state n0 + (j ^ pm)
   const int s = blockIdx.y, b = blockIdx.z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  float4* sP = reinterpret_cast<float4*>(smem + m.off_p);        // [TT][CB] (delta, x, gy, dyg)
-  float* sSPG = reinterpret_cast<float*>(smem + m.off_spg);      // [TT][CB] softplus'(pre)
+  float2* sD2 = reinterpret_cast<float2*>(smem + m.off_p);       // [TT][CB] (delta, delta x)
+  float* sGy = reinterpret_cast<float*>(smem + m.off_spg);       // [TT][CB] gy = dy silu(z)
+  float4* sE = reinterpret_cast<float4*>(smem + m.off_e);        // [TT][CB] (x, gy, dyg, softplus')
   float* sPB = reinterpret_cast<float*>(smem + m.off_part);      // [TT][threads] sum_n dh B
   float* sPA = sPB + TT * kScanThreads;                           // [TT][threads] sum_n A w
   float* sPY = sPA + TT * kScanThreads;                           // [TT][threads] sum_n C h
@@ -258,25 +287,57 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       const float pre = raw + sPar[CB + c];
       const float dl = p.softplus ? softplusf_(pre) : raw;
       const float xv = lds_f(sx + idx);
-      float gy = 0.0f, dyg = 0.0f;
       if (cs.lvl == 1) {
         const float dyv = lds_f(sdy + idx);
-        gy = dyv;
+        float gy = dyv, dyg = 0.0f;
         if (p.z) {
           const float zv = lds_f(sz + idx), sgm = sigmoidf_(zv);
           gy = dyv * zv * sgm;
           dyg = dyv * sgm * (1.0f + zv * (1.0f - sgm));
         }
-        if (p.softplus) sSPG[idx] = softplus_gradf_(pre);
+        sGy[idx] = gy;
+        sE[idx] = make_float4(xv, gy, dyg, p.softplus ? softplus_gradf_(pre) : 1.0f);
       }
-      sP[idx] = make_float4(dl, xv, gy, dyg);
+      sD2[idx] = make_float2(dl, dl * xv);
     }
-    float* const sBq = reinterpret_cast<float*>(smem + m.off_bf);
-    float* const sCq = reinterpret_cast<float*>(smem + m.off_cf);
-    tile_rows_perm<IO>(base + m.off_b, sBq, TT * N);
-    if (cs.lvl == 1) tile_rows_perm<IO>(base + m.off_c, sCq, TT * N);
-    const float* sBf = sBq + pm * TT * N;  // this lane's copy
-    const float* sCf = sCq + pm * TT * N;
+    // B and C: this lane's permuted copy (bf16 records for bf16 I/O, fp32 rows otherwise)
+    const uint4* sBCq = reinterpret_cast<const uint4*>(smem + m.off_bf) + pm * (TT * N / 4);
+    const float* sBf = reinterpret_cast<const float*>(smem + m.off_bf) + pm * TT * N;
+    const float* sCf = reinterpret_cast<const float*>(smem + m.off_cf) + pm * TT * N;
+    if constexpr (sizeof(IO) == 2) {
+      tile_bc_perm_bf16(base + m.off_b, base + m.off_c, reinterpret_cast<uint4*>(smem + m.off_bf),
+                        TT * N / 4, cs.lvl == 1);
+    } else {
+      tile_rows_perm<IO>(base + m.off_b, reinterpret_cast<float*>(smem + m.off_bf), TT * N);
+      if (cs.lvl == 1) tile_rows_perm<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N);
+    }
+    auto ld_b = [&](int i, f2_t (&B2)[2]) {
+      if constexpr (sizeof(IO) == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(sBCq + i * (N / 4) + (n0 >> 2));
+        B2[0] = bf2_to_f2(v.x);
+        B2[1] = bf2_to_f2(v.y);
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0);
+        B2[0] = f2_pack(v.x, v.y);
+        B2[1] = f2_pack(v.z, v.w);
+      }
+    };
+    auto ld_bc = [&](int i, f2_t (&B2)[2], f2_t (&C2)[2]) {
+      if constexpr (sizeof(IO) == 2) {
+        const uint4 v = sBCq[i * (N / 4) + (n0 >> 2)];
+        B2[0] = bf2_to_f2(v.x);
+        B2[1] = bf2_to_f2(v.y);
+        C2[0] = bf2_to_f2(v.z);
+        C2[1] = bf2_to_f2(v.w);
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(sBf + i * N + n0);
+        const float4 w = *reinterpret_cast<const float4*>(sCf + i * N + n0);
+        B2[0] = f2_pack(v.x, v.y);
+        B2[1] = f2_pack(v.z, v.w);
+        C2[0] = f2_pack(w.x, w.y);
+        C2[1] = f2_pack(w.z, w.w);
+      }
+    };
     __syncthreads();
 
     if (cs.lvl == 0) {
@@ -293,13 +354,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
           f2_unpack(hp[1], h2, h3);
           bnd[(cs.j * (TT / kTsub) + i / kTsub) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
         }
-        const float4 p4 = sP[i * CB + cl];
-        const f2_t dl2 = f2_pack(p4.x, p4.x);
-        const float dx = p4.x * p4.y;
-        const f2_t dx2 = f2_pack(dx, dx);
-        const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
-        hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
-        hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+        const float2 d2 = sD2[i * CB + cl];
+        const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
+        f2_t B2[2];
+        ld_b(i, B2);
+        hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, B2[0]));
+        hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, B2[1]));
       };
       if (cnt == TT) {  // full tile: no per-token branch, so tokens can interleave
 #pragma unroll
@@ -328,15 +388,14 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 #pragma unroll
       for (int r = 0; r < kTsub; r++) {
         if (FULL || r < c8) {
-          const float4 p4 = sP[(i0 + r) * CB + cl];
-          const f2_t dl2 = f2_pack(p4.x, p4.x);
-          const float dx = p4.x * p4.y;
-          const f2_t dx2 = f2_pack(dx, dx);
-          const float4 bv = *reinterpret_cast<const float4*>(sBf + (i0 + r) * N + n0);
+          const float2 d2 = sD2[(i0 + r) * CB + cl];
+          const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
+          f2_t B2[2];
+          ld_b(i0 + r, B2);
           aa[r][0] = decay2<ACC>(dl2, A2p[0]);
           aa[r][1] = decay2<ACC>(dl2, A2p[1]);
-          hh[r + 1][0] = step2<ACC>(aa[r][0], hh[r][0], f2_mul(dx2, f2_pack(bv.x, bv.y)));
-          hh[r + 1][1] = step2<ACC>(aa[r][1], hh[r][1], f2_mul(dx2, f2_pack(bv.z, bv.w)));
+          hh[r + 1][0] = step2<ACC>(aa[r][0], hh[r][0], f2_mul(dx2, B2[0]));
+          hh[r + 1][1] = step2<ACC>(aa[r][1], hh[r][1], f2_mul(dx2, B2[1]));
         } else {
           aa[r][0] = aa[r][1] = 0ull;
           hh[r + 1][0] = hh[r][0];
@@ -347,14 +406,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       for (int r = kTsub - 1; r >= 0; r--) {
         if (FULL || r < c8) {  // uniform over the block
           const int i = i0 + r;
-          const float4 p4 = sP[i * CB + cl];
-          const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.z, p4.z);
-          const float dlx = p4.x * p4.y;
-          const f2_t dlx2 = f2_pack(dlx, dlx);
-          const float4 bv = *reinterpret_cast<const float4*>(sBf + i * N + n0);
-          const float4 cv = *reinterpret_cast<const float4*>(sCf + i * N + n0);
-          const f2_t B2[2] = {f2_pack(bv.x, bv.y), f2_pack(bv.z, bv.w)};
-          const f2_t C2[2] = {f2_pack(cv.x, cv.y), f2_pack(cv.z, cv.w)};
+          const float2 d2 = sD2[i * CB + cl];
+          const float gyv = sGy[i * CB + cl];
+          const f2_t dl2 = f2_pack(d2.x, d2.x), gy2 = f2_pack(gyv, gyv);
+          const f2_t dlx2 = f2_pack(d2.y, d2.y);
+          f2_t B2[2], C2[2];
+          ld_bc(i, B2, C2);
           f2_t sB2 = 0ull, sAw2 = 0ull, yp2 = 0ull, dB2[2], dC2[2];
 #pragma unroll
           for (int q = 0; q < 2; q++) {
@@ -401,14 +458,15 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       const float sBt = (vb.x + vb.y) + (vb.z + vb.w);
       const float sAwt = (va.x + va.y) + (va.z + va.w);
       const float ypt = (vy.x + vy.y) + (vy.z + vy.w);
-      const float4 p4 = sP[idx];
+      const float4 e4 = sE[idx];                  // (x, gy, dyg, softplus')
+      const float dl = sD2[idx].x;
       const float D = sPar[c];
-      const float ddl = fmaf(p4.y, sBt, sAwt);
-      const float ddt = p.softplus ? ddl * sSPG[idx] : ddl;
-      sts_f(odx + idx, fmaf(p4.z, D, p4.x * sBt));
-      sts_f(odz + idx, p4.w * fmaf(D, p4.y, ypt));
+      const float ddl = fmaf(e4.x, sBt, sAwt);
+      const float ddt = p.softplus ? ddl * e4.w : ddl;
+      sts_f(odx + idx, fmaf(e4.y, D, dl * sBt));
+      sts_f(odz + idx, e4.z * fmaf(D, e4.x, ypt));
       sts_f(oddt + idx, ddt);
-      dD_acc = fmaf(p4.z, p4.y, dD_acc);
+      dD_acc = fmaf(e4.y, e4.x, dD_acc);
       dtb_acc += ddt;
     }
     for (int idx = tid; idx < cnt * 2 * N; idx += kScanThreads) {
@@ -469,7 +527,7 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
   const int s = blockIdx.y + 1, b = blockIdx.z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  float4* sP = reinterpret_cast<float4*>(smem + m.off_p);
+  float4* sP = reinterpret_cast<float4*>(smem + m.off_e);
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);
   const int t_begin = s * a.seg_chunks * a.chunk_b;
   const int t_end = min(p.L, t_begin + a.seg_chunks * a.chunk_b);
@@ -584,10 +642,13 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->stage_stride = m->off_c + al(row);
   uint32_t off = kBwdStages * m->stage_stride;
   auto take = [&](uint32_t bytes) { uint32_t o = off; off = al(off + bytes); return o; };
-  m->off_p = take(TT * cb * 16);
+  m->off_p = take(TT * cb * 8);
   m->off_spg = take(TT * cb * 4);
-  m->off_bf = take(4 * TT * p.N * 4);  // 4 permuted copies (main kernel); copy 0 also serves
-  m->off_cf = take(4 * TT * p.N * 4);  // the local kernel
+  m->off_e = take(TT * cb * 16);
+  // B, C in 4 permuted copies: bf16 records (B and C together) or fp32 rows; off_cf also holds
+  // the local kernel's fp32 C rows
+  m->off_bf = take(io == 2 ? 4 * TT * p.N * 4 : 4 * TT * p.N * 4);
+  m->off_cf = take(io == 2 ? TT * p.N * 4 : 4 * TT * p.N * 4);
   m->off_part = take(3 * TT * kScanThreads * 4);
   m->off_red = take(TT * kWarps * 2 * p.N * 4);
   m->out_tile = al(tile);
