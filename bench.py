@@ -16,6 +16,7 @@ independent replica (the path has no cross-GPU exchange), value = all tokens / m
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -62,6 +63,38 @@ def alg_bytes(w) -> dict:
 SCAN_FLOPS = {"scan_fwd": 6, "scan_bwd": 22}
 FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (packed f32x2
                           # issues half the instructions at the same lane rate)
+
+
+# DRAM traffic of the dominant kernel per launch, from one ncu capture of this workload
+# (dram__bytes_read.sum + dram__bytes_write.sum; summary in profiles/).  Reported only while the
+# kernel's sources hash to what was captured; any edit makes it null until it is captured again.
+TRAFFIC_CAPTURES = {
+    "scan_bwd": {
+        "kernel": "scan_bwd_tma_kernel<bf16>",
+        "bytes": 472636928 + 671771136,
+        "sources": {
+            "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
+                "ba17adf4abf05e68d12daf15bcb9993c2a33ac1a8dbf9f827b519fa7babd14ef",
+            "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
+                "02495c2a1664a92abfc2ed6cd2cd1cfb1ad3cbced02778247fb73bbd0072dbbe",
+        },
+    },
+}
+
+
+def captured_traffic(stage: str):
+    """(bytes, kernel) of the capture for `stage` if its sources are unchanged, else (None, None)."""
+    cap = TRAFFIC_CAPTURES.get(stage)
+    if cap is None:
+        return None, None
+    for rel, digest in cap["sources"].items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None, None
+        except OSError:
+            return None, None
+    return cap["bytes"], cap["kernel"]
 
 
 def _measured_peaks():
@@ -429,6 +462,7 @@ def main():
     props = torch.cuda.get_device_properties(dev)
     mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
     fp32_peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12  # TFLOP/s
+    traffic, traffic_kernel = captured_traffic(dom)
     if dom in SCAN_FLOPS:
         # The scan kernels are bound by FP32 arithmetic, not HBM: per element the backward needs
         # ~22 flops for ~0.9 bytes, far above the GB300 ridge (~12 flops/byte).
@@ -438,14 +472,15 @@ def main():
         roofline = {"kernel": f"ssm_{dom}", "bound": "alu", "achieved": ach_tf,
                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach_tf / fp32_peak,
                     "peak_source": f"derived: SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz",
-                    "traffic": None, "algorithmic_flops_per_launch": flops,
+                    "traffic": traffic, "traffic_kernel": traffic_kernel,
+                    "algorithmic_flops_per_launch": flops,
                     "hbm": {"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src,
                             "algorithmic_bytes_per_launch": dom_bytes}}
     else:
         roofline = {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "peak_source": peak_src, "traffic": None,
+                    "peak_source": peak_src, "traffic": traffic, "traffic_kernel": traffic_kernel,
                     "algorithmic_bytes_per_launch": dom_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
