@@ -165,7 +165,10 @@ constexpr int kSegWarps = 8;
 constexpr int kSegThreads = 32 * kSegWarps;
 constexpr int kSegTT = kSeg * kSegWarps;       // tokens per tile
 constexpr int kSegRows = 32;                   // channels per tile
-constexpr int kRowsPerWarp = kSegRows / kSegWarps;
+// Lanes per row when moving sx rows into shared memory (see rows_to_smem); measured best on
+// GB300 for each kernel.
+constexpr int kFwdLanesPerRow = 8;
+constexpr int kBwdLanesPerRow = 1;
 
 template <typename IO>
 __device__ __forceinline__ void unpack16(const uint4 u, float* v) {
@@ -197,38 +200,47 @@ __device__ __forceinline__ uint4 pack16(const float* v) {
   }
 }
 
-// Copies columns [c0, c0 + NC) of rows d0 + wid + 8q (q < 4) of a time-fastest [..][W] array into
-// s[q'][0..NC) (row stride SP floats) as fp32; zero outside [0, W) and for rows >= D.  16-byte
-// groups aligned in global memory; a group partly outside the row is read element by element.
-template <typename IO, int NC, int SP>
+// Copies columns [c0, c0 + NC) of rows d0 .. d0+31 of a time-fastest [..][W] array into
+// s[r][0..NC) (row stride SP floats, odd) as fp32; zero outside [0, W) and for rows >= D.
+// 16-byte groups aligned in global memory; a group partly outside the row is read element by
+// element.  LPR lanes share a row: LPR = 1 gives one row per lane (32 rows per shared store
+// instruction, conflict-free with the odd stride); LPR = 8 gives 4 rows x 8 consecutive groups
+// (128-byte global runs, 2-way conflicts).
+template <typename IO, int NC, int SP, int LPR>
 __device__ __forceinline__ void rows_to_smem(const IO* base, int d0, int D, long c0, long W,
                                              float* s, int wid, int lane) {
   constexpr int V = 16 / sizeof(IO);
   constexpr int NG = (NC + V - 1) / V + 1;  // groups covering NC columns at any alignment
-  for (int idx = lane; idx < kRowsPerWarp * NG; idx += 32) {
-    const int q = idx / NG, gi = idx - q * NG;
-    const int r = wid + q * kSegWarps, d = d0 + r;
-    if (d >= D) continue;
+  constexpr int RPW = 32 / LPR;             // rows per warp instruction
+  constexpr int ROW_PASSES = kSegRows / (RPW * kSegWarps) > 0 ? kSegRows / (RPW * kSegWarps) : 1;
+  constexpr int G0 = LPR == 1 ? kSegWarps : LPR;  // group stride of one lane
+#pragma unroll
+  for (int rp = 0; rp < ROW_PASSES; rp++) {
+    const int r = LPR == 1 ? lane : (rp * kSegWarps + wid) * RPW + lane / LPR;
+    const int d = d0 + r;
+    if (r >= kSegRows || d >= D) continue;
     const IO* row = base + (long)d * W;
     const int ph = (int)(((uintptr_t)(row + c0) & 15) / sizeof(IO));
-    const long cs = c0 - ph + (long)gi * V;  // column of the group's first element
-    const int j0 = (int)(cs - c0);           // its index in s
-    if (j0 >= NC) continue;
-    float v[V];
-    if (cs >= 0 && cs + V <= W) {
-      unpack16<IO>(__ldg(reinterpret_cast<const uint4*>(row + cs)), v);
-    } else {
+    float* srow = s + r * SP;
+    for (int gi = (LPR == 1 ? wid : lane % LPR); gi < NG; gi += G0) {
+      const long cs = c0 - ph + (long)gi * V;  // column of the group's first element
+      const int j0 = (int)(cs - c0);           // its index in s
+      if (j0 >= NC) break;
+      float v[V];
+      if (cs >= 0 && cs + V <= W) {
+        unpack16<IO>(__ldg(reinterpret_cast<const uint4*>(row + cs)), v);
+      } else {
 #pragma unroll
-      for (int e = 0; e < V; e++) v[e] = (cs + e >= 0 && cs + e < W) ? ld(row + cs + e) : 0.0f;
-    }
-    float* dst = s + r * SP + j0;
-    if (j0 >= 0 && j0 + V <= NC) {
+        for (int e = 0; e < V; e++) v[e] = (cs + e >= 0 && cs + e < W) ? ld(row + cs + e) : 0.0f;
+      }
+      if (j0 >= 0 && j0 + V <= NC) {
 #pragma unroll
-      for (int e = 0; e < V; e++) dst[e] = v[e];
-    } else {
+        for (int e = 0; e < V; e++) srow[j0 + e] = v[e];
+      } else {
 #pragma unroll
-      for (int e = 0; e < V; e++)
-        if (j0 + e >= 0 && j0 + e < NC) dst[e] = v[e];
+        for (int e = 0; e < V; e++)
+          if (j0 + e >= 0 && j0 + e < NC) srow[j0 + e] = v[e];
+      }
     }
   }
 }
@@ -242,7 +254,7 @@ conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
   const long W = (long)L + K - 1;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, i0, W, s, wid, lane);
+  rows_to_smem<IO, NC, SP, kFwdLanesPerRow>(sx + (long)b * D * W, d0, D, i0, W, s, wid, lane);
   __syncthreads();
   const int d = d0 + lane, s0 = i0 + wid * kSeg;
   if (d >= D || s0 >= L) return;
@@ -281,7 +293,7 @@ conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
 }
 
 template <typename IO, int K>
-__global__ void __launch_bounds__(kSegThreads, 3)
+__global__ void __launch_bounds__(kSegThreads, 4)
 conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
                     const float* __restrict__ bias, const IO* __restrict__ dout,
                     IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int silu) {
@@ -305,7 +317,7 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
     const int t = t_first + u;
     dv[u] = (active && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
   }
-  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
+  rows_to_smem<IO, NC, SP, kBwdLanesPerRow>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
   __syncthreads();
   float ox[kSeg];
   float pk[K + 1];
@@ -365,19 +377,18 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
     if (dd < D) part[(((long)b * nt + blockIdx.y) * D + dd) * (K + 1) + k] = v;
   }
   __syncthreads();
-  // d_sx rows: columns [i0, min(i0 + TT, W)), 16-byte aligned groups + scalar edges
+  // d_sx rows: columns [i0, min(i0 + TT, W)), 16-byte aligned groups + scalar edges; lane =
+  // row, warp = group, as in rows_to_smem
   constexpr int V = 16 / sizeof(IO);
   constexpr int NG = (kSegTT + V - 1) / V + 1;
   const int n = (int)min((long)kSegTT, W - i0);
-  for (int idx = lane; idx < kRowsPerWarp * NG; idx += 32) {
-    const int q = idx / NG, gi = idx - q * NG;
-    const int r = wid + q * kSegWarps, dd = d0 + r;
-    if (dd >= D) continue;
-    IO* row = d_sx + ((long)b * D + dd) * W + i0;
-    const int ph = (int)(((uintptr_t)row & 15) / sizeof(IO));
+  const int dd = d0 + lane;
+  IO* row = d_sx + ((long)b * D + dd) * W + i0;
+  const int ph = (int)(((uintptr_t)row & 15) / sizeof(IO));
+  for (int gi = wid; gi < NG && dd < D; gi += kSegWarps) {
     const int j0 = gi * V - ph;
-    if (j0 >= n) continue;
-    const float* src = s + r * SO + j0;
+    if (j0 >= n) break;
+    const float* src = s + lane * SO + j0;
     if (j0 >= 0 && j0 + V <= n) {
       float v[V];
 #pragma unroll
