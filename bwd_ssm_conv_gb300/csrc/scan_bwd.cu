@@ -425,7 +425,8 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.nch_b = (p.L + q.chunk_b - 1) / q.chunk_b;
   const long base_threads = (long)p.ns * p.G * q.bpg * kScanThreads;
   const long target = (long)num_sms * kBwdTargetThreadsPerSM;
-  long S = (target + base_threads - 1) / base_threads;
+  long S = base_threads >= (long)num_sms * kBwdNoSplitThreadsPerSM
+               ? 1 : (target + base_threads - 1) / base_threads;
   if (S > q.nch_b) S = q.nch_b;
   if (S < 1) S = 1;
   q.seg_chunks = (int)((q.nch_b + S - 1) / S);

@@ -8,7 +8,11 @@ namespace ssm {
 
 constexpr int kScanThreads = 128;              // threads per scan block
 constexpr long kFwdTargetThreadsPerSM = 768;   // below this, time segments add parallelism
-constexpr long kBwdTargetThreadsPerSM = 512;
+// Backward time segments: none when the (sequence, channel block) grid alone has
+// kBwdNoSplitThreadsPerSM threads per SM; otherwise enough segments for kBwdTargetThreadsPerSM
+// (each extra segment costs a local adjoint pass; measured on GB300 with one long sequence).
+constexpr long kBwdNoSplitThreadsPerSM = 512;
+constexpr long kBwdTargetThreadsPerSM = 4096;
 constexpr int kMinSegment = 64;                // shortest time segment worth a block
 
 __host__ inline int pow2_ceil(int v) {

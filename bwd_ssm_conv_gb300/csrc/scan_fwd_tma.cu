@@ -18,6 +18,11 @@ namespace ssm {
 
 constexpr int kFwdStages = 3;
 constexpr int kFwdTile = 16;  // tokens per staged tile
+// Time segments: none when the (sequence, channel block) grid alone has kFwdNoSplitBlocksPerSM
+// blocks per SM; otherwise enough for kFwdTargetBlocksPerSM (each extra segment costs a
+// local-aggregate pass over its tokens; measured on GB300 with one long sequence).
+constexpr long kFwdNoSplitBlocksPerSM = 4;
+constexpr long kFwdTargetBlocksPerSM = 8;
 
 struct FwdTmaArgs {
   CUtensorMap mx, mdt, mz, my, mb, mc;
@@ -340,7 +345,8 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   (void)per_tok;
   q.tt = kFwdTile;
   const long base = (long)p.ns * (p.HP / q.cb);
-  long S = (2L * num_sms + base - 1) / base;
+  long S = base >= kFwdNoSplitBlocksPerSM * num_sms
+               ? 1 : (kFwdTargetBlocksPerSM * num_sms + base - 1) / base;
   const long max_s = (p.L + kMinSegment - 1) / kMinSegment;
   if (S > max_s) S = max_s;
   if (S < 1) S = 1;
