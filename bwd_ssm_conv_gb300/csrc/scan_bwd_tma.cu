@@ -56,30 +56,6 @@ __device__ __forceinline__ void sts_f(IO* p, float v) {
   else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
 }
 
-// Packed decay for a pair of states: the coefficient and the two uses of it (see
-// scan_common.cuh for the fast and the accurate forms).
-template <bool ACC>
-__device__ __forceinline__ f2_t decay2(f2_t dl2, f2_t A2p) {
-  if constexpr (!ACC) return f2_ex2(f2_mul(dl2, A2p));
-  float dl, d2, a0, a1;
-  f2_unpack(dl2, dl, d2);
-  f2_unpack(A2p, a0, a1);
-  return f2_pack(decay_coef<true>(dl, a0), decay_coef<true>(dl, a1));
-}
-template <bool ACC>
-__device__ __forceinline__ f2_t step2(f2_t coef, f2_t h, f2_t u) {
-  return ACC ? f2_add(h, f2_fma(coef, h, u)) : f2_fma(coef, h, u);
-}
-template <bool ACC>
-__device__ __forceinline__ f2_t apply2(f2_t coef, f2_t v) {
-  return ACC ? f2_fma(coef, v, v) : f2_mul(coef, v);
-}
-__device__ __forceinline__ float f2_sum(f2_t v) {
-  float lo, hi;
-  f2_unpack(v, lo, hi);
-  return lo + hi;
-}
-
 // B (and C) of a tile as fp32: the staged tile itself for fp32 I/O, else converted once.
 template <typename IO>
 __device__ __forceinline__ const float* tile_rows_f32(const unsigned char* stage_rows, float* conv,

@@ -58,6 +58,29 @@ __device__ __forceinline__ float decay_apply(float coef, float v) {
   return ACC ? fmaf(coef, v, v) : coef * v;
 }
 
+// Packed versions for a pair of states (f32x2): the coefficient and its two uses.
+template <bool ACC>
+__device__ __forceinline__ f2_t decay2(f2_t dl2, f2_t A2p) {
+  if constexpr (!ACC) return f2_ex2(f2_mul(dl2, A2p));
+  float dl, d2, a0, a1;
+  f2_unpack(dl2, dl, d2);
+  f2_unpack(A2p, a0, a1);
+  return f2_pack(decay_coef<true>(dl, a0), decay_coef<true>(dl, a1));
+}
+template <bool ACC>
+__device__ __forceinline__ f2_t step2(f2_t coef, f2_t h, f2_t u) {
+  return ACC ? f2_add(h, f2_fma(coef, h, u)) : f2_fma(coef, h, u);
+}
+template <bool ACC>
+__device__ __forceinline__ f2_t apply2(f2_t coef, f2_t v) {
+  return ACC ? f2_fma(coef, v, v) : f2_mul(coef, v);
+}
+__device__ __forceinline__ float f2_sum(f2_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return lo + hi;
+}
+
 // Lanes of the tpc-lane group this lane belongs to (xor-shuffles stay inside it).
 __device__ __forceinline__ unsigned group_mask(int tpc) {
   if (tpc >= 32) return 0xffffffffu;

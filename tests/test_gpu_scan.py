@@ -36,6 +36,14 @@ CASES = [
     ("tma_bf16_softplus", (3, 520, 96, 1, 16, 1), "bf16", False, 128, True, False),
     ("tma_chunk24_tile8", (1, 200, 32, 1, 16, 1), "f32", False, 24, False, False),
     ("tma_groups", (2, 100, 64, 1, 16, 2), "bf16", False, 32, False, False),
+    # Mamba-2 form (one A per head) with several heads per channel block, two groups
+    ("mamba2_f32_heads", (2, 200, 16, 8, 32, 2), "f32", True, 32, False, False),
+    # ... bf16 with softplus(dt + dt_bias)
+    ("mamba2_bf16_softplus", (2, 160, 8, 16, 64, 1), "bf16", True, 32, True, False),
+    # TMA forward with fp32 I/O and one A per channel (head_dim 1), softplus, several segments
+    ("tma_f32_scalar_a_softplus", (2, 400, 64, 1, 16, 1), "f32", True, 32, True, False),
+    # TMA forward, bf16, one A per channel, d_state 64 (16 states x 4 threads per channel)
+    ("tma_bf16_scalar_a_n64", (3, 130, 32, 1, 64, 1), "bf16", True, 16, False, False),
 ]
 
 
