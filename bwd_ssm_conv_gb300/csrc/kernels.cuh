@@ -35,11 +35,15 @@ struct ScanProblem {
 };
 
 // Forward.  y may be NULL (states / checkpoints only), state_out may be NULL, ckpt may be NULL.
-// launch_scan_fwd takes the TMA-staged path (scan_fwd_tma.cu) when it applies.
+// launch_scan_fwd takes a TMA-staged path when one applies: scan_fwd_tma.cu (head_dim 1) or
+// scan_fwd_heads.cu (one A per head, head_dim a multiple of 64, d_state 128).
 size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms);
 size_t scan_fwd_tma_ws_bytes(const ScanProblem& p, int num_sms);  // 0: path does not apply
 cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out, float* ckpt,
                                 void* ws, int num_sms, cudaStream_t st);
+size_t scan_fwd_heads_ws_bytes(const ScanProblem& p, int num_sms);  // 0: path does not apply
+cudaError_t launch_scan_fwd_heads(const ScanProblem& p, void* y, float* state_out, float* ckpt,
+                                  void* ws, int num_sms, cudaStream_t st);
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st);
 

@@ -183,8 +183,10 @@ static FwdPlan plan_fwd(const ScanProblem& p, int num_sms) {
 }
 
 size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms) {
-  const size_t a = plan_fwd(p, num_sms).bytes, b = scan_fwd_tma_ws_bytes(p, num_sms);
-  return a > b ? a : b;
+  size_t a = plan_fwd(p, num_sms).bytes;
+  const size_t b = scan_fwd_tma_ws_bytes(p, num_sms), c = scan_fwd_heads_ws_bytes(p, num_sms);
+  if (b > a) a = b;
+  return c > a ? c : a;
 }
 
 template <typename IO, int NS, bool SCALAR_A, bool FULL>
@@ -224,7 +226,9 @@ static void launch_fwd_io(const FwdArgs& a, int ns_state, int blocks_x, bool ful
 
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st) {
-  const cudaError_t e = launch_scan_fwd_tma(p, y, state_out, ckpt, ws, num_sms, st);
+  cudaError_t e = launch_scan_fwd_tma(p, y, state_out, ckpt, ws, num_sms, st);
+  if (e != cudaErrorNotSupported) return e;
+  e = launch_scan_fwd_heads(p, y, state_out, ckpt, ws, num_sms, st);
   if (e != cudaErrorNotSupported) return e;
   const FwdPlan q = plan_fwd(p, num_sms);
   FwdArgs a{};

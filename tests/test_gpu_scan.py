@@ -40,6 +40,10 @@ CASES = [
     ("mamba2_f32_heads", (2, 200, 16, 8, 32, 2), "f32", True, 32, False, False),
     # ... bf16 with softplus(dt + dt_bias)
     ("mamba2_bf16_softplus", (2, 160, 8, 16, 64, 1), "bf16", True, 32, True, False),
+    # Mamba-2 form on the head-tiled forward: head_dim 64, d_state 128, two groups, 4 segments
+    ("mh_f32_groups_segments", (2, 200, 4, 64, 128, 2), "f32", True, 32, False, False),
+    # ... bf16 with softplus, head_dim 128 (two blocks per head)
+    ("mh_bf16_softplus_p128", (1, 100, 8, 128, 128, 1), "bf16", True, 16, True, False),
     # TMA forward with fp32 I/O and one A per channel (head_dim 1), softplus, several segments
     ("tma_f32_scalar_a_softplus", (2, 400, 64, 1, 16, 1), "f32", True, 32, True, False),
     # TMA forward, bf16, one A per channel, d_state 64 (16 states x 4 threads per channel)
