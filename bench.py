@@ -60,7 +60,10 @@ def alg_bytes(w) -> dict:
 #   backward: two forward recomputes (4 each, without C h) + the adjoint: dh = gy C + carry (2),
 #             dC += gy h (1), sum dh B (2), dB = dh delta x (1), carry = a dh (1),
 #             w = carry h_prev (1), sum A w (2), dA += delta w (2), y_pre += C h (2)      = 22
+# With one A per head (the Mamba-2 form) delta*A is one product per (token, head), not per
+# element: 5 and 20.
 SCAN_FLOPS = {"scan_fwd": 6, "scan_bwd": 22}
+SCAN_FLOPS_SCALAR_A = {"scan_fwd": 5, "scan_bwd": 20}
 FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (packed f32x2
                           # issues half the instructions at the same lane rate)
 
@@ -467,7 +470,7 @@ def main():
         # The scan kernels are bound by FP32 arithmetic, not HBM: per element the backward needs
         # ~22 flops for ~0.9 bytes, far above the GB300 ridge (~12 flops/byte).
         elems = tokens * w.channels * w.d_state
-        flops = SCAN_FLOPS[dom] * elems
+        flops = (SCAN_FLOPS_SCALAR_A if w.scalar_a else SCAN_FLOPS)[dom] * elems
         ach_tf = flops / (stage_ms[dom] * 1e-3) / 1e12
         roofline = {"kernel": f"ssm_{dom}", "bound": "alu", "achieved": ach_tf,
                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach_tf / fp32_peak,

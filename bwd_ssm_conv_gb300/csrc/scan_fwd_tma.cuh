@@ -1,13 +1,14 @@
 // scan_fwd_tma.cuh -- forward scan with TMA-staged tiles: the fast path for head_dim 1 (the
 // Mamba-1 layout), channel rows 16-byte aligned, d_state a multiple of 4 and a checkpoint
 // interval that is a multiple of the 16-token tile; A per state or one A per channel; bf16 or
-// fp32 I/O.  Other shapes (head_dim > 1: the Mamba-2 form) use scan_fwd.cu.
+// fp32 I/O.  The Mamba-2 form (head_dim > 1) uses scan_fwd_heads.cu where it applies, other
+// shapes scan_fwd.cu.
 //
 // Same arithmetic and segment decomposition as scan_fwd.cu (local aggregate, carry, main),
 // but every block streams its inputs as [tile tokens][block channels] tiles of x, dt, z and
-// [tile tokens][N] tiles of B, C into a ring of
-// shared-memory stages: one elected thread issues 3-D cp.async.bulk.tensor loads that complete
-// on an mbarrier per stage, so the loads of the next tiles overlap the arithmetic of this one.
+// [tile tokens][N] tiles of B, C into a ring of shared-memory stages: one elected thread
+// issues 3-D cp.async.bulk.tensor loads that complete on an mbarrier per stage, so the loads
+// of the next tiles overlap the arithmetic of this one.
 // y leaves the same way, one tile per TMA store.  Segments are whole tiles long, so no tile
 // straddles two segments; the sequence end is clipped by the tensor bounds (loads fill zeros,
 // stores skip).
