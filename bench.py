@@ -286,16 +286,14 @@ def time_device(step, steps, warmup, flush):
     return total, per_stage, launches
 
 
-def time_e2e(step, steps, warmup):
-    """Same step through the public API with host buffers: every step copies its inputs from
-    pinned host memory and reads its results back."""
+def time_e2e_serial(step, steps, warmup):
+    """Same step through the public API with host buffers, one stream: every step copies its
+    inputs from pinned host memory, runs, and reads its results back before the next starts."""
     host_in = [t.detach().cpu().pin_memory() for t in step.inputs()]
     dev_in = step.inputs()
     outs = step.outputs()
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     stages = step.stages()
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
 
     def one():
         for h, d in zip(host_in, dev_in):
@@ -314,6 +312,59 @@ def time_e2e(step, steps, warmup):
     for _ in range(steps):
         one()
     e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def time_e2e(pair, steps, warmup):
+    """Same step through the public API with host buffers: every step copies all its inputs
+    from pinned host memory and reads all its results back.  Two device buffer sets (`pair`)
+    and three streams let step i's kernels overlap the input copies of step i+1 and the result
+    copies of step i-1; events keep each buffer set's copies and kernels in order.  Returns
+    (ms per step from the first input copy to the last result copy, bytes in, bytes out)."""
+    host_in = [t.detach().cpu().pin_memory() for t in pair[0].inputs()]
+    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outputs()]
+                for st in pair]
+    dev_in = [st.inputs() for st in pair]
+    dev_out = [st.outputs() for st in pair]
+    stages = [st.stages() for st in pair]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    run_done, out_done = [None, None], [None, None]
+
+    def one(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if run_done[k] is not None:  # step i-2's kernels are done with this input set
+                s_in.wait_event(run_done[k])
+            for h, d in zip(host_in, dev_in[k]):
+                d.copy_(h, non_blocking=True)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(in_done)
+            if out_done[k] is not None:  # step i-2's results have left this output set
+                s_run.wait_event(out_done[k])
+            for _, fn in stages[k]:
+                fn()
+            run_done[k] = torch.cuda.Event()
+            run_done[k].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(run_done[k])
+            for d, h in zip(dev_out[k], host_out[k]):
+                h.copy_(d, non_blocking=True)
+            out_done[k] = torch.cuda.Event()
+            out_done[k].record(s_out)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(warmup, warmup + steps):
+        one(i)
+    e1.record(s_out)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
@@ -446,7 +497,9 @@ def main():
     if dist is not None:
         dist.barrier()
 
-    e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 20)), 2)
+    e2e_steps = max(3, min(args.steps, 20))
+    serial_ms = reduce_max(time_e2e_serial(step, e2e_steps, 2), dist, dev)
+    e2e_ms, h2d, d2h = time_e2e((step, Step(w, dev, inp)), e2e_steps, 2)
     e2e_ms = reduce_max(e2e_ms, dist, dev)
 
     if rank != 0:
@@ -498,7 +551,9 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clocks,
         "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "pipelined": "2 buffer sets, copies of steps i+1 / i-1 overlap step i",
+                "serial_ms_per_step": serial_ms},
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
