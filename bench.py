@@ -74,12 +74,14 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16>",
-        "bytes": 472636928 + 671771136,
+        "bytes": 472173056 + 672165632,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "ba17adf4abf05e68d12daf15bcb9993c2a33ac1a8dbf9f827b519fa7babd14ef",
+                "9697604387c734027bc4e8f5b3b91571b6f347ca15c43c0d79246f7cfef7c467",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "02495c2a1664a92abfc2ed6cd2cd1cfb1ad3cbced02778247fb73bbd0072dbbe",
+            "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
+                "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
         },
     },
 }
