@@ -245,10 +245,10 @@ __device__ __forceinline__ void rows_to_smem(const IO* base, int d0, int D, long
   }
 }
 
-template <typename IO, int K>
+template <typename IO, int K, bool SILU>
 __global__ void __launch_bounds__(kSegThreads)
 conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
-                    const float* __restrict__ bias, IO* __restrict__ out, int D, int L, int silu) {
+                    const float* __restrict__ bias, IO* __restrict__ out, int D, int L) {
   constexpr int NC = kSegTT + K - 1, SP = NC | 1;  // odd stride: lanes read distinct banks
   __shared__ float s[kSegRows * SP];
   const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
@@ -277,7 +277,7 @@ conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
       float acc = bv;
 #pragma unroll
       for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
-      st(o + (long)u * D, silu ? siluf_(acc) : acc);
+      st(o + (long)u * D, SILU ? siluf_(acc) : acc);
     }
   } else {
     for (int u = 0; u < n; u++) {
@@ -287,16 +287,16 @@ conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
       float acc = bv;
 #pragma unroll
       for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
-      st(o + (long)u * D, silu ? siluf_(acc) : acc);
+      st(o + (long)u * D, SILU ? siluf_(acc) : acc);
     }
   }
 }
 
-template <typename IO, int K>
+template <typename IO, int K, bool SILU>
 __global__ void __launch_bounds__(kSegThreads, 4)
 conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
                     const float* __restrict__ bias, const IO* __restrict__ dout,
-                    IO* __restrict__ d_sx, float* __restrict__ part, int D, int L, int silu) {
+                    IO* __restrict__ d_sx, float* __restrict__ part, int D, int L) {
   // sx columns i0-K+1 .. i0+TT+K-2 (inputs of tokens i0-K+1 .. i0+TT-1); later reused for the
   // d_sx tile (columns i0 .. i0+TT-1).
   constexpr int NC = kSegTT + 2 * K - 2, SP = NC | 1;
@@ -312,10 +312,16 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   // loads are in flight together
   float dv[NU];
   const int t_first = s0 - (K - 1);
+  if (active && t_first >= 0 && t_first + NU <= L) {  // interior segment: no per-token checks
+    const IO* dp = dout + ((long)b * L + t_first) * D + d;
 #pragma unroll
-  for (int u = 0; u < NU; u++) {
-    const int t = t_first + u;
-    dv[u] = (active && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+    for (int u = 0; u < NU; u++) dv[u] = ld(dp + (long)u * D);
+  } else {
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+      const int t = t_first + u;
+      dv[u] = (active && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
+    }
   }
   rows_to_smem<IO, NC, SP, kBwdLanesPerRow>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
   __syncthreads();
@@ -340,7 +346,7 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
       for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
       xw[K - 1] = xr[u + K - 1];
       float g = dv[u];
-      if (silu) {  // pre recomputed with the forward's tap order
+      if constexpr (SILU) {  // pre recomputed with the forward's tap order
         float pre = bv;
 #pragma unroll
         for (int k = 0; k < K; k++) pre = fmaf(xw[k], w[k], pre);
@@ -442,10 +448,14 @@ static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias,
   IO* o = (IO*)out;
   const dim3 gseg((D + kSegRows - 1) / kSegRows, (L + kSegTT - 1) / kSegTT, n_s);
   switch (K) {
-    case 1: conv_fwd_seg_kernel<IO, 1><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 2: conv_fwd_seg_kernel<IO, 2><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 3: conv_fwd_seg_kernel<IO, 3><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
-    case 4: conv_fwd_seg_kernel<IO, 4><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L, silu); break;
+    case 1: silu ? conv_fwd_seg_kernel<IO, 1, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
+                 : conv_fwd_seg_kernel<IO, 1, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
+    case 2: silu ? conv_fwd_seg_kernel<IO, 2, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
+                 : conv_fwd_seg_kernel<IO, 2, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
+    case 3: silu ? conv_fwd_seg_kernel<IO, 3, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
+                 : conv_fwd_seg_kernel<IO, 3, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
+    case 4: silu ? conv_fwd_seg_kernel<IO, 4, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
+                 : conv_fwd_seg_kernel<IO, 4, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
     default: {
       size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
       conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, o, D, L, K, silu);
@@ -476,10 +486,14 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
   const IO* g = (const IO*)dout;
   IO* dx = (IO*)d_sx;
   switch (K) {
-    case 1: conv_bwd_seg_kernel<IO, 1><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 2: conv_bwd_seg_kernel<IO, 2><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 3: conv_bwd_seg_kernel<IO, 3><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
-    case 4: conv_bwd_seg_kernel<IO, 4><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L, silu); break;
+    case 1: silu ? conv_bwd_seg_kernel<IO, 1, true><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L)
+                 : conv_bwd_seg_kernel<IO, 1, false><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L); break;
+    case 2: silu ? conv_bwd_seg_kernel<IO, 2, true><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L)
+                 : conv_bwd_seg_kernel<IO, 2, false><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L); break;
+    case 3: silu ? conv_bwd_seg_kernel<IO, 3, true><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L)
+                 : conv_bwd_seg_kernel<IO, 3, false><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L); break;
+    case 4: silu ? conv_bwd_seg_kernel<IO, 4, true><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L)
+                 : conv_bwd_seg_kernel<IO, 4, false><<<grid, kSegThreads, 0, st>>>(x, c, bias, g, dx, part, D, L); break;
     default:
       conv_bwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, g, dx, part, D, L, K, silu);
   }
