@@ -22,8 +22,8 @@ SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NONFINITE = -4, -5, -6
 SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE = 1, 2, 4
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
-            "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_status", "ssm_status_string",
-            "ssm_abi_version", "ssm_kernel_launches")
+            "ssm_scan_fwd", "ssm_scan_bwd", "ssm_decode_step", "ssm_scan_status",
+            "ssm_status_string", "ssm_abi_version", "ssm_kernel_launches")
 
 
 class SsmError(RuntimeError):
@@ -61,6 +61,8 @@ def lib():
         L.ssm_scan_workspace_size.restype = _sz
         L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanDesc)] + [_vp] * 13 + [_sz, _vp]
         L.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanDesc)] + [_vp] * 23 + [_sz, _vp]
+        L.ssm_decode_step.argtypes = ([ctypes.POINTER(ScanDesc), _i, _u] + [_vp] * 15 +
+                                      [_sz, _vp])
         L.ssm_scan_status.argtypes = [_vp, ctypes.POINTER(_i), _vp]
         L.ssm_status_string.argtypes = [_i]
         L.ssm_status_string.restype = ctypes.c_char_p
@@ -223,6 +225,36 @@ def ssm_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, s0=None, ids=None
                             _ptr(ws), ws.numel(), _stream(stream))
     _check("ssm_scan_fwd", rc)
     return y, st, ck
+
+
+def ssm_decode_step(x_new, conv_state, c, dt, A, B, C, state, bias=None, D=None, z=None,
+                    dt_bias=None, ids=None, silu=True, softplus=False, check_finite=False,
+                    ws=None, out=None, stream=None):
+    """One token per sequence: rolls ``conv_state`` [rows][H*P][K-1] and updates ``state``
+    [rows][H][P][N] in place, returns y [n_s][H][P].  x_new [n_s][H][P] (the pre-conv input),
+    dt [n_s][H], B / C [n_s][G][N], z [n_s][H][P]; the rest as in ssm_scan_fwd."""
+    n_s, H, P = x_new.shape
+    rows, _, _, N = state.shape
+    G = B.shape[1]
+    K = c.shape[1]
+    io = x_new.dtype
+    dev = x_new.device
+    flags = (SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0)
+    sh = ScanShape(n_s, 1, H, P, N, G, 1 if A.dim() == 2 else 0, rows, 1, _io_of(x_new), flags)
+    y = torch.empty_like(x_new) if out is None else out
+    ws = _workspace(256, dev, ws)
+    d = sh.desc()
+    rc = lib().ssm_decode_step(ctypes.byref(d), K, SSM_CONV_SILU if silu else 0,
+                               _ptr(ids, torch.int32, "ids"), _ptr(x_new, io, "x_new"),
+                               _ptr(conv_state, io, "conv_state"), _ptr(c, torch.float32, "c"),
+                               _ptr(bias, torch.float32, "bias"), _ptr(dt, io, "dt"),
+                               _ptr(A, torch.float32, "A"), _ptr(B, io, "B"), _ptr(C, io, "C"),
+                               _ptr(D, torch.float32, "D"), _ptr(z, io, "z"),
+                               _ptr(dt_bias, torch.float32, "dt_bias"),
+                               _ptr(state, torch.float32, "state"), _ptr(y, io, "y"), _ptr(ws),
+                               ws.numel(), _stream(stream))
+    _check("ssm_decode_step", rc)
+    return y
 
 
 GRAD_NAMES = ("d_s0", "d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_dt_bias")

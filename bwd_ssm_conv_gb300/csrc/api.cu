@@ -101,7 +101,7 @@ const char* ssm_status_string(int s) {
     case SSM_ERR_UNSUPPORTED: return "size beyond a documented limit of this library";
     case SSM_ERR_WORKSPACE: return "workspace missing or smaller than the *_workspace_size result";
     case SSM_ERR_CUDA: return "a CUDA launch failed";
-    case SSM_ERR_TIMEOUT: return "timeout (reserved; no kernel of this version waits)";
+    case SSM_ERR_TIMEOUT: return "a bounded wait for a staged tile gave up; that block skipped the rest of its work";
     case SSM_ERR_NONFINITE: return "a non-finite output was produced";
     default: return "unknown status";
   }
@@ -210,6 +210,40 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
   cudaError_t e = ssm::launch_scan_bwd(p, ckpt, g, ws, sms, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_decode_step(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags,
+                    const int32_t* ids, const void* x_new, void* conv_state, const float* c,
+                    const float* bias, const void* dt, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* dt_bias,
+                    float* state, void* y, void* ws, size_t ws_bytes, void* stream) {
+  ScanProblem p;
+  int rc = scan_problem(desc, 0, &p);
+  if (rc != SSM_OK) return rc;
+  if (p.L != 1) return SSM_ERR_INVALID_ARG;
+  if (d_conv <= 0) return SSM_ERR_INVALID_ARG;
+  if (d_conv > SSM_MAX_D_CONV) return SSM_ERR_UNSUPPORTED;
+  if (conv_flags & ~(unsigned)SSM_CONV_SILU) return SSM_ERR_INVALID_ARG;
+  if (!x_new || !c || !dt || !A || !B || !C || !state || !y || (d_conv > 1 && !conv_state))
+    return SSM_ERR_INVALID_ARG;
+  const int io = p.io;
+  if (!check_act(x_new, io) || !check_act(dt, io) || !check_act(B, io) || !check_act(C, io) ||
+      !check_act(y, io) || (z && !check_act(z, io)) || (conv_state && !check_act(conv_state, io)) ||
+      !aligned(c, 4) || (bias && !aligned(bias, 4)) || !aligned(A, 4) || !aligned(state, 4) ||
+      (ids && !aligned(ids, 4)) || (D && !aligned(D, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+    return SSM_ERR_INVALID_ARG;
+  if (!ids && p.state_rows < p.ns) return SSM_ERR_INVALID_ARG;
+  if ((long long)p.state_rows * p.HP * p.N > kMaxTotal ||
+      (long long)p.state_rows * p.HP * d_conv > kMaxTotal)
+    return SSM_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < ssm::kStatusBytes || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
+  p.ids = ids; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.dt_bias = dt_bias;
+  p.status = (int*)ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  cudaError_t e = ssm::launch_decode_step(p, d_conv, (conv_flags & SSM_CONV_SILU) ? 1 : 0, x_new,
+                                          conv_state, c, bias, state, y, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -173,6 +173,33 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
                  void* d_B, void* d_C, float* d_D, void* d_z, float* d_dt_bias, void* ws,
                  size_t ws_bytes, void* stream);
 
+/* ---- single-token decode step -----------------------------------------------------------
+ * One token per sequence in one launch: the conv ring-state roll, conv1d(+bias, SiLU) of the
+ * new input column, and one step of the scan.  This is the per-token loop of infotheory's
+ * mamba1 runtime (forward_impl on one token: depthwise_conv_step on its conv ring buffer,
+ * then selective_scan_state16 on its recurrent state) and ggml's ssm_conv + ssm_scan with
+ * n_seq_tokens = 1 (ggmlR tests).  The results equal ssm_conv_fwd on
+ * [conv_state | x_new] (x rounded to the io type as that call stores it) followed by
+ * ssm_scan_fwd on one token from `state`.
+ *   desc        the scan descriptor with n_tok == 1 (chunk is ignored); d_inner = H*P
+ *   d_conv      K (1 .. SSM_MAX_D_CONV); conv_flags: SSM_CONV_SILU
+ *   ids         [n_s] int32 or NULL: sequence b uses row ids[b] of conv_state and state (rows
+ *               = state_rows, or n_s when 0); the rows of one call must be distinct.  An id
+ *               outside [0, rows) is recorded in the status word and that sequence is skipped.
+ *   x_new       [n_s][H*P] io: the new pre-conv input column
+ *   conv_state  [rows][H*P][K-1] io, in/out (oldest first); may be NULL when K == 1
+ *   c, bias     [H*P][K], [H*P] fp32; bias may be NULL
+ *   dt [n_s][H], A, B / C [n_s][G][N], D, z [n_s][H*P], dt_bias: as in ssm_scan_fwd
+ *   state       [rows][H][P][N] fp32, in/out
+ *   y           [n_s][H*P] io, out
+ *   ws          >= 256 bytes, 256-byte aligned: the status word (read with ssm_scan_status)
+ * Allocates, frees and synchronises nothing. */
+int ssm_decode_step(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags,
+                    const int32_t* ids, const void* x_new, void* conv_state, const float* c,
+                    const float* bias, const void* dt, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* dt_bias,
+                    float* state, void* y, void* ws, size_t ws_bytes, void* stream);
+
 /* Reads the device status word of the last scan call that used `ws` (waits for `stream`).
  * Writes SSM_OK, SSM_ERR_INVALID_ARG (bad id) or SSM_ERR_NONFINITE to *status and returns
  * SSM_OK; returns SSM_ERR_INVALID_ARG for NULL pointers or SSM_ERR_CUDA. */

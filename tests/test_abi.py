@@ -136,3 +136,30 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def _decode_args(d, K=4, flags=1, **over):
+    # desc, d_conv, conv_flags, ids, x_new, conv_state, c, bias, dt, A, B, C, D, z, dt_bias,
+    # state, y, ws, ws_bytes, stream
+    a = dict(ids=None, x_new=FAKE, conv_state=FAKE, c=FAKE, bias=None, dt=FAKE, A=FAKE, B=FAKE,
+             C=FAKE, D=None, z=None, dt_bias=None, state=FAKE, y=FAKE, ws=None, ws_bytes=0)
+    a.update(over)
+    return [ctypes.byref(d), K, flags, a["ids"], a["x_new"], a["conv_state"], a["c"], a["bias"],
+            a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"], a["dt_bias"], a["state"], a["y"],
+            a["ws"], a["ws_bytes"], None]
+
+
+def test_decode_step_rejects_bad_arguments(L):
+    one = _desc(n_tok=1)
+    INV, UNS, WS = binding.SSM_ERR_INVALID_ARG, binding.SSM_ERR_UNSUPPORTED, binding.SSM_ERR_WORKSPACE
+    assert L.ssm_decode_step(*_decode_args(_desc(n_tok=2))) == INV      # one token only
+    assert L.ssm_decode_step(*_decode_args(one, K=0)) == INV
+    assert L.ssm_decode_step(*_decode_args(one, K=65)) == UNS
+    assert L.ssm_decode_step(*_decode_args(one, flags=2)) == INV       # conv flags: SiLU only
+    for name in ("x_new", "c", "dt", "A", "B", "C", "state", "y", "conv_state"):
+        assert L.ssm_decode_step(*_decode_args(one, **{name: None})) == INV, name
+    assert L.ssm_decode_step(*_decode_args(one, x_new=FAKE + 2)) == INV  # misaligned fp32
+    assert L.ssm_decode_step(*_decode_args(_desc(n_tok=1, state_rows=1))) == INV  # rows < n_s
+    # valid arguments reach the workspace check: K = 1 needs no conv state
+    assert L.ssm_decode_step(*_decode_args(one, K=1, conv_state=None)) == WS
+    assert L.ssm_decode_step(*_decode_args(one, ws=FAKE, ws_bytes=128)) == WS
