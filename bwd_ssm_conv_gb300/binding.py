@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libssm_gb300.so")
 SSM_F32, SSM_BF16 = 0, 1
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_WORKSPACE = 0, -1, -2, -3
 SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NONFINITE = -4, -5, -6
-SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE = 1, 2, 4
+SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE, SSM_A_LOG = 1, 2, 4, 8
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
             "ssm_scan_fwd", "ssm_scan_bwd", "ssm_decode_step", "ssm_scan_status",
@@ -185,12 +185,13 @@ class ScanShape:
 
 
 def scan_shape(x, dt, A, B, s0=None, chunk=256, softplus=False, check_finite=False,
-               state_rows=0) -> ScanShape:
+               state_rows=0, a_log=False) -> ScanShape:
     n_s, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     a_per_state = 1 if A.dim() == 2 else 0
     rows = state_rows if state_rows else (s0.shape[0] if s0 is not None else 0)
-    flags = (SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0)
+    flags = ((SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0) |
+             (SSM_A_LOG if a_log else 0))
     return ScanShape(n_s, L, H, P, N, G, a_per_state, rows, chunk, _io_of(x), flags)
 
 
@@ -201,9 +202,10 @@ def ssm_scan_workspace_size(shape: ScanShape, backward: bool) -> int:
 
 def ssm_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, s0=None, ids=None, chunk=256,
                  softplus=False, check_finite=False, want_ckpt=True, state_rows=0, ws=None,
-                 out=None, stream=None):
-    """Returns (y, state_out, ckpt).  ``out`` = (y, state_out, ckpt) preallocated, optional."""
-    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows)
+                 out=None, stream=None, a_log=False):
+    """Returns (y, state_out, ckpt).  ``out`` = (y, state_out, ckpt) preallocated, optional.
+    ``a_log``: A holds A_log (the scan uses -exp(A_log))."""
+    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
     io = x.dtype
     dev = x.device
     if out is None:
@@ -229,7 +231,7 @@ def ssm_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, s0=None, ids=None
 
 def ssm_decode_step(x_new, conv_state, c, dt, A, B, C, state, bias=None, D=None, z=None,
                     dt_bias=None, ids=None, silu=True, softplus=False, check_finite=False,
-                    ws=None, out=None, stream=None):
+                    ws=None, out=None, stream=None, a_log=False):
     """One token per sequence: rolls ``conv_state`` [rows][H*P][K-1] and updates ``state``
     [rows][H][P][N] in place, returns y [n_s][H][P].  x_new [n_s][H][P] (the pre-conv input),
     dt [n_s][H], B / C [n_s][G][N], z [n_s][H][P]; the rest as in ssm_scan_fwd."""
@@ -239,10 +241,11 @@ def ssm_decode_step(x_new, conv_state, c, dt, A, B, C, state, bias=None, D=None,
     K = c.shape[1]
     io = x_new.dtype
     dev = x_new.device
-    flags = (SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0)
+    flags = ((SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0) |
+             (SSM_A_LOG if a_log else 0))
     sh = ScanShape(n_s, 1, H, P, N, G, 1 if A.dim() == 2 else 0, rows, 1, _io_of(x_new), flags)
     y = torch.empty_like(x_new) if out is None else out
-    ws = _workspace(256, dev, ws)
+    ws = _workspace(256 + (-(-4 * A.numel() // 256) * 256 if a_log else 0), dev, ws)
     d = sh.desc()
     rc = lib().ssm_decode_step(ctypes.byref(d), K, SSM_CONV_SILU if silu else 0,
                                _ptr(ids, torch.int32, "ids"), _ptr(x_new, io, "x_new"),
@@ -262,9 +265,10 @@ GRAD_NAMES = ("d_s0", "d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_dt_bi
 
 def ssm_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, s0=None, ids=None, ckpt=None,
                  d_state_out=None, chunk=256, softplus=False, check_finite=False, state_rows=0,
-                 want_ds0=True, ws=None, out=None, stream=None):
-    """Returns a dict keyed by GRAD_NAMES (None where not requested / not applicable)."""
-    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows)
+                 want_ds0=True, ws=None, out=None, stream=None, a_log=False):
+    """Returns a dict keyed by GRAD_NAMES (None where not requested / not applicable).
+    ``a_log``: A holds A_log and d_A is dL/dA_log."""
+    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
     io = x.dtype
     dev = x.device
     if out is None:

@@ -57,7 +57,8 @@ int scan_problem(const ssm_scan_desc* d, int backward, ScanProblem* p) {
   if (d->n_head % d->n_group != 0) return SSM_ERR_INVALID_ARG;
   if (d->a_per_state != 0 && d->a_per_state != 1) return SSM_ERR_INVALID_ARG;
   if (!io_size(d->io)) return SSM_ERR_INVALID_ARG;
-  if (d->flags & ~(unsigned)(SSM_DT_SOFTPLUS | SSM_CHECK_FINITE)) return SSM_ERR_INVALID_ARG;
+  if (d->flags & ~(unsigned)(SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG))
+    return SSM_ERR_INVALID_ARG;
   if (d->d_state > (backward ? SSM_MAX_D_STATE_BWD : SSM_MAX_D_STATE)) return SSM_ERR_UNSUPPORTED;
   const long long HP = (long long)d->n_head * d->head_dim;
   const long long per_seq = (long long)d->n_tok * HP * d->d_state;
@@ -83,6 +84,21 @@ int scan_problem(const ssm_scan_desc* d, int backward, ScanProblem* p) {
 }
 
 int check_act(const void* ptr, int io) { return aligned(ptr, io_size(io)); }
+
+// SSM_A_LOG: elements of A and the 256-aligned scratch holding A = -exp(A_log), placed after
+// the `base` bytes a call's plan needs.
+bool a_log_of(const ssm_scan_desc* d) { return d && (d->flags & SSM_A_LOG); }
+int a_count(const ScanProblem& p) { return p.a_per_state ? p.H * p.N : p.H; }
+size_t a_bytes(const ScanProblem& p) { return ssm::align_up(sizeof(float) * (size_t)a_count(p), 256); }
+
+// Converts A_log into the scratch after `base` and points p->A at it.
+int stage_a(const ssm_scan_desc* d, ScanProblem* p, void* ws, size_t base, cudaStream_t st) {
+  if (!a_log_of(d)) return SSM_OK;
+  float* a = (float*)((char*)ws + ssm::align_up(base, 256));
+  if (ssm::launch_a_from_log(p->A, a, a_count(*p), st) != cudaSuccess) return SSM_ERR_CUDA;
+  p->A = a;
+  return SSM_OK;
+}
 
 }  // namespace
 
@@ -146,7 +162,8 @@ size_t ssm_scan_workspace_size(const ssm_scan_desc* desc, int backward) {
   if (scan_problem(desc, backward, &p) != SSM_OK) return 0;
   const int sms = num_sms_current();
   if (sms <= 0) return 0;
-  return backward ? ssm::scan_bwd_ws_bytes(p, sms) : ssm::scan_fwd_ws_bytes(p, sms);
+  const size_t base = backward ? ssm::scan_bwd_ws_bytes(p, sms) : ssm::scan_fwd_ws_bytes(p, sms);
+  return a_log_of(desc) ? ssm::align_up(base, 256) + a_bytes(p) : base;
 }
 
 int ssm_scan_fwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids, const void* x,
@@ -166,13 +183,15 @@ int ssm_scan_fwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
   if (!ids && s0 && p.state_rows < p.ns) return SSM_ERR_INVALID_ARG;
   const int sms = num_sms_current();
   if (sms <= 0) return SSM_ERR_CUDA;
-  const size_t need = ssm::scan_fwd_ws_bytes(p, sms);
+  const size_t base = ssm::scan_fwd_ws_bytes(p, sms);
+  const size_t need = a_log_of(desc) ? ssm::align_up(base, 256) + a_bytes(p) : base;
   if (!ws || ws_bytes < need || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
   p.s0 = s0; p.ids = ids; p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.dt_bias = dt_bias;
   p.status = (int*)ws;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((rc = stage_a(desc, &p, ws, base, st)) != SSM_OK) return rc;
   cudaError_t e = ssm::launch_scan_fwd(p, y, state_out, ckpt, ws, sms, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -201,7 +220,8 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
   if (!ids && (s0 || d_s0) && p.state_rows < p.ns) return SSM_ERR_INVALID_ARG;
   const int sms = num_sms_current();
   if (sms <= 0) return SSM_ERR_CUDA;
-  const size_t need = ssm::scan_bwd_ws_bytes(p, sms);
+  const size_t base = ssm::scan_bwd_ws_bytes(p, sms);
+  const size_t need = a_log_of(desc) ? ssm::align_up(base, 256) + a_bytes(p) : base;
   if (!ws || ws_bytes < need || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
   p.s0 = s0; p.ids = ids; p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.dt_bias = dt_bias;
@@ -209,7 +229,9 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
   ScanGrads g{dy, d_state_out, d_s0, d_x, d_dt, d_A, d_B, d_C, d_D, d_z, d_dt_bias};
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((rc = stage_a(desc, &p, ws, base, st)) != SSM_OK) return rc;
   cudaError_t e = ssm::launch_scan_bwd(p, ckpt, g, ws, sms, st);
+  if (e == cudaSuccess && a_log_of(desc)) e = ssm::launch_scale_dA(d_A, p.A, a_count(p), st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -237,11 +259,13 @@ int ssm_decode_step(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags,
   if ((long long)p.state_rows * p.HP * p.N > kMaxTotal ||
       (long long)p.state_rows * p.HP * d_conv > kMaxTotal)
     return SSM_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < ssm::kStatusBytes || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
+  const size_t need = ssm::kStatusBytes + (a_log_of(desc) ? a_bytes(p) : 0);
+  if (!ws || ws_bytes < need || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
   p.ids = ids; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.dt_bias = dt_bias;
   p.status = (int*)ws;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((rc = stage_a(desc, &p, ws, ssm::kStatusBytes, st)) != SSM_OK) return rc;
   cudaError_t e = ssm::launch_decode_step(p, d_conv, (conv_flags & SSM_CONV_SILU) ? 1 : 0, x_new,
                                           conv_state, c, bias, state, y, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -66,6 +66,10 @@ size_t scan_bwd_ws_bytes(const ScanProblem& p, int num_sms);
 cudaError_t launch_scan_bwd(const ScanProblem& p, const float* ckpt, const ScanGrads& g, void* ws,
                             int num_sms, cudaStream_t st);
 
+// A_log parameterisation (params.cu): a = -exp(a_log); d_a *= a.
+cudaError_t launch_a_from_log(const float* a_log, float* a, int n, cudaStream_t st);
+cudaError_t launch_scale_dA(float* d_a, const float* a, int n, cudaStream_t st);
+
 // Single-token step (decode.cu): p describes one token per sequence (p.L == 1); conv_state
 // [rows][HP][K-1] and state [rows][HP][N] are updated in place at row ids[b] (or b).
 cudaError_t launch_decode_step(const ScanProblem& p, int K, int silu, const void* x_new,

@@ -81,7 +81,12 @@ enum {
 enum {
   SSM_CONV_SILU = 1u,    /* conv: apply SiLU after the convolution (+bias) */
   SSM_DT_SOFTPLUS = 2u,  /* scan: delta = softplus(dt + dt_bias) instead of delta = dt */
-  SSM_CHECK_FINITE = 4u  /* scan: record SSM_ERR_NONFINITE in the status word on a non-finite output */
+  SSM_CHECK_FINITE = 4u, /* scan: record SSM_ERR_NONFINITE in the status word on a non-finite output */
+  SSM_A_LOG = 8u         /* scan: the A argument holds A_log and the scan uses A = -exp(A_log)
+                            (infotheory's mamba1 parameterisation); d_A returns dL/dA_log =
+                            dL/dA * A.  The workspace grows by a buffer for A: the
+                            *_workspace_size results include it; ssm_decode_step then needs
+                            ws_bytes >= 256 + 4 * (elements of A) rounded up to 256. */
 };
 
 /* Limits (checked on the host; SSM_ERR_UNSUPPORTED beyond them).  Every tensor must also
@@ -101,7 +106,7 @@ typedef struct {
   int state_rows;   /* rows of s0 / d_s0; 0 means n_seqs.  Without ids, must be >= n_seqs */
   int chunk;        /* checkpoint interval in tokens; 0 means 256 */
   int io;           /* ssm_dtype of the activations */
-  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE */
+  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG */
 } ssm_scan_desc;
 
 /* ---- causal depthwise conv1d (+bias, +SiLU) --------------------------------------------
