@@ -1,6 +1,6 @@
-// params.cu -- the A_log parameterisation of the scan (infotheory's mamba1 model stores A_log
-// and uses A = -exp(A_log); kizzasi-model's SSM likewise keeps a log-parameterised decay):
-// A from A_log into scratch before a scan call, and dL/dA_log = dL/dA * A after the backward.
+// params.cu -- the A_log parameterisation of the scan (infotheory's mamba1 layer weights hold
+// A_log and A = -exp(A_log), and its gradient path turns dA into dA_log = dA * A): A from A_log
+// into scratch before a scan call, and dL/dA_log = dL/dA * A after the backward.
 #include "common.cuh"
 #include "kernels.cuh"
 
