@@ -307,22 +307,6 @@ __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
 }
 
 // ---- fixed-order reductions --------------------------------------------------------------
-template <typename IO>
-__global__ void reduce_bc_kernel(const BwdArgs a) {
-  const ScanProblem& p = a.p;
-  const long total = (long)p.ns * p.L * p.G * 2 * p.N;
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
-       i += (long)gridDim.x * blockDim.x) {
-    const int r = (int)(i % (2 * p.N));
-    const long tg = i / (2 * p.N);  // tok * G + g
-    const float* src = a.part_bc + tg * a.bpg * 2 * p.N + r;
-    float v = 0.0f;
-    for (int k = 0; k < a.bpg; k++) v += src[(long)k * 2 * p.N];
-    const int q = r / p.N, n = r - q * p.N;
-    st((IO*)(q == 0 ? a.g.d_B : a.g.d_C) + tg * p.N + n, v);
-  }
-}
-
 __global__ void reduce_params_kernel(const BwdArgs a) {
   const ScanProblem& p = a.p;
   const int nA = p.a_per_state ? p.H * p.N : p.H;
@@ -414,6 +398,10 @@ __global__ void reduce_ds0_kernel(const BwdArgs a) {
 
 // ---- host side -------------------------------------------------------------------------
 
+// Time segments of the head-tiled Mamba-2-form path: none when the (sequence, head, 32-channel
+// block) grid alone has this many blocks per SM, else enough to reach it.
+constexpr long kBwdHeadsBlocksPerSM = 3;
+
 static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   BwdPlan q{};
   int ns;
@@ -423,10 +411,18 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.bpg = (q.gc + cpb - 1) / cpb;
   q.chunk_b = p.chunk <= kMaxBwdChunk ? p.chunk : kDefaultChunk;
   q.nch_b = (p.L + q.chunk_b - 1) / q.chunk_b;
-  const long base_threads = (long)p.ns * p.G * q.bpg * kScanThreads;
-  const long target = (long)num_sms * kBwdTargetThreadsPerSM;
-  long S = base_threads >= (long)num_sms * kBwdNoSplitThreadsPerSM
-               ? 1 : (target + base_threads - 1) / base_threads;
+  q.heads = bwd_heads_applies(p, q.chunk_b);
+  long S;
+  if (q.heads) {  // the head-tiled path: blocks of 32 channels x 128 states
+    const long base = bwd_heads_blocks(p);
+    S = base >= kBwdHeadsBlocksPerSM * num_sms
+            ? 1 : (kBwdHeadsBlocksPerSM * num_sms + base - 1) / base;
+  } else {
+    const long base_threads = (long)p.ns * p.G * q.bpg * kScanThreads;
+    const long target = (long)num_sms * kBwdTargetThreadsPerSM;
+    S = base_threads >= (long)num_sms * kBwdNoSplitThreadsPerSM
+            ? 1 : (target + base_threads - 1) / base_threads;
+  }
   if (S > q.nch_b) S = q.nch_b;
   if (S < 1) S = 1;
   q.seg_chunks = (int)((q.nch_b + S - 1) / S);
@@ -457,6 +453,7 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
     const size_t blocks = (size_t)p.G * q.bpg * q.S * p.ns;
     q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsub) * kScanThreads);
   }
+  if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));
   q.bytes = off;
   const int nsub_max = (q.chunk_b + kTsub - 1) / kTsub;
   q.smem = sizeof(float4) * (size_t)nsub_max * kScanThreads +
@@ -485,6 +482,13 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const BwdPlan& q, char* w, cud
       return e;
     }
     scan_bwd_carry_kernel<<<blocks_for((long)p.ns * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
+  }
+  if (q.heads) {
+    cudaError_t e = launch_bwd_heads(a, (float*)(w + q.off_mh), st);
+    if (e != cudaSuccess) return e;
+    if (a.g.d_s0)
+      reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
+    return cudaGetLastError();
   }
   cudaError_t e = q.tma_tt ? launch_bwd_tma_main(a, q, w, st) : cudaErrorNotSupported;
   if (e == cudaErrorNotSupported) {

@@ -30,6 +30,23 @@ struct BwdArgs {
   float* dh0;         // [ns][HP][N]
 };
 
+// dB, dC of every (token, group) = the sum over the blocks' partials, in block order.
+template <typename IO>
+__global__ void reduce_bc_kernel(const BwdArgs a) {
+  const ScanProblem& p = a.p;
+  const long total = (long)p.ns * p.L * p.G * 2 * p.N;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    const int r = (int)(i % (2 * p.N));
+    const long tg = i / (2 * p.N);  // tok * G + g
+    const float* src = a.part_bc + tg * a.bpg * 2 * p.N + r;
+    float v = 0.0f;
+    for (int k = 0; k < a.bpg; k++) v += src[(long)k * 2 * p.N];
+    const int q = r / p.N, n = r - q * p.N;
+    st((IO*)(q == 0 ? a.g.d_B : a.g.d_C) + tg * p.N + n, v);
+  }
+}
+
 struct Lane {
   int tpc, cl, sg, g, blk, cig, ch, h, n0;
   bool valid;
@@ -65,9 +82,16 @@ __device__ __forceinline__ float delta_of(const ScanProblem& p, const IO* dt, lo
 struct BwdPlan {
   int tpc, gc, bpg, chunk_b, nch_b, S, seg_chunks;
   int tma_tt;  // tile tokens of the TMA-staged path; 0 when the shape does not allow it
+  bool heads;  // the Mamba-2-form path (scan_bwd_heads.cu) applies
   size_t off_fwd, fwd_bytes, off_ckpt, off_dhloc, off_segend, off_sumd, off_part_bc, off_dA,
-      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, bytes, smem;
+      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, bytes, smem;
 };
+
+// Mamba-2-form backward (scan_bwd_heads.cu): one A per head, head_dim % 32 == 0, d_state 128.
+bool bwd_heads_applies(const ScanProblem& p, int chunk_b);
+int bwd_heads_blocks(const ScanProblem& p);
+size_t bwd_heads_scratch_floats(const ScanProblem& p, int S, int chunk_b);
+cudaError_t launch_bwd_heads(const BwdArgs& a, float* scratch, cudaStream_t st);
 
 // TMA-staged backward kernels (scan_bwd_tma.cu), Mamba-1 layout with d_state 16.
 // bwd_tma_tile: the tile size this shape would use, 0 if the path cannot take it.
