@@ -35,6 +35,7 @@ struct BhArgs {
   BwdArgs a;       // problem, gradients, segment buffers of the general plan
   int bph;         // blocks per head (P / 32)
   int bpg;         // blocks per group ((H / G) * bph)
+  int vec;         // x, dy, z, B, C allow 4-element vector loads
   float* bnd;      // [blocks][S][tiles per chunk][threads][32]  tile start states
   float* hist;     // [blocks][S][16][threads][32]               states after each token
   float* part_dd;  // [ns * L][H][bph]   d delta partial of the block (before softplus')
@@ -51,6 +52,18 @@ struct BhSmem {
   float red[kBhGrp][kBhWarps][2 * kBhN];  // per warp: dB (0..127), dC (128..255)
   float dd[kBhThreads];                   // per thread: dD accumulators, then dA
 };
+
+// 4 consecutive values (16 bytes of fp32, 8 of bf16; aligned) as fp32.
+template <typename IO>
+__device__ __forceinline__ float4 bh_ld4(const IO* p) {
+  if constexpr (sizeof(IO) == 4) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+  } else {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  }
+}
 
 template <typename IO>
 __device__ __forceinline__ float bh_ld(const IO* p) {
@@ -81,29 +94,63 @@ __device__ void bh_load_tile(const BhArgs& A, BhSmem& S, long tok0, int cnt, int
     S.tc[tid][1] = dl;
     S.tc[tid][2] = spg;
   }
-  for (int idx = tid; idx < kBhTile * kBhP; idx += kBhThreads) {
-    const int i = idx / kBhP, c = idx - i * kBhP;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int idx = tid; idx < kBhTile * kBhP / 4; idx += kBhThreads) {  // 4 channels per item
+    const int i = idx / (kBhP / 4), c = (idx - i * (kBhP / 4)) * 4;
     const long off = (tok0 + i) * p.HP + ch0 + c;
     const bool in = i < cnt;
-    S.x[i][c] = in ? bh_ld(reinterpret_cast<const IO*>(p.x) + off) : 0.0f;
-    if (adjoint) {
-      const float dyv = in ? bh_ld(reinterpret_cast<const IO*>(A.a.g.dy) + off) : 0.0f;
-      float gy = dyv, dyg = 0.0f;
-      if (p.z && in) {
-        const float zv = bh_ld(reinterpret_cast<const IO*>(p.z) + off), sg = sigmoidf_(zv);
-        gy = dyv * zv * sg;
-        dyg = dyv * sg * (1.0f + zv * (1.0f - sg));
+    float xs[4], gys[4], dygs[4];
+    float4 v = zero4, dv = zero4, zv4 = zero4;
+    if (in) {
+      if (A.vec) {
+        v = bh_ld4(reinterpret_cast<const IO*>(p.x) + off);
+        if (adjoint) dv = bh_ld4(reinterpret_cast<const IO*>(A.a.g.dy) + off);
+        if (adjoint && p.z) zv4 = bh_ld4(reinterpret_cast<const IO*>(p.z) + off);
+      } else {
+        const IO* xp = reinterpret_cast<const IO*>(p.x) + off;
+        v = make_float4(bh_ld(xp), bh_ld(xp + 1), bh_ld(xp + 2), bh_ld(xp + 3));
+        if (adjoint) {
+          const IO* yp = reinterpret_cast<const IO*>(A.a.g.dy) + off;
+          dv = make_float4(bh_ld(yp), bh_ld(yp + 1), bh_ld(yp + 2), bh_ld(yp + 3));
+          if (p.z) {
+            const IO* zp = reinterpret_cast<const IO*>(p.z) + off;
+            zv4 = make_float4(bh_ld(zp), bh_ld(zp + 1), bh_ld(zp + 2), bh_ld(zp + 3));
+          }
+        }
       }
-      S.gy[i][c] = gy;
-      S.dyg[i][c] = dyg;
+    }
+    xs[0] = v.x; xs[1] = v.y; xs[2] = v.z; xs[3] = v.w;
+    const float dys[4] = {dv.x, dv.y, dv.z, dv.w}, zs[4] = {zv4.x, zv4.y, zv4.z, zv4.w};
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      gys[e] = dys[e];
+      dygs[e] = 0.0f;
+      if (adjoint && p.z && in) {
+        const float sg = sigmoidf_(zs[e]);
+        gys[e] = dys[e] * zs[e] * sg;
+        dygs[e] = dys[e] * sg * (1.0f + zs[e] * (1.0f - sg));
+      }
+    }
+    *reinterpret_cast<float4*>(&S.x[i][c]) = v;
+    if (adjoint) {
+      *reinterpret_cast<float4*>(&S.gy[i][c]) = make_float4(gys[0], gys[1], gys[2], gys[3]);
+      *reinterpret_cast<float4*>(&S.dyg[i][c]) = make_float4(dygs[0], dygs[1], dygs[2], dygs[3]);
     }
   }
-  for (int idx = tid; idx < kBhTile * kBhN; idx += kBhThreads) {
-    const int i = idx / kBhN, n = idx - i * kBhN;
+  for (int idx = tid; idx < kBhTile * kBhN / 4; idx += kBhThreads) {  // 4 states per item
+    const int i = idx / (kBhN / 4), n = (idx - i * (kBhN / 4)) * 4;
     const long off = ((tok0 + i) * p.G + g) * kBhN + n;
     const bool in = i < cnt;
-    S.B[i][n] = in ? bh_ld(reinterpret_cast<const IO*>(p.B) + off) : 0.0f;
-    if (adjoint) S.C[i][n] = in ? bh_ld(reinterpret_cast<const IO*>(p.C) + off) : 0.0f;
+    const IO* bp = reinterpret_cast<const IO*>(p.B) + off;
+    const IO* cp = reinterpret_cast<const IO*>(p.C) + off;
+    float4 bv = zero4, cv = zero4;
+    if (in) {
+      bv = A.vec ? bh_ld4(bp) : make_float4(bh_ld(bp), bh_ld(bp + 1), bh_ld(bp + 2), bh_ld(bp + 3));
+      if (adjoint)
+        cv = A.vec ? bh_ld4(cp) : make_float4(bh_ld(cp), bh_ld(cp + 1), bh_ld(cp + 2), bh_ld(cp + 3));
+    }
+    *reinterpret_cast<float4*>(&S.B[i][n]) = bv;
+    if (adjoint) *reinterpret_cast<float4*>(&S.C[i][n]) = cv;
   }
   __syncthreads();
   for (int idx = tid; idx < kBhTile * kBhP; idx += kBhThreads) {
@@ -263,10 +310,17 @@ scan_bwd_heads_kernel(const BhArgs A) {
         }
         bh_store(hist_slot(i), hv);
       }
-      // hv = state after the tile's last token: h_t of the first adjoint step
+      // hv = state after the tile's last token: h_t of the first adjoint step.  h_{t-1} of
+      // step i is loaded one step ahead (hn), so the scratch latency overlaps a step's work.
+      f2_t hn[kBhTP][kBhTN / 2];
+      bh_load(cnt > 1 ? hist_slot(cnt - 2) : bnd_slot(j), hn);
       for (int i = cnt - 1; i >= 0; i--) {
         f2_t hp[kBhTP][kBhTN / 2];
-        bh_load(i > 0 ? hist_slot(i - 1) : bnd_slot(j), hp);  // h_{t-1}
+#pragma unroll
+        for (int c = 0; c < kBhTP; c++)
+#pragma unroll
+          for (int q = 0; q < kBhTN / 2; q++) hp[c][q] = hn[c][q];  // h_{t-1}
+        if (i > 0) bh_load(i > 1 ? hist_slot(i - 2) : bnd_slot(j), hn);
         const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
         const float dl = S.tc[i][1];
         const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
@@ -490,6 +544,9 @@ cudaError_t launch_bwd_heads(const BwdArgs& a, float* scratch, cudaStream_t st) 
   A.bnd = scratch;
   A.hist = scratch + blocks * (size_t)(a.chunk_b / kBhTile) * kBhThreads * kBhTS;
   A.part_dd = a.ddt_part;
+  const uintptr_t al = p.io == SSM_BF16 ? 8 : 16;
+  auto ok = [&](const void* q) { return q == nullptr || ((uintptr_t)q % al) == 0; };
+  A.vec = ok(p.x) && ok(a.g.dy) && ok(p.z) && ok(p.B) && ok(p.C);
   A.dA_blk = a.dA_part;
   const dim3 grid(p.H * A.bph, a.S, p.ns);
   if (p.io == SSM_BF16)
