@@ -5,13 +5,14 @@
 
 namespace ssm {
 
-#define SSM_EXTERN_F32(NS, TPC, SA) \
-  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA>(FwdTmaArgs&, size_t, cudaStream_t);
+#define SSM_EXTERN_F32(NS, TPC, SA, THR) \
+  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR>(FwdTmaArgs&, size_t, cudaStream_t);
 SSM_FWD_TMA_VARIANTS(SSM_EXTERN_F32)
 #undef SSM_EXTERN_F32
 
-static bool instantiated(int ns, int tpc, bool scalar_a) {
-#define SSM_MATCH(NS, TPC, SA) if (ns == NS && tpc == TPC && scalar_a == SA) return true;
+static bool instantiated(int ns, int tpc, bool scalar_a, int thr = 128) {
+#define SSM_MATCH(NS, TPC, SA, THR) \
+  if (ns == NS && tpc == TPC && scalar_a == SA && thr == THR) return true;
   SSM_FWD_TMA_VARIANTS(SSM_MATCH)
 #undef SSM_MATCH
   return false;
@@ -19,7 +20,7 @@ static bool instantiated(int ns, int tpc, bool scalar_a) {
 
 struct FwdTmaPlan {
   bool ok;
-  int ns_state, tpc, cb, tt, S, seg_len;
+  int ns_state, tpc, thr, cb, tt, S, seg_len;
   size_t off_segstart, off_hloc, off_sumdelta, bytes;
 };
 
@@ -46,10 +47,12 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   if (ns == 0) return q;
   q.ns_state = ns;
   q.tpc = p.N / ns;
-  q.cb = kScanThreads / q.tpc;
+  q.thr = kScanThreads;
+  q.cb = q.thr / q.tpc;
   if ((p.H / p.G) % q.cb != 0 || p.HP % q.cb != 0 || q.cb * io < 16) return q;
   q.tt = kFwdTile;
-  const long base = (long)p.ns * (p.HP / q.cb);
+  // counted in 128-thread block equivalents, whatever the block size
+  const long base = (long)p.ns * (p.HP / q.cb) * q.thr / kScanThreads;
   long S = base >= kFwdNoSplitBlocksPerSM * num_sms
                ? 1 : (kFwdTargetBlocksPerSM * num_sms + base - 1) / base;
   const long max_s = (p.L + kMinSegment - 1) / kMinSegment;
@@ -112,9 +115,11 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_c = a.off_b + al(row);
   a.stage_stride = a.off_c + al(row);
   a.off_dd = kFwdStages * a.stage_stride;                       // float2 (delta, delta x)
-  a.off_bc = a.off_dd + al((uint32_t)(q.tt * q.cb * 8));         // B, C records
-  a.off_acc = a.off_bc + al((uint32_t)(q.tt * p.N * (io == 2 ? 4 : 8)));
-  a.off_par = a.off_acc + al((uint32_t)(q.tt * kScanThreads * 4));
+  // B and C of a tile as fp32 rows (bf16 I/O only; fp32 I/O reads the staged rows)
+  const uint32_t frow = io == 2 ? al((uint32_t)(q.tt * p.N * 4)) : 0u;
+  a.off_bf = a.off_dd + al((uint32_t)(q.tt * q.cb * 8));
+  a.off_cf = a.off_bf + frow;
+  a.off_par = a.off_cf + frow;
   a.off_y = a.off_par + al((uint32_t)(2 * q.cb * 4));
   a.y_stride = al(tile);
   a.off_bar = a.off_y + 2 * a.y_stride;
@@ -123,10 +128,10 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.bytes_local = 2 * tile + row;
   a.bytes_main = (2 + (p.z ? 1 : 0)) * tile + 2 * row;
   const bool sa = !p.a_per_state;
-#define SSM_DISPATCH(NS, TPC, SA)                                                   \
-  if (q.ns_state == NS && q.tpc == TPC && sa == SA)                                 \
-    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA>(a, smem, st)      \
-                   : launch_fwd_tma_t<float, NS, TPC, SA>(a, smem, st);
+#define SSM_DISPATCH(NS, TPC, SA, THR)                                              \
+  if (q.ns_state == NS && q.tpc == TPC && sa == SA && q.thr == THR)                 \
+    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA, THR>(a, smem, st) \
+                   : launch_fwd_tma_t<float, NS, TPC, SA, THR>(a, smem, st);
   SSM_FWD_TMA_VARIANTS(SSM_DISPATCH)
 #undef SSM_DISPATCH
   return cudaErrorNotSupported;

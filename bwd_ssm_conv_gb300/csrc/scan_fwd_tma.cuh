@@ -14,8 +14,10 @@
 // stores skip).
 //
 // Per tile a prepass does the per-(token, channel) work once -- delta (softplus when asked),
-// delta x -- and lays B and C out as one record per 4 states (B then C: 16 bytes for bf16,
-// 32 for fp32), so the recurrence reads a thread's states with one or two 16-byte loads.
+// delta x -- and converts bf16 B and C rows to fp32 once, so the recurrence reads 4 states of
+// B or C with one 16-byte shared load and no per-thread conversion.  The lanes of a channel
+// finish C . h with a shuffle reduce-scatter over groups of tokens and each writes the y of
+// one token, so no partial sums go through shared memory and no separate epilogue pass runs.
 // With one A per channel the decay is one exponential per (token, channel) for all states.
 // fp32 I/O uses the accurate decay form h <- h + (expm1(delta A) h + u) (scan_common.cuh).
 #pragma once
@@ -24,6 +26,8 @@
 #include "kernels.cuh"
 #include "scan_common.cuh"
 #include "tma.cuh"
+
+#include <type_traits>
 
 namespace ssm {
 
@@ -47,7 +51,7 @@ struct FwdTmaArgs {
   int has_y;
   uint32_t bytes_main, bytes_local;        // expected transaction bytes per stage
   uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride;  // inside a stage
-  uint32_t off_dd, off_bc, off_acc, off_par, off_y, y_stride, off_bar;
+  uint32_t off_dd, off_bf, off_cf, off_par, off_y, y_stride, off_bar;
 };
 
 template <typename IO>
@@ -56,44 +60,45 @@ __device__ __forceinline__ float lds1(const IO* p) {
   else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
 
-// A bf16 pair (one 32-bit word, low half first) as a packed fp32 pair; exact.
-__device__ __forceinline__ f2_t fwd_bf2_to_f2(uint32_t w) {
-  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// B and C of 4 states (n0 .. n0+3, n0 % 4 == 0) of token i from the record array.
-template <typename IO>
-__device__ __forceinline__ void ld_bc4(const unsigned char* rec, int i, int N, int n0,
-                                      f2_t (&B2)[2], f2_t (&C2)[2]) {
-  if constexpr (sizeof(IO) == 2) {
-    const uint4 v = reinterpret_cast<const uint4*>(rec)[(i * N + n0) / 4];
-    B2[0] = fwd_bf2_to_f2(v.x);
-    B2[1] = fwd_bf2_to_f2(v.y);
-    C2[0] = fwd_bf2_to_f2(v.z);
-    C2[1] = fwd_bf2_to_f2(v.w);
-  } else {
-    const float4* r = reinterpret_cast<const float4*>(rec) + 2 * ((i * N + n0) / 4);
-    const float4 vb = r[0], vc = r[1];
-    B2[0] = f2_pack(vb.x, vb.y);
-    B2[1] = f2_pack(vb.z, vb.w);
-    C2[0] = f2_pack(vc.x, vc.y);
-    C2[1] = f2_pack(vc.z, vc.w);
+// Sum over the TPC lanes of a channel group of v[0..TPC-1] (one value per token of a group of
+// TPC consecutive tokens), scattered: lane sg of the group ends with the total of token sg in
+// v[0].  Recursive halving: at distance d the lane keeps the half of its range that its bit d
+// selects and sends the other half to the partner, which keeps it.  TPC - 1 shuffles.
+template <int TPC>
+__device__ __forceinline__ float group_reduce_scatter(float (&v)[TPC], int sg) {
+#pragma unroll
+  for (int d = TPC / 2; d >= 1; d >>= 1) {
+    const bool up = (sg & d) != 0;
+#pragma unroll
+    for (int j = 0; j < d; j++) {
+      const float keep = up ? v[j + d] : v[j];
+      const float send = up ? v[j] : v[j + d];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+    }
   }
+  return v[0];
 }
 
-// A block = 128 threads = (128 / TPC) channels x N states, NS = N / TPC states per thread, one
+// A block = THR threads = (THR / TPC) channels x N states, NS = N / TPC states per thread, one
 // sequence, one time segment.  SCALAR_A: one A per channel (the head of head_dim 1).
-template <typename IO, int NS, int TPC, bool LOCAL, bool SCALAR_A>
-__global__ void __launch_bounds__(kScanThreads)
+//
+// Per tile: a prepass writes (delta, delta x) once per (token, channel) and, for bf16 I/O, B and
+// C as fp32 rows (fp32 I/O reads the staged rows as they are).  The recurrence then runs over
+// groups of TPC tokens; after each group the lanes of a channel reduce-scatter their partial
+// C . h sums so that lane sg holds token sg's total and writes that token's
+// y = (C . h + D x) silu(z) into the output tile itself.
+template <typename IO, int NS, int TPC, int THR, bool LOCAL, bool SCALAR_A>
+__global__ void __launch_bounds__(THR)
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;  // accurate decay form for fp32 I/O
   constexpr int TT = kFwdTile;
-  constexpr int tpc = TPC, cb = kScanThreads / TPC;  // compile-time: index math is shifts
-  static_assert(NS % 4 == 0, "states per thread come in records of 4");
+  constexpr int cb = THR / TPC;  // compile-time: index math is shifts
+  static_assert(NS % 4 == 0, "states per thread come in groups of 4");
+  static_assert(TT % TPC == 0, "token groups tile the staged tile");
   extern __shared__ __align__(128) unsigned char smem[];
   const ScanProblem& p = a.p;
   const int tid = threadIdx.x;
-  const int cl = tid / tpc, sg = tid - cl * tpc;
+  const int cl = tid / TPC, sg = tid - cl * TPC;
   const int ch0 = blockIdx.x * cb, ch = ch0 + cl;
   const int s = blockIdx.y, b = blockIdx.z;
   const int N = p.N, n0 = sg * NS;
@@ -104,15 +109,15 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   const bool want_y = !LOCAL && a.has_y;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
   float2* sDD = reinterpret_cast<float2*>(smem + a.off_dd);  // [TT][cb] (delta, delta x)
-  unsigned char* sBC = smem + a.off_bc;                       // [TT][N/4] records of B, C
-  float* sACC = reinterpret_cast<float*>(smem + a.off_acc);  // [TT][cb * tpc] partial C . h
+  float* sBf = reinterpret_cast<float*>(smem + a.off_bf);     // [TT][N] B as fp32 (bf16 I/O)
+  float* sCf = reinterpret_cast<float*>(smem + a.off_cf);     // [TT][N] C as fp32 (bf16 I/O)
   float* sPar = reinterpret_cast<float*>(smem + a.off_par);  // [cb] D, [cb] dt_bias
 
   if (tid == 0) {
     for (int i = 0; i < kFwdStages; i++) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
-  for (int c = tid; c < cb; c += kScanThreads) {
+  for (int c = tid; c < cb; c += THR) {
     sPar[c] = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
     sPar[cb + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
   }
@@ -153,12 +158,43 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       hp[j] = f2_pack(h0, h1);
     }
   }
+  const float Dc = sPar[cl];
   float sumd = 0.0f;
 
   for (int k = 0; k < ntiles; k++) {
     const int stg = k % kFwdStages;
     if (want_y && tid == 0) tma_store_wait_read<1>();  // store k-2 has read its y buffer
     const bool ok = mbar_wait(&full[stg], (uint32_t)(k / kFwdStages) & 1u);
+    unsigned char* base = smem + stg * a.stage_stride;
+    const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
+    const IO* sdt = reinterpret_cast<const IO*>(base + a.off_dt);
+    const IO* sz = reinterpret_cast<const IO*>(base + a.off_z);
+    const int t0 = t_begin + k * TT;
+    const int cnt = min(TT, t_end - t0);
+
+    // ---- prepass (a tile that never arrived leaves stale but in-bounds shared memory) ------
+    for (int idx = tid; idx < TT * cb; idx += THR) {
+      const int c = idx % cb;
+      float dl = lds1(sdt + idx);
+      if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
+      sDD[idx] = make_float2(dl, dl * lds1(sx + idx));
+    }
+    if constexpr (sizeof(IO) == 2) {
+      const uint2* rb = reinterpret_cast<const uint2*>(base + a.off_b);
+      const uint2* rc = reinterpret_cast<const uint2*>(base + a.off_c);
+      for (int idx = tid; idx < TT * N / 4; idx += THR) {
+        const uint2 vb = rb[idx];
+        reinterpret_cast<float4*>(sBf)[idx] =
+            make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
+                        __uint_as_float(vb.y << 16), __uint_as_float(vb.y & 0xffff0000u));
+        if (!LOCAL) {
+          const uint2 vc = rc[idx];
+          reinterpret_cast<float4*>(sCf)[idx] =
+              make_float4(__uint_as_float(vc.x << 16), __uint_as_float(vc.x & 0xffff0000u),
+                          __uint_as_float(vc.y << 16), __uint_as_float(vc.y & 0xffff0000u));
+        }
+      }
+    }
     if (__syncthreads_or(!ok)) {  // a tile never arrived: report, drain, leave
       if (tid == 0) {
         record_status(p.status, SSM_ERR_TIMEOUT);
@@ -168,34 +204,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
       return;
     }
-    unsigned char* base = smem + stg * a.stage_stride;
-    const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
-    const IO* sdt = reinterpret_cast<const IO*>(base + a.off_dt);
-    const IO* sz = reinterpret_cast<const IO*>(base + a.off_z);
-    const int t0 = t_begin + k * TT;
-    const int cnt = min(TT, t_end - t0);
-
-    // ---- prepass, once per (token, channel): delta, delta x; B, C records -------------------
-    for (int idx = tid; idx < TT * cb; idx += kScanThreads) {
-      const int i = idx / cb, c = idx - i * cb;
-      float dl = lds1(sdt + idx);
-      if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
-      sDD[idx] = make_float2(dl, dl * lds1(sx + idx));
-    }
-    for (int idx = tid; idx < TT * N / 4; idx += kScanThreads) {
-      if constexpr (sizeof(IO) == 2) {
-        const uint2 vb = reinterpret_cast<const uint2*>(base + a.off_b)[idx];
-        const uint2 vc = LOCAL ? make_uint2(0u, 0u) : reinterpret_cast<const uint2*>(base + a.off_c)[idx];
-        reinterpret_cast<uint4*>(sBC)[idx] = make_uint4(vb.x, vb.y, vc.x, vc.y);
-      } else {
-        const float4 vb = reinterpret_cast<const float4*>(base + a.off_b)[idx];
-        const float4 vc = LOCAL ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : reinterpret_cast<const float4*>(base + a.off_c)[idx];
-        reinterpret_cast<float4*>(sBC)[2 * idx] = vb;
-        reinterpret_cast<float4*>(sBC)[2 * idx + 1] = vc;
-      }
-    }
-    __syncthreads();
+    const float* Bf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_b) : sBf;
+    const float* Cf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_c) : sCf;
 
     // ---- the recurrence: per thread, its channel's NS states over the tile ------------------
     if (!LOCAL && a.ckpt && t0 % p.chunk == 0) {  // checkpoints fall on tile starts
@@ -208,7 +218,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         *reinterpret_cast<float4*>(dst + 2 * j) = make_float4(x0, x1, x2, x3);
       }
     }
-    auto token = [&](int i) {
+    // one token: advance the states; returns this thread's part of C . h
+    auto token = [&](int i) -> float {
       const float2 dd = sDD[i * cb + cl];
       const f2_t dx2 = f2_pack(dd.y, dd.y);
       f2_t dl2 = 0ull, cs2 = 0ull;
@@ -221,8 +232,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       f2_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
       for (int j = 0; j < NS; j += 4) {
-        f2_t B2[2], C2[2];
-        ld_bc4<IO>(sBC, i, N, n0 + j, B2, C2);
+        const float4 vb = *reinterpret_cast<const float4*>(Bf + i * N + n0 + j);
+        const f2_t B2[2] = {f2_pack(vb.x, vb.y), f2_pack(vb.z, vb.w)};
         const int q = j / 2;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
@@ -230,62 +241,52 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
           hp[q + e] = step2<ACC>(cf2, hp[q + e], f2_mul(dx2, B2[e]));
         }
         if (!LOCAL) {
-          acc0 = f2_fma(C2[0], hp[q], acc0);
-          acc1 = f2_fma(C2[1], hp[q + 1], acc1);
+          const float4 vc = *reinterpret_cast<const float4*>(Cf + i * N + n0 + j);
+          acc0 = f2_fma(f2_pack(vc.x, vc.y), hp[q], acc0);
+          acc1 = f2_fma(f2_pack(vc.z, vc.w), hp[q + 1], acc1);
         }
       }
       if (LOCAL) {
         sumd += dd.x;
-      } else {
-        float lo, hi;
-        f2_unpack(f2_add(acc0, acc1), lo, hi);
-        sACC[i * cb * tpc + tid] = lo + hi;
+        return 0.0f;
+      }
+      return f2_sum(f2_add(acc0, acc1));
+    };
+    IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
+    // one group of TPC tokens; FULL: every token of the group is inside the sequence
+    auto group = [&](int i0, auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
+      float acc[TPC];
+#pragma unroll
+      for (int u = 0; u < TPC; u++) acc[u] = (FULL || i0 + u < cnt) ? token(i0 + u) : 0.0f;
+      if (LOCAL) return;
+      const float tot = group_reduce_scatter<TPC>(acc, sg);
+      if (want_y) {  // token i0 + sg of channel cl (rows past the sequence end are not stored)
+        const int idx = (i0 + sg) * cb + cl;
+        float yv = fmaf(Dc, lds1(sx + idx), tot);
+        if (p.z) yv *= siluf_(lds1(sz + idx));
+        if (p.check_finite && (FULL || i0 + sg < cnt) && !isfinite(yv))
+          record_status(p.status, SSM_ERR_NONFINITE);
+        if constexpr (sizeof(IO) == 4) sy[idx] = yv;
+        else sy[idx] = __float2bfloat16_rn(yv);
       }
     };
     if (cnt == TT) {  // full tile: no per-token branch, so tokens can interleave
 #pragma unroll
-      for (int i = 0; i < TT; i++) token(i);
+      for (int i0 = 0; i0 < TT; i0 += TPC) group(i0, std::true_type{});
     } else {
 #pragma unroll
-      for (int i = 0; i < TT; i++)
-        if (i < cnt) token(i);
+      for (int i0 = 0; i0 < TT; i0 += TPC) group(i0, std::false_type{});
     }
-    __syncthreads();
-
-    // ---- epilogue, once per (token, channel): y = (C . h + D x) silu(z) -> TMA store -----------
-    if (want_y) {
-      IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
-      for (int idx = tid; idx < cnt * cb; idx += kScanThreads) {
-        const int i = idx / cb, c = idx - i * cb;
-        const float* pa = sACC + (i * cb + c) * tpc;  // the channel's tpc partials, contiguous
-        float acc;
-        if constexpr (tpc == 8) {
-          const float4 v = *reinterpret_cast<const float4*>(pa);
-          const float4 w = *reinterpret_cast<const float4*>(pa + 4);
-          acc = ((v.x + v.y) + (v.z + v.w)) + ((w.x + w.y) + (w.z + w.w));
-        } else if constexpr (tpc == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(pa);
-          acc = (v.x + v.y) + (v.z + v.w);
-        } else if constexpr (tpc == 2) {
-          const float2 v = *reinterpret_cast<const float2*>(pa);
-          acc = v.x + v.y;
-        } else {
-          acc = pa[0];
-        }
-        float yv = fmaf(sPar[c], lds1(sx + idx), acc);
-        if (p.z) yv *= siluf_(lds1(sz + idx));
-        if (p.check_finite && !isfinite(yv)) record_status(p.status, SSM_ERR_NONFINITE);
-        if constexpr (sizeof(IO) == 4) sy[idx] = yv;
-        else sy[idx] = __float2bfloat16_rn(yv);
-      }
-      fence_async_shared();
-      __syncthreads();  // y tile complete; stage stg fully read
-      if (tid == 0) {
+    if (want_y) fence_async_shared();
+    __syncthreads();  // y tile complete; stage stg and the prepass buffers fully read
+    if (tid == 0) {
+      if (want_y) {
         tma_store_3d(&a.my, sy, ch0, t0, b);
         tma_store_commit();
       }
+      if (k + kFwdStages < ntiles) issue(k + kFwdStages);
     }
-    if (tid == 0 && k + kFwdStages < ntiles) issue(k + kFwdStages);
   }
   if (want_y && tid == 0) tma_store_wait_all();
 
@@ -326,28 +327,29 @@ __global__ void scan_fwd_tma_carry_kernel(const __grid_constant__ FwdTmaArgs a) 
   }
 }
 
-template <typename IO, int NS, int TPC, bool SCALAR_A>
+template <typename IO, int NS, int TPC, bool SCALAR_A, int THR>
 cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
-  auto km = scan_fwd_tma_kernel<IO, NS, TPC, false, SCALAR_A>;
-  auto kl = scan_fwd_tma_kernel<IO, NS, TPC, true, SCALAR_A>;
+  auto km = scan_fwd_tma_kernel<IO, NS, TPC, THR, false, SCALAR_A>;
+  auto kl = scan_fwd_tma_kernel<IO, NS, TPC, THR, true, SCALAR_A>;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int bx = a.p.HP / a.cb;
   if (a.S > 1) {
-    kl<<<dim3(bx, a.S - 1, a.p.ns), kScanThreads, smem, st>>>(a), count_launches(1);
+    kl<<<dim3(bx, a.S - 1, a.p.ns), THR, smem, st>>>(a), count_launches(1);
     const long total = (long)a.p.ns * a.p.HP * a.p.N;
     scan_fwd_tma_carry_kernel<IO><<<(int)((total + 255) / 256), 256, 0, st>>>(a), count_launches(1);
   }
-  km<<<dim3(bx, a.S, a.p.ns), kScanThreads, smem, st>>>(a), count_launches(1);
+  km<<<dim3(bx, a.S, a.p.ns), THR, smem, st>>>(a), count_launches(1);
   return cudaGetLastError();
 }
 
-// The (states per thread, threads per channel, A form) combinations instantiated for each I/O
-// type; X(NS, TPC, SCALAR_A).
+// The (states per thread, threads per channel, A form, block threads) combinations instantiated
+// for each I/O type; X(NS, TPC, SCALAR_A, THR).
 #define SSM_FWD_TMA_VARIANTS(X) \
-  X(16, 1, false) X(8, 2, false) X(4, 4, false) X(16, 2, false) X(8, 4, false) X(16, 4, false) \
-  X(16, 8, true) X(8, 4, true) X(16, 4, true) X(4, 4, true)
+  X(16, 1, false, 128) X(8, 2, false, 128) X(4, 4, false, 128) X(16, 2, false, 128) \
+  X(8, 4, false, 128) X(16, 4, false, 128) X(16, 8, true, 128) X(8, 4, true, 128) \
+  X(16, 4, true, 128) X(4, 4, true, 128)
 
 }  // namespace ssm
