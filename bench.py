@@ -74,12 +74,12 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16>",
-        "bytes": 472173056 + 672165632,
+        "bytes": 472008448 + 671865600,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
                 "9697604387c734027bc4e8f5b3b91571b6f347ca15c43c0d79246f7cfef7c467",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
-                "02495c2a1664a92abfc2ed6cd2cd1cfb1ad3cbced02778247fb73bbd0072dbbe",
+                "86ccb87afc65ae1c37670cde906c2143e309573a654f307343a7bfc832f51a8c",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
                 "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
         },

@@ -425,6 +425,14 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   }
   if (S > q.nch_b) S = q.nch_b;
   if (S < 1) S = 1;
+  q.tma_tt = q.heads ? 0 : bwd_tma_tile(p, q.chunk_b, q.tpc, q.gc);
+  // Without time segments the (sequence, channel block) chains alone fill the GPU, but as whole
+  // launches they quantise into waves (e.g. 768 chains on 456 resident blocks = 1.68 waves).
+  // The TMA path then runs persistent blocks over (chain, chunk) units instead: every chunk
+  // is a segment, and no local adjoint pass is needed because each unit waits for the start
+  // adjoint of the chunk after it, which a unit taken earlier from the queue produces.
+  q.persist = q.tma_tt && S == 1 && q.nch_b >= 2;
+  if (q.persist) S = q.nch_b;
   q.seg_chunks = (int)((q.nch_b + S - 1) / S);
   q.S = (q.nch_b + q.seg_chunks - 1) / q.seg_chunks;
 
@@ -448,10 +456,12 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.off_dtb = take(segch);
   q.off_ddt = take(p.P > 1 ? F * (size_t)p.ns * p.L * p.HP : 0);
   q.off_dh0 = take(F * (size_t)p.ns * p.HP * p.N);
-  q.tma_tt = bwd_tma_tile(p, q.chunk_b, q.tpc, q.gc);
   if (q.tma_tt) {
-    const size_t blocks = (size_t)p.G * q.bpg * q.S * p.ns;
+    const size_t units = (size_t)p.G * q.bpg * q.S * p.ns;
+    const size_t slots = (size_t)num_sms * kBwdPersistBlocksPerSM;
+    const size_t blocks = q.persist && slots < units ? slots : units;  // one per resident block
     q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsub) * kScanThreads);
+    if (q.persist) q.off_queue = take(sizeof(int) * (1 + units));  // counter, then unit flags
   }
   if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));
   q.bytes = off;
@@ -473,7 +483,10 @@ static int blocks_for(long total) {
 template <typename IO, bool SCALAR_A, bool FULL>
 static cudaError_t launch_bwd_t(const BwdArgs& a, const BwdPlan& q, char* w, cudaStream_t st) {
   const ScanProblem& p = a.p;
-  if (a.S > 1) {
+  // the persistent TMA path needs no local adjoint pass; if its pointers do not allow TMA, the
+  // general kernels take the same segments with one
+  const bool persist = q.persist && bwd_tma_ready(a, q);
+  if (a.S > 1 && !persist) {
     cudaError_t e = q.tma_tt ? launch_bwd_tma_local(a, q, w, st) : cudaErrorNotSupported;
     if (e == cudaErrorNotSupported) {
       dim3 g1(p.G * a.bpg, a.S - 1, p.ns);

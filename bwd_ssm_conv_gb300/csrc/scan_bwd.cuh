@@ -52,13 +52,15 @@ struct Lane {
   bool valid;
 };
 
-__device__ __forceinline__ Lane lane_of(const BwdArgs& a) {
+// bx: the block's index along (group, channel block), blockIdx.x unless a persistent block
+// takes its work units from a queue.
+__device__ __forceinline__ Lane lane_of(const BwdArgs& a, int bx) {
   Lane l;
   l.tpc = a.tpc;
   l.cl = threadIdx.x / l.tpc;
   l.sg = threadIdx.x - l.cl * l.tpc;
-  l.g = blockIdx.x / a.bpg;
-  l.blk = blockIdx.x - l.g * a.bpg;
+  l.g = bx / a.bpg;
+  l.blk = bx - l.g * a.bpg;
   l.cig = l.blk * (kScanThreads / l.tpc) + l.cl;
   l.valid = l.cig < a.gc;
   l.ch = l.g * a.gc + (l.valid ? l.cig : 0);
@@ -66,6 +68,7 @@ __device__ __forceinline__ Lane lane_of(const BwdArgs& a) {
   l.n0 = l.sg * kBwdNS;
   return l;
 }
+__device__ __forceinline__ Lane lane_of(const BwdArgs& a) { return lane_of(a, blockIdx.x); }
 
 template <typename IO>
 __device__ __forceinline__ float delta_of(const ScanProblem& p, const IO* dt, long tok, int h,
@@ -83,9 +86,15 @@ struct BwdPlan {
   int tpc, gc, bpg, chunk_b, nch_b, S, seg_chunks;
   int tma_tt;  // tile tokens of the TMA-staged path; 0 when the shape does not allow it
   bool heads;  // the Mamba-2-form path (scan_bwd_heads.cu) applies
+  // Persistent TMA path: every chunk is a segment (S == nch_b), resident blocks take (chain,
+  // chunk) units from a queue, last chunk first, and hand each chunk's start adjoint to the unit
+  // of the chunk before it (see scan_bwd_tma.cu).
+  bool persist;
   size_t off_fwd, fwd_bytes, off_ckpt, off_dhloc, off_segend, off_sumd, off_part_bc, off_dA,
-      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, bytes, smem;
+      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, off_queue, bytes, smem;
 };
+// Resident blocks per SM the persistent path is sized for (the kernel's launch bound).
+constexpr int kBwdPersistBlocksPerSM = 3;
 
 // Mamba-2-form backward (scan_bwd_heads.cu): one A per head, head_dim % 32 == 0, d_state 128.
 bool bwd_heads_applies(const ScanProblem& p, int chunk_b);
@@ -100,5 +109,7 @@ int bwd_tma_tile(const ScanProblem& p, int chunk_b, int tpc, int gc);
 // path; the caller then runs the general kernels.
 cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st);
 cudaError_t launch_bwd_tma_main(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st);
+// Whether launch_bwd_tma_main will take this call (the plan allows TMA and the pointers do).
+bool bwd_tma_ready(const BwdArgs& a, const BwdPlan& q);
 
 }  // namespace ssm

@@ -35,7 +35,30 @@ struct BwdTma {
   uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
   float4* bnd;
+  // persistent mode: unit queue counter, per-unit ready flags, units, chains, chain stride
+  int* counter;
+  int* flags;
+  int units, chains, gx;
 };
+
+constexpr uint32_t kFlagSpin = 1u << 22;  // polls of a unit flag before the wait gives up
+
+// Waits (bounded) until another block has published *flag; gives up at once when any block has
+// recorded an error in the status word, so that one failure cannot chain into long waits.
+__device__ __forceinline__ bool wait_unit_flag(const int* flag, const int* status) {
+  for (uint32_t i = 0; i < kFlagSpin; i++) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) return true;
+    if (status && *reinterpret_cast<const volatile int*>(status)) return false;
+    __nanosleep(64);
+  }
+  return false;
+}
+__device__ __forceinline__ void publish_unit_flag(int* flag) {
+  __threadfence();
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
 
 int bwd_tma_tile(const ScanProblem& p, int chunk_b, int tpc, int gc) {
   const int io = p.io == SSM_BF16 ? 2 : 4;
@@ -133,19 +156,48 @@ __device__ __forceinline__ f2_t reduce_bc_warp(f2_t dB01, f2_t dB23, f2_t dC01, 
   return f2_add(x, f2_pack(__shfl_xor_sync(0xffffffffu, xb, 4), __shfl_xor_sync(0xffffffffu, xc, 4)));
 }
 
-template <typename IO>
-__global__ void __launch_bounds__(kScanThreads, 3)
+// PERSIST: the grid is a set of resident blocks that take (chain, chunk) units from a queue in
+// the order chunk-major, last chunk first (unit u: chain u % chains, chunk nch - 1 - u / chains),
+// so the unit that produces a chunk's end adjoint (the start adjoint of the chunk after it) was
+// taken from the queue `chains` units earlier by a running block.  Otherwise one block = one
+// (sequence, channel block, segment) of whole chunks, as given by the grid.
+template <typename IO, bool PERSIST>
+__global__ void __launch_bounds__(kScanThreads, kBwdPersistBlocksPerSM)
 scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;
   constexpr int TT = kBwdTile, CB = kCB, N = 16;
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int sUnit;
   const ScanProblem& p = a.p;
-  const Lane l = lane_of(a);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
   const int pm = (lane >> 3) & 3;  // slot j holds state n0 + (j ^ pm)
-  const int s = blockIdx.y, b = blockIdx.z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
+  if (tid == 0) {
+    for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  // ring cursors run on across units: a stage's barrier phase follows the count of its uses
+  int issued = 0, qpos = 0, n_l2 = 0;
+  for (int round = 0;; round++) {
+  int ux, s, b;
+  if constexpr (PERSIST) {
+    if (tid == 0) {
+      const bool failed = p.status && *reinterpret_cast<const volatile int*>(p.status) != 0;
+      sUnit = failed ? m.units : atomicAdd(m.counter, 1);
+    }
+    __syncthreads();
+    const int u = sUnit;
+    if (u >= m.units) break;
+    const int chain = u % m.chains;
+    s = a.nch_b - 1 - u / m.chains;
+    ux = chain % m.gx;
+    b = chain / m.gx;
+  } else {
+    if (round > 0) break;
+    ux = blockIdx.x; s = blockIdx.y; b = blockIdx.z;
+  }
+  const Lane l = lane_of(a, ux);
+  const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
   float2* sD2 = reinterpret_cast<float2*>(smem + m.off_p);       // [TT][CB] (delta, delta x)
   float* sGy = reinterpret_cast<float*>(smem + m.off_spg);       // [TT][CB] gy = dy silu(z)
   float4* sE = reinterpret_cast<float4*>(smem + m.off_e);        // [TT][CB] (x, gy, dyg, softplus')
@@ -156,7 +208,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);      // D[CB], dt_bias[CB]
   float* sAcc = reinterpret_cast<float*>(smem + m.off_acc);      // [warps][CB][2]
   const int nsub_max = a.chunk_b / kTsub;
-  float4* bnd = m.bnd + ((long)(b * a.S + s) * gridDim.x + blockIdx.x) * nsub_max * kScanThreads;
+  float4* bnd = m.bnd + (PERSIST ? (long)blockIdx.x
+                                 : ((long)(b * a.S + s) * gridDim.x + blockIdx.x)) *
+                            nsub_max * kScanThreads;
   const int c_first = s * a.seg_chunks;
   const int c_last = min(a.nch_b, c_first + a.seg_chunks) - 1;
 
@@ -177,17 +231,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
   };
 
-  if (tid == 0) {
-    for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
-    fence_barrier_init();
-  }
   for (int c = tid; c < CB; c += kScanThreads) {
     sPar[c] = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
     sPar[CB + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
   }
   __syncthreads();
   Pos pp = first();
-  int issued = 0;
   auto issue = [&]() {  // thread 0 only
     const int stg = issued % kBwdStages;
     unsigned char* base = smem + stg * m.stage_stride;
@@ -215,11 +264,20 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   f2_t A2p[2], Anp[2], carry2[2], dA2[2] = {0ull, 0ull}, hp[2] = {0ull, 0ull};
   {
     const long si = ((long)b * a.S + s) * p.HP + ch;
+    // the adjoint at the segment's end: given by the caller for the last one; else from the
+    // carry pass, or (persistent) from the unit of the next chunk once it has published it
+    const bool from_next = a.S > 1 && s < a.S - 1;
+    if (PERSIST && from_next) {
+      if (tid == 0 &&
+          !wait_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s, p.status))
+        record_status(p.status, SSM_ERR_TIMEOUT);
+      __syncthreads();
+    }
     float cv[4], av[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const int n = n0 + (j ^ pm);
-      if (a.S > 1) cv[j] = a.segend[si * N + n];
+      if (from_next) cv[j] = __ldcg(a.segend + si * N + n);
       else cv[j] = a.g.d_state_out ? __ldg(a.g.d_state_out + ((long)b * p.HP + ch) * N + n) : 0.0f;
       av[j] = __ldg(p.A + (long)ch * N + n);
     }
@@ -232,9 +290,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
   }
   float dD_acc = 0.0f, dtb_acc = 0.0f;  // of channel tid % CB, over this thread's epilogue items
-  int n_l2 = 0;
 
-  int qpos = 0;
   for (Pos cs = first(); cs.ck >= c_first; advance(cs), qpos++) {
     const int stg = qpos % kBwdStages;
     if (cs.lvl == 1 && tid == 0) tma_store_wait_read<1>();  // out buffer (n_l2 & 1) is free
@@ -488,6 +544,16 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     a.dD_part[sc] = vD;
     a.dtb_part[sc] = vT;
   }
+  if (PERSIST && s > 0) {  // this chunk's start adjoint ends chunk s - 1: hand it over
+    const long se = ((long)b * a.S + s - 1) * p.HP + ch;
+#pragma unroll
+    for (int q = 0; q < 2; q++)
+      f2_unpack(carry2[q], a.segend[se * N + n0 + ((2 * q) ^ pm)],
+                a.segend[se * N + n0 + ((2 * q + 1) ^ pm)]);
+    __syncthreads();
+    if (tid == 0) publish_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s - 1);
+  }
+  }  // units
 }
 
 // Local adjoint of segments 1..S-1 (zero adjoint at the segment end), tiles in reverse.
@@ -637,28 +703,62 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->bytes_l1 = 2 * tile + row;
   m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
   m->bytes_loc = (2 + (p.z ? 1 : 0)) * tile + row;
-  m->bnd = reinterpret_cast<float4*>(w + q.off_bnd);
+  m->bnd = w ? reinterpret_cast<float4*>(w + q.off_bnd) : nullptr;
   return true;
+}
+
+bool bwd_tma_ready(const BwdArgs& a, const BwdPlan& q) {
+  BwdTma m;
+  return setup_bwd_tma(a, q, nullptr, &m);
+}
+
+// Zeroes the persistent path's queue counter and unit flags (the workspace holds anything).
+__global__ void bwd_queue_reset_kernel(int* q, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) q[i] = 0;
+}
+
+template <typename IO, bool PERSIST>
+static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, int num_sms,
+                                 cudaStream_t st) {
+  const ScanProblem& p = a.p;
+  auto k = scan_bwd_tma_kernel<IO, PERSIST>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+  if (e != cudaSuccess) return e;
+  if (!PERSIST) {
+    k<<<dim3(p.G * a.bpg, a.S, p.ns), kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+    return cudaGetLastError();
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kScanThreads, m.smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorNotSupported;
+  if (per_sm > kBwdPersistBlocksPerSM) per_sm = kBwdPersistBlocksPerSM;  // the scratch is sized so
+  m.gx = p.G * a.bpg;
+  m.chains = m.gx * p.ns;
+  m.units = m.chains * a.nch_b;
+  const long slots = (long)per_sm * num_sms;
+  const int grid = (int)(slots < m.units ? slots : m.units);
+  bwd_queue_reset_kernel<<<(1 + m.units + 255) / 256, 256, 0, st>>>(m.counter, 1 + m.units),
+      count_launches(1);
+  k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_tma_main(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st) {
   BwdTma m;
   if (!setup_bwd_tma(a, q, ws, &m)) return cudaErrorNotSupported;
-  const ScanProblem& p = a.p;
-  dim3 grid(p.G * a.bpg, a.S, p.ns);
-  cudaError_t e;
-  if (p.io == SSM_BF16) {
-    auto k = scan_bwd_tma_kernel<__nv_bfloat16>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
-  } else {
-    auto k = scan_bwd_tma_kernel<float>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+  int dev = 0, num_sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (q.persist) {
+    m.counter = reinterpret_cast<int*>(ws + q.off_queue);
+    m.flags = m.counter + 1;
+    return a.p.io == SSM_BF16 ? launch_main_t<__nv_bfloat16, true>(m, a, q, num_sms, st)
+                              : launch_main_t<float, true>(m, a, q, num_sms, st);
   }
-  return cudaGetLastError();
+  return a.p.io == SSM_BF16 ? launch_main_t<__nv_bfloat16, false>(m, a, q, num_sms, st)
+                            : launch_main_t<float, false>(m, a, q, num_sms, st);
 }
 
 cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st) {

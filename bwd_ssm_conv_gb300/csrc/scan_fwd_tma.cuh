@@ -218,17 +218,21 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         *reinterpret_cast<float4*>(dst + 2 * j) = make_float4(x0, x1, x2, x3);
       }
     }
-    // one token: advance the states; returns this thread's part of C . h
-    auto token = [&](int i) -> float {
-      const float2 dd = sDD[i * cb + cl];
-      const f2_t dx2 = f2_pack(dd.y, dd.y);
-      f2_t dl2 = 0ull, cs2 = 0ull;
+    // the decay coefficients of one token (one per state pair, or one for all states)
+    auto decays = [&](float dl, f2_t (&cf)[NS / 2]) {
       if constexpr (SCALAR_A) {
-        const float cf = decay_coef<ACC>(dd.x, A2s);  // one decay for all the thread's states
-        cs2 = f2_pack(cf, cf);
+        const float c = decay_coef<ACC>(dl, A2s);
+#pragma unroll
+        for (int q = 0; q < NS / 2; q++) cf[q] = f2_pack(c, c);
       } else {
-        dl2 = f2_pack(dd.x, dd.x);
+        const f2_t dl2 = f2_pack(dl, dl);
+#pragma unroll
+        for (int q = 0; q < NS / 2; q++) cf[q] = decay2<ACC>(dl2, A2p[q]);
       }
+    };
+    // one token: advance the states with its decays; returns this thread's part of C . h
+    auto token = [&](int i, float2 dd, const f2_t (&cf)[NS / 2]) -> float {
+      const f2_t dx2 = f2_pack(dd.y, dd.y);
       f2_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
       for (int j = 0; j < NS; j += 4) {
@@ -236,10 +240,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         const f2_t B2[2] = {f2_pack(vb.x, vb.y), f2_pack(vb.z, vb.w)};
         const int q = j / 2;
 #pragma unroll
-        for (int e = 0; e < 2; e++) {
-          const f2_t cf2 = SCALAR_A ? cs2 : decay2<ACC>(dl2, A2p[SCALAR_A ? 0 : q + e]);
-          hp[q + e] = step2<ACC>(cf2, hp[q + e], f2_mul(dx2, B2[e]));
-        }
+        for (int e = 0; e < 2; e++) hp[q + e] = step2<ACC>(cf[q + e], hp[q + e], f2_mul(dx2, B2[e]));
         if (!LOCAL) {
           const float4 vc = *reinterpret_cast<const float4*>(Cf + i * N + n0 + j);
           acc0 = f2_fma(f2_pack(vc.x, vc.y), hp[q], acc0);
@@ -253,12 +254,39 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       return f2_sum(f2_add(acc0, acc1));
     };
     IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
+    // fp32 I/O with one A per state: the decays of a whole group (the long accurate expm1 form)
+    // are computed before its state updates, which do not feed them, so their latency overlaps
+    // the update chain (measured faster).  bf16 I/O makes them token by token: batched there,
+    // the one-instruction SFU decays measured 45 % slower.  Large groups would not fit in
+    // registers, and the one-A-per-channel form has a single decay per token.
+    constexpr bool BATCH = ACC && !SCALAR_A && TPC * NS <= 32;
     // one group of TPC tokens; FULL: every token of the group is inside the sequence
     auto group = [&](int i0, auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;
       float acc[TPC];
+      if constexpr (BATCH) {
+        float2 dd[TPC];
+        f2_t cf[TPC][NS / 2];
 #pragma unroll
-      for (int u = 0; u < TPC; u++) acc[u] = (FULL || i0 + u < cnt) ? token(i0 + u) : 0.0f;
+        for (int u = 0; u < TPC; u++) {
+          dd[u] = sDD[(i0 + u) * cb + cl];
+          decays(dd[u].x, cf[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < TPC; u++)
+          acc[u] = (FULL || i0 + u < cnt) ? token(i0 + u, dd[u], cf[u]) : 0.0f;
+      } else {
+#pragma unroll
+        for (int u = 0; u < TPC; u++) {
+          acc[u] = 0.0f;
+          if (FULL || i0 + u < cnt) {
+            const float2 dd = sDD[(i0 + u) * cb + cl];
+            f2_t cf[NS / 2];
+            decays(dd.x, cf);
+            acc[u] = token(i0 + u, dd, cf);
+          }
+        }
+      }
       if (LOCAL) return;
       const float tot = group_reduce_scatter<TPC>(acc, sg);
       if (want_y) {  // token i0 + sg of channel cl (rows past the sequence end are not stored)

@@ -96,6 +96,33 @@ def test_scan_backward_parity(case):
     assert binding.ssm_scan_status(g["_ws"]) == 0
 
 
+# Enough (sequence, 32-channel block) chains to fill a 152-SM GPU without time segments (20 x 32
+# = 640): the backward then runs resident blocks over (chain, chunk) units, last chunk first,
+# each handing its chunk's start adjoint to the unit of the chunk before it.  Ragged last chunk.
+PERSIST_CASES = [
+    ("persist_bf16", (20, 100, 1024, 1, 16, 1), "bf16", 32, False),
+    ("persist_f32_softplus", (20, 72, 1024, 1, 16, 1), "f32", 16, True),
+]
+
+
+@pytest.mark.parametrize("case", PERSIST_CASES, ids=[c[0] for c in PERSIST_CASES])
+def test_persistent_backward_parity_and_determinism(case):
+    name, shape, io, chunk, softplus = case
+    inp = _inputs(shape, io, False, softplus, seed=zlib.crc32(name.encode()) % 1000)
+    _, _, ck = gpu_fwd(inp, chunk, softplus)
+    g = gpu_bwd(inp, chunk, ckpt=ck, softplus=softplus)
+    o = oracle_bwd(inp, chunk, softplus)
+    t = tol(io, grad=True)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], t)
+    assert binding.ssm_scan_status(g["_ws"]) == 0
+    g2 = gpu_bwd(inp, chunk, ckpt=ck, softplus=softplus)
+    for k in GRADS:
+        if g.get(k) is not None:
+            assert torch.equal(g[k], g2[k]), k
+
+
 def test_misaligned_inputs_fall_back_to_general_kernels():
     inp = _inputs((2, 150, 64, 1, 16, 1), "f32", False, False, seed=11)
     # x one element past a 16-byte boundary: the TMA paths cannot take it
