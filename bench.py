@@ -73,13 +73,13 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 # kernel's sources hash to what was captured; any edit makes it null until it is captured again.
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
-        "kernel": "scan_bwd_tma_kernel<bf16>",
-        "bytes": 472008448 + 671865600,
+        "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
+        "bytes": 516003840 + 762793472,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "9697604387c734027bc4e8f5b3b91571b6f347ca15c43c0d79246f7cfef7c467",
+                "b57d9bbb2bc602d3f350f0a0a483128eaa0ec2c6a6d5df51e4336d34f86d8ff5",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
-                "86ccb87afc65ae1c37670cde906c2143e309573a654f307343a7bfc832f51a8c",
+                "54df7bbba274f39ff23189bccf24ac256aa5719c795314518a5ada5d2a05324c",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
                 "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
         },

@@ -307,6 +307,22 @@ __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
 }
 
 // ---- fixed-order reductions --------------------------------------------------------------
+// sum_{j < count} base[j * stride], added in the order of j; the loads go out eight at a time
+// so that a long sum is not one load latency per term.
+__device__ __forceinline__ float sum_strided(const float* base, long stride, int count) {
+  float v = 0.0f;
+  int j = 0;
+  for (; j + 8 <= count; j += 8) {
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) t[u] = base[(long)(j + u) * stride];
+#pragma unroll
+    for (int u = 0; u < 8; u++) v += t[u];
+  }
+  for (; j < count; j++) v += base[(long)j * stride];
+  return v;
+}
+
 __global__ void reduce_params_kernel(const BwdArgs a) {
   const ScanProblem& p = a.p;
   const int nA = p.a_per_state ? p.H * p.N : p.H;
@@ -318,26 +334,24 @@ __global__ void reduce_params_kernel(const BwdArgs a) {
       const int n_lo = p.a_per_state ? (int)(i % p.N) : 0;
       const int n_hi = p.a_per_state ? n_lo + 1 : p.N;
       float v = 0.0f;
-      for (int b = 0; b < p.ns; b++)
-        for (int s = 0; s < a.S; s++)
-          for (int pp = 0; pp < p.P; pp++)
-            for (int n = n_lo; n < n_hi; n++)
-              v += a.dA_part[(((long)b * a.S + s) * p.HP + h * p.P + pp) * p.N + n];
+      if (p.P == 1 && n_hi == n_lo + 1) {  // one term per (sequence, segment), in that order
+        v = sum_strided(a.dA_part + (long)h * p.N + n_lo, (long)p.HP * p.N, p.ns * a.S);
+      } else {
+        for (int b = 0; b < p.ns; b++)
+          for (int s = 0; s < a.S; s++)
+            for (int pp = 0; pp < p.P; pp++)
+              for (int n = n_lo; n < n_hi; n++)
+                v += a.dA_part[(((long)b * a.S + s) * p.HP + h * p.P + pp) * p.N + n];
+      }
       a.g.d_A[i] = v;
     } else if (i < nA + p.HP) {  // dD
       const int ch = (int)(i - nA);
       if (!a.g.d_D) continue;
-      float v = 0.0f;
-      for (int b = 0; b < p.ns; b++)
-        for (int s = 0; s < a.S; s++) v += a.dD_part[((long)b * a.S + s) * p.HP + ch];
-      a.g.d_D[ch] = v;
+      a.g.d_D[ch] = sum_strided(a.dD_part + ch, p.HP, p.ns * a.S);
     } else {  // d dt_bias (head_dim == 1; the head_dim > 1 case is reduce_ddt_kernel's)
       const int h = (int)(i - nA - p.HP);
       if (!a.g.d_dt_bias || p.P != 1) continue;
-      float v = 0.0f;
-      for (int b = 0; b < p.ns; b++)
-        for (int s = 0; s < a.S; s++) v += a.dtb_part[((long)b * a.S + s) * p.HP + h];
-      a.g.d_dt_bias[h] = v;
+      a.g.d_dt_bias[h] = sum_strided(a.dtb_part + h, p.HP, p.ns * a.S);
     }
   }
 }
