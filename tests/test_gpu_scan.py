@@ -123,6 +123,23 @@ def test_persistent_backward_parity_and_determinism(case):
             assert torch.equal(g[k], g2[k]), k
 
 
+def test_persistent_backward_ids_without_final_state_gradient():
+    """The persistent path seeds the last chunk with zero when no final-state gradient is given
+    and sums d_s0 over the sequences that share an initial-state row."""
+    ns, L, H = 20, 80, 1024
+    inp = _inputs((ns, L, H, 1, 16, 1), "bf16", False, False, seed=41)
+    rows = 3
+    inp["s0"] = 0.5 * torch.randn(rows, H, 1, 16)
+    ids = torch.tensor([i % rows for i in range(ns)], dtype=torch.int32)
+    _, _, ck = gpu_fwd(inp, 32, ids=ids, state_rows=rows)
+    g = gpu_bwd(inp, 32, ckpt=ck, ids=ids, state_rows=rows, d_state_out=False)
+    o = oracle_bwd(inp, 32, ids=ids, state_rows=rows, d_state_out=False)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], tol("bf16", grad=True))
+    assert binding.ssm_scan_status(g["_ws"]) == 0
+
+
 def test_misaligned_inputs_fall_back_to_general_kernels():
     inp = _inputs((2, 150, 64, 1, 16, 1), "f32", False, False, seed=11)
     # x one element past a 16-byte boundary: the TMA paths cannot take it
