@@ -474,7 +474,7 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
     const size_t units = (size_t)p.G * q.bpg * q.S * p.ns;
     const size_t slots = (size_t)num_sms * kBwdPersistBlocksPerSM;
     const size_t blocks = q.persist && slots < units ? slots : units;  // one per resident block
-    q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsub) * kScanThreads);
+    q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsubTma) * kScanThreads);
     if (q.persist) q.off_queue = take(sizeof(int) * (1 + units));  // counter, then unit flags
   }
   if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));

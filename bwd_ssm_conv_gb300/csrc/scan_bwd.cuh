@@ -9,6 +9,7 @@ namespace ssm {
 
 constexpr int kBwdNS = 4;          // states per thread
 constexpr int kTsub = 8;           // tokens of state history held in registers
+constexpr int kTsubTma = 4;        // the same for the TMA-staged Mamba-1 kernel
 constexpr int kMaxBwdChunk = 512;  // larger checkpoint intervals are re-checkpointed at 256
 constexpr int kDefaultChunk = 256;
 
@@ -94,7 +95,7 @@ struct BwdPlan {
       off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, off_queue, bytes, smem;
 };
 // Resident blocks per SM the persistent path is sized for (the kernel's launch bound).
-constexpr int kBwdPersistBlocksPerSM = 3;
+constexpr int kBwdPersistBlocksPerSM = 4;
 
 // Mamba-2-form backward (scan_bwd_heads.cu): one A per head, head_dim % 32 == 0, d_state 128.
 bool bwd_heads_applies(const ScanProblem& p, int chunk_b);

@@ -23,7 +23,7 @@
 
 namespace ssm {
 
-constexpr int kBwdStages = 3;
+constexpr int kBwdStages = 2;
 constexpr int kBwdTile = 16;                  // tokens per staged tile (two sub-chunks)
 constexpr int kCB = kScanThreads / 4;         // channels per block
 constexpr int kWarps = kScanThreads / 32;
@@ -201,13 +201,14 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   float2* sD2 = reinterpret_cast<float2*>(smem + m.off_p);       // [TT][CB] (delta, delta x)
   float* sGy = reinterpret_cast<float*>(smem + m.off_spg);       // [TT][CB] gy = dy silu(z)
   float4* sE = reinterpret_cast<float4*>(smem + m.off_e);        // [TT][CB] (x, gy, dyg, softplus')
-  float* sPB = reinterpret_cast<float*>(smem + m.off_part);      // [TT][threads] sum_n dh B
-  float* sPA = sPB + TT * kScanThreads;                           // [TT][threads] sum_n A w
-  float* sPY = sPA + TT * kScanThreads;                           // [TT][threads] sum_n C h
+  // per-channel state sums of lane pairs (4 lanes hold a channel's 16 states): [TT][threads / 2]
+  float* sPB = reinterpret_cast<float*>(smem + m.off_part);      // sum_n dh B
+  float* sPA = sPB + TT * kScanThreads / 2;                       // sum_n A w
+  float* sPY = sPA + TT * kScanThreads / 2;                       // sum_n C h
   float* red = reinterpret_cast<float*>(smem + m.off_red);       // [TT][warps][2N]
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);      // D[CB], dt_bias[CB]
   float* sAcc = reinterpret_cast<float*>(smem + m.off_acc);      // [warps][CB][2]
-  const int nsub_max = a.chunk_b / kTsub;
+  const int nsub_max = a.chunk_b / kTsubTma;
   float4* bnd = m.bnd + (PERSIST ? (long)blockIdx.x
                                  : ((long)(b * a.S + s) * gridDim.x + blockIdx.x)) *
                             nsub_max * kScanThreads;
@@ -293,7 +294,6 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 
   for (Pos cs = first(); cs.ck >= c_first; advance(cs), qpos++) {
     const int stg = qpos % kBwdStages;
-    if (cs.lvl == 1 && tid == 0) tma_store_wait_read<1>();  // out buffer (n_l2 & 1) is free
     const bool ok = mbar_wait(&full[stg], (uint32_t)(qpos / kBwdStages) & 1u);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
@@ -380,11 +380,11 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         hp[1] = f2_pack(src[2 ^ pm], src[3 ^ pm]);
       }
       auto token = [&](int i) {
-        if (i % kTsub == 0) {
+        if (i % kTsubTma == 0) {
           float h0, h1, h2, h3;
           f2_unpack(hp[0], h0, h1);
           f2_unpack(hp[1], h2, h3);
-          bnd[(cs.j * (TT / kTsub) + i / kTsub) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
+          bnd[(cs.j * (TT / kTsubTma) + i / kTsubTma) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
         }
         const float2 d2 = sD2[i * CB + cl];
         const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
@@ -407,18 +407,18 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
 
     // ---- level 2: sub-chunks last to first: recompute 8 states, then the adjoint ------------
-    // One sub-chunk; FULL (all kTsub tokens present) drops the per-token branches.
+    // One sub-chunk; FULL (all kTsubTma tokens present) drops the per-token branches.
     auto sub_chunk = [&](int k, int c8, auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;
-      const int i0 = k * kTsub;
-      f2_t hh[kTsub + 1][2], aa[kTsub][2];
+      const int i0 = k * kTsubTma;
+      f2_t hh[kTsubTma + 1][2], aa[kTsubTma][2];
       {
-        const float4 v = bnd[(cs.j * (TT / kTsub) + k) * kScanThreads + tid];
+        const float4 v = bnd[(cs.j * (TT / kTsubTma) + k) * kScanThreads + tid];
         hh[0][0] = f2_pack(v.x, v.y);
         hh[0][1] = f2_pack(v.z, v.w);
       }
 #pragma unroll
-      for (int r = 0; r < kTsub; r++) {
+      for (int r = 0; r < kTsubTma; r++) {
         if (FULL || r < c8) {
           const float2 d2 = sD2[(i0 + r) * CB + cl];
           const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
@@ -435,7 +435,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         }
       }
 #pragma unroll
-      for (int r = kTsub - 1; r >= 0; r--) {
+      for (int r = kTsubTma - 1; r >= 0; r--) {
         if (FULL || r < c8) {  // uniform over the block
           const int i = i0 + r;
           const float2 d2 = sD2[i * CB + cl];
@@ -458,9 +458,19 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
             yp2 = f2_fma(C2[q], hh[r + 1][q], yp2);
             carry2[q] = cn2;
           }
-          sPB[i * kScanThreads + tid] = f2_sum(sB2);
-          sPA[i * kScanThreads + tid] = f2_sum(sAw2);
-          sPY[i * kScanThreads + tid] = f2_sum(yp2);
+          {  // sum the lane pair (states n0 .. n0+3 and the neighbour's 4), one store per sum
+            float vb = f2_sum(sB2), va = f2_sum(sAw2), vy = f2_sum(yp2);
+            vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+            va += __shfl_xor_sync(0xffffffffu, va, 1);
+            vy += __shfl_xor_sync(0xffffffffu, vy, 1);
+            const int q = i * (kScanThreads / 2) + (tid >> 1);
+            if (tid & 1) {
+              sPY[q] = vy;
+            } else {
+              sPB[q] = vb;
+              sPA[q] = va;
+            }
+          }
           float tb, tc;
           f2_unpack(reduce_bc_warp(dB2[0], dB2[1], dC2[0], dC2[1]), tb, tc);
           const int hi = (lane >> 2) & 1;  // of the lane pair: 0 writes dB, 1 writes dC
@@ -468,28 +478,29 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         }
       }
     };
-    const int nsub = (cnt + kTsub - 1) / kTsub;
+    const int nsub = (cnt + kTsubTma - 1) / kTsubTma;
     for (int k = nsub - 1; k >= 0; k--) {
-      const int c8 = min(kTsub, cnt - k * kTsub);
-      if (c8 == kTsub) sub_chunk(k, c8, std::true_type{});
+      const int c8 = min(kTsubTma, cnt - k * kTsubTma);
+      if (c8 == kTsubTma) sub_chunk(k, c8, std::true_type{});
       else sub_chunk(k, c8, std::false_type{});
     }
-    __syncthreads();  // sPart and red complete
+    if (tid == 0) tma_store_wait_read<0>();  // the previous tile's stores have read `out`
+    __syncthreads();  // sPart and red complete; `out` free
 
     // ---- epilogue, once per (token, channel): dx, dz, ddt; dD and d dt_bias partials --------
-    IO* out = reinterpret_cast<IO*>(smem + m.off_out + (n_l2 & 1) * m.out_stride);
+    IO* out = reinterpret_cast<IO*>(smem + m.off_out);
     IO* odx = out;
     IO* odz = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + m.out_tile);
     IO* oddt = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + 2 * m.out_tile);
     for (int idx = tid; idx < cnt * CB; idx += kScanThreads) {
       const int i = idx / CB, c = idx - i * CB;  // c == tid % CB for every item of this thread
-      const int pi = i * kScanThreads + c * 4;  // the 4 threads of channel c, 16 bytes per lane
-      const float4 vb = *reinterpret_cast<const float4*>(sPB + pi);
-      const float4 va = *reinterpret_cast<const float4*>(sPA + pi);
-      const float4 vy = *reinterpret_cast<const float4*>(sPY + pi);
-      const float sBt = (vb.x + vb.y) + (vb.z + vb.w);
-      const float sAwt = (va.x + va.y) + (va.z + va.w);
-      const float ypt = (vy.x + vy.y) + (vy.z + vy.w);
+      const int pi = i * (kScanThreads / 2) + c * 2;  // the 2 lane pairs of channel c
+      const float2 vb = *reinterpret_cast<const float2*>(sPB + pi);
+      const float2 va = *reinterpret_cast<const float2*>(sPA + pi);
+      const float2 vy = *reinterpret_cast<const float2*>(sPY + pi);
+      const float sBt = vb.x + vb.y;
+      const float sAwt = va.x + va.y;
+      const float ypt = vy.x + vy.y;
       const float4 e4 = sE[idx];                  // (x, gy, dyg, softplus')
       const float dl = sD2[idx].x;
       const float D = sPar[c];
@@ -691,11 +702,11 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   // the local kernel's fp32 C rows
   m->off_bf = take(io == 2 ? 4 * TT * p.N * 4 : 4 * TT * p.N * 4);
   m->off_cf = take(io == 2 ? TT * p.N * 4 : 4 * TT * p.N * 4);
-  m->off_part = take(3 * TT * kScanThreads * 4);
+  m->off_part = take(3 * TT * (kScanThreads / 2) * 4);
   m->off_red = take(TT * kWarps * 2 * p.N * 4);
   m->out_tile = al(tile);
   m->out_stride = 3 * m->out_tile;
-  m->off_out = take(2 * m->out_stride);
+  m->off_out = take(m->out_stride);
   m->off_par = take(2 * cb * 4);
   m->off_acc = take(kWarps * cb * 2 * 4);
   m->off_bar = take(64);
