@@ -311,6 +311,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     const int t0c = cs.ck * a.chunk_b, t1c = min(p.L, t0c + a.chunk_b);
     const int t0 = t0c + cs.j * TT;
     const int cnt = min(TT, t1c - t0);
+    // level 2: the start state of the tile's last sub-chunk, loaded before the prepass so that
+    // its latency overlaps it (scratch written by level 1 may have left L2)
+    const int nsub = (cnt + kTsubTma - 1) / kTsubTma;
+    const float4* bnd_tile = bnd + cs.j * (TT / kTsubTma) * kScanThreads + tid;
+    float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (cs.lvl == 1) nxt = bnd_tile[(nsub - 1) * kScanThreads];
 
     // ---- prepass, once per (token, channel) -----------------------------------------------
     for (int idx = tid; idx < TT * CB; idx += kScanThreads) {
@@ -408,15 +414,13 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 
     // ---- level 2: sub-chunks last to first: recompute 8 states, then the adjoint ------------
     // One sub-chunk; FULL (all kTsubTma tokens present) drops the per-token branches.
-    auto sub_chunk = [&](int k, int c8, auto full_tag) {
+    // v: the sub-chunk's start state (loaded one sub-chunk ahead by the caller)
+    auto sub_chunk = [&](int k, int c8, float4 v, auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;
       const int i0 = k * kTsubTma;
       f2_t hh[kTsubTma + 1][2], aa[kTsubTma][2];
-      {
-        const float4 v = bnd[(cs.j * (TT / kTsubTma) + k) * kScanThreads + tid];
-        hh[0][0] = f2_pack(v.x, v.y);
-        hh[0][1] = f2_pack(v.z, v.w);
-      }
+      hh[0][0] = f2_pack(v.x, v.y);
+      hh[0][1] = f2_pack(v.z, v.w);
 #pragma unroll
       for (int r = 0; r < kTsubTma; r++) {
         if (FULL || r < c8) {
@@ -478,11 +482,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         }
       }
     };
-    const int nsub = (cnt + kTsubTma - 1) / kTsubTma;
     for (int k = nsub - 1; k >= 0; k--) {
+      const float4 cur = nxt;
+      if (k > 0) nxt = bnd_tile[(k - 1) * kScanThreads];  // hide the scratch latency
       const int c8 = min(kTsubTma, cnt - k * kTsubTma);
-      if (c8 == kTsubTma) sub_chunk(k, c8, std::true_type{});
-      else sub_chunk(k, c8, std::false_type{});
+      if (c8 == kTsubTma) sub_chunk(k, c8, cur, std::true_type{});
+      else sub_chunk(k, c8, cur, std::false_type{});
     }
     if (tid == 0) tma_store_wait_read<0>();  // the previous tile's stores have read `out`
     __syncthreads();  // sPart and red complete; `out` free
