@@ -74,12 +74,12 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 516003840 + 762793472,
+        "bytes": 965108224 + 1296313088,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "b57d9bbb2bc602d3f350f0a0a483128eaa0ec2c6a6d5df51e4336d34f86d8ff5",
+                "11b82b77ee8072be04d4a20ad638a78a8ab1d5603d37fd240f10b8d8b6bbca4c",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
-                "54df7bbba274f39ff23189bccf24ac256aa5719c795314518a5ada5d2a05324c",
+                "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
                 "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
         },
