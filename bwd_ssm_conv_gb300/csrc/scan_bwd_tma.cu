@@ -497,7 +497,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     IO* odx = out;
     IO* odz = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + m.out_tile);
     IO* oddt = reinterpret_cast<IO*>(reinterpret_cast<unsigned char*>(out) + 2 * m.out_tile);
-    for (int idx = tid; idx < cnt * CB; idx += kScanThreads) {
+    auto epi = [&](int idx) {
       const int i = idx / CB, c = idx - i * CB;  // c == tid % CB for every item of this thread
       const int pi = i * (kScanThreads / 2) + c * 2;  // the 2 lane pairs of channel c
       const float2 vb = *reinterpret_cast<const float2*>(sPB + pi);
@@ -516,14 +516,24 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       sts_f(oddt + idx, ddt);
       dD_acc = fmaf(e4.y, e4.x, dD_acc);
       dtb_acc += ddt;
-    }
-    for (int idx = tid; idx < cnt * 2 * N; idx += kScanThreads) {
+    };
+    // dB and dC of the tile's tokens: this block's sum over its warps, one partial per block
+    auto red_item = [&](int idx) {
       const int i = idx / (2 * N), r = idx - i * 2 * N;
       float v = 0.0f;
 #pragma unroll
       for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
       const long tok = (long)b * p.L + t0 + i;
       a.part_bc[((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r] = v;
+    };
+    if (cnt == TT) {  // full tile: a compile-time item count, so the items interleave
+#pragma unroll
+      for (int u = 0; u < TT * CB / kScanThreads; u++) epi(tid + u * kScanThreads);
+#pragma unroll
+      for (int u = 0; u < TT * 2 * N / kScanThreads; u++) red_item(tid + u * kScanThreads);
+    } else {
+      for (int idx = tid; idx < cnt * CB; idx += kScanThreads) epi(idx);
+      for (int idx = tid; idx < cnt * 2 * N; idx += kScanThreads) red_item(idx);
     }
     fence_async_shared();
     __syncthreads();  // out tiles complete; stage fully read
