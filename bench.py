@@ -164,6 +164,20 @@ class ClockSampler:
 
 
 # ---- the step ----------------------------------------------------------------------------
+def packed(specs, dev):
+    """One flat device byte buffer holding tensors of the given (shape, dtype) specs at 256-byte
+    aligned offsets; returns (buffer, views).  A step's inputs and its results each live in one
+    such buffer, so that the end-to-end leg moves them with one copy per direction."""
+    offs, off = [], 0
+    for shape, dt in specs:
+        nbytes = torch.Size(shape).numel() * torch.empty(0, dtype=dt).element_size()
+        offs.append((off, nbytes))
+        off = (off + nbytes + 255) // 256 * 256
+    buf = torch.empty(max(off, 1), dtype=torch.uint8, device=dev)
+    views = [buf[o:o + n].view(dt).view(shape) for (o, n), (shape, dt) in zip(offs, specs)]
+    return buf, views
+
+
 class Step:
     """Device buffers for one step of the hot path and the calls that run it."""
 
@@ -172,7 +186,15 @@ class Step:
         self.B = B
         self.w = w
         self.dev = dev
-        d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+        self.in_keys = [k for k in (["sx", "c"] if w.d_conv else ["x"]) +
+                        ["dt", "A", "B", "C", "D", "z", "s0", "dy", "d_state_out"]
+                        if inp.get(k) is not None]
+        self.in_buf, views = packed([(inp[k].shape, inp[k].dtype) for k in self.in_keys], dev)
+        d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()
+             if k not in self.in_keys}
+        for k, v in zip(self.in_keys, views):
+            v.copy_(inp[k])
+            d[k] = v
         self.d = d
         ns, L, H, P, N = w.n_seqs, w.n_tok, w.n_head, w.head_dim, w.d_state
         io = w.torch_io
@@ -180,8 +202,23 @@ class Step:
         self.x = (torch.empty(ns, L, H * P, dtype=io, device=dev) if w.d_conv
                   else d["x"].view(ns, L, H * P))
         self.x4 = self.x.view(ns, L, H, P)
-        self.y = torch.empty(ns, L, H, P, dtype=io, device=dev)
-        self.st = torch.empty(ns, H, P, N, dtype=f32, device=dev)
+        # the step's results, in the order outputs() lists them, in one buffer
+        ospec = [("y", (ns, L, H, P), io), ("st", (ns, H, P, N), f32)]
+        if not w.fwd_only:
+            ospec += [("d_sx", tuple(d["sx"].shape), io) if w.d_conv else ("d_x", (ns, L, H, P), io),
+                      ("d_dt", tuple(d["dt"].shape), d["dt"].dtype),
+                      ("d_A", tuple(d["A"].shape), f32), ("d_B", tuple(d["B"].shape), io),
+                      ("d_C", tuple(d["C"].shape), io)]
+            if d["D"] is not None:
+                ospec.append(("d_D", tuple(d["D"].shape), f32))
+            if d["z"] is not None:
+                ospec.append(("d_z", (ns, L, H, P), io))
+            if w.d_conv:
+                ospec.append(("d_c", tuple(d["c"].shape), f32))
+        self.out_buf, oviews = packed([(sh, dt) for _, sh, dt in ospec], dev)
+        o = dict(zip([k for k, _, _ in ospec], oviews))
+        self.y = o["y"]
+        self.st = o["st"]
         nch = (L + w.chunk - 1) // w.chunk
         self.ck = torch.empty(ns, nch, H, P, N, dtype=f32, device=dev)
         shape = B.scan_shape(self.x4, d["dt"], d["A"], d["B"], d["s0"], w.chunk)
@@ -189,18 +226,16 @@ class Step:
                                 device=dev)
         self.ws_b = torch.empty(B.ssm_scan_workspace_size(shape, True), dtype=torch.uint8,
                                 device=dev)
-        self.g = dict(d_s0=torch.empty(ns, H, P, N, dtype=f32, device=dev),
-                      d_x=torch.empty_like(self.x4), d_dt=torch.empty_like(d["dt"]),
-                      d_A=torch.empty_like(d["A"]), d_B=torch.empty_like(d["B"]),
-                      d_C=torch.empty_like(d["C"]),
-                      d_D=torch.empty_like(d["D"]) if d["D"] is not None else None,
-                      d_z=torch.empty_like(d["z"]) if d["z"] is not None else None,
-                      d_dt_bias=None)
-        if w.d_conv:
+        if not w.fwd_only:
+            self.g = dict(d_s0=torch.empty(ns, H, P, N, dtype=f32, device=dev),
+                          d_x=o["d_x"] if "d_x" in o else torch.empty_like(self.x4),
+                          d_dt=o["d_dt"], d_A=o["d_A"], d_B=o["d_B"], d_C=o["d_C"],
+                          d_D=o.get("d_D"), d_z=o.get("d_z"), d_dt_bias=None)
+        if w.d_conv and not w.fwd_only:
             self.ws_c = torch.empty(B.ssm_conv_workspace_size(ns, H * P, L, w.d_conv),
                                     dtype=torch.uint8, device=dev)
-            self.d_sx = torch.empty_like(d["sx"])
-            self.d_c = torch.empty_like(d["c"])
+            self.d_sx = o["d_sx"]
+            self.d_c = o["d_c"]
 
     def stages(self):
         B, w, d = self.B, self.w, self.d
@@ -236,10 +271,7 @@ class Step:
         return res
 
     def inputs(self):
-        d = self.d
-        keys = ["sx", "c"] if self.w.d_conv else ["x"]
-        keys += ["dt", "A", "B", "C", "D", "z", "s0", "dy", "d_state_out"]
-        return [d[k] for k in keys if d.get(k) is not None]
+        return [self.d[k] for k in self.in_keys]
 
 
 def reduce_max(value: float, dist=None, device=None) -> float:
@@ -290,20 +322,17 @@ def time_device(step, steps, warmup, flush):
 
 def time_e2e_serial(step, steps, warmup):
     """Same step through the public API with host buffers, one stream: every step copies its
-    inputs from pinned host memory, runs, and reads its results back before the next starts."""
-    host_in = [t.detach().cpu().pin_memory() for t in step.inputs()]
-    dev_in = step.inputs()
-    outs = step.outputs()
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    inputs from pinned host memory, runs, and reads its results back before the next starts.
+    Inputs and results each travel as one packed buffer (Step.in_buf / Step.out_buf)."""
+    host_in = step.in_buf.cpu().pin_memory()
+    host_out = torch.empty(step.out_buf.shape, dtype=torch.uint8, pin_memory=True)
     stages = step.stages()
 
     def one():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
+        step.in_buf.copy_(host_in, non_blocking=True)
         for _, fn in stages:
             fn()
-        for d, h in zip(outs, host_out):
-            h.copy_(d, non_blocking=True)
+        host_out.copy_(step.out_buf, non_blocking=True)
 
     for _ in range(warmup):
         one()
@@ -320,18 +349,16 @@ def time_e2e_serial(step, steps, warmup):
 
 def time_e2e(pair, steps, warmup):
     """Same step through the public API with host buffers: every step copies all its inputs
-    from pinned host memory and reads all its results back.  Two device buffer sets (`pair`)
+    from pinned host memory and reads all its results back, each as one packed buffer (one
+    copy per direction, so no per-tensor copy overhead).  Two device buffer sets (`pair`)
     and three streams let step i's kernels overlap the input copies of step i+1 and the result
     copies of step i-1; events keep each buffer set's copies and kernels in order.  Returns
     (ms per step from the first input copy to the last result copy, bytes in, bytes out)."""
-    host_in = [t.detach().cpu().pin_memory() for t in pair[0].inputs()]
-    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outputs()]
-                for st in pair]
-    dev_in = [st.inputs() for st in pair]
-    dev_out = [st.outputs() for st in pair]
+    host_in = pair[0].in_buf.cpu().pin_memory()
+    host_out = [torch.empty(st.out_buf.shape, dtype=torch.uint8, pin_memory=True) for st in pair]
     stages = [st.stages() for st in pair]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    h2d = host_in.numel()
+    d2h = host_out[0].numel()
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     run_done, out_done = [None, None], [None, None]
 
@@ -340,8 +367,7 @@ def time_e2e(pair, steps, warmup):
         with torch.cuda.stream(s_in):
             if run_done[k] is not None:  # step i-2's kernels are done with this input set
                 s_in.wait_event(run_done[k])
-            for h, d in zip(host_in, dev_in[k]):
-                d.copy_(h, non_blocking=True)
+            pair[k].in_buf.copy_(host_in, non_blocking=True)
             in_done = torch.cuda.Event()
             in_done.record(s_in)
         with torch.cuda.stream(s_run):
@@ -354,8 +380,7 @@ def time_e2e(pair, steps, warmup):
             run_done[k].record(s_run)
         with torch.cuda.stream(s_out):
             s_out.wait_event(run_done[k])
-            for d, h in zip(dev_out[k], host_out[k]):
-                h.copy_(d, non_blocking=True)
+            host_out[k].copy_(pair[k].out_buf, non_blocking=True)
             out_done[k] = torch.cuda.Event()
             out_done[k].record(s_out)
 
@@ -554,7 +579,7 @@ def main():
         "clocks": clocks,
         "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "pipelined": "2 buffer sets, copies of steps i+1 / i-1 overlap step i",
+                "pipelined": "2 buffer sets, copies of steps i+1 / i-1 overlap step i; inputs and results each one packed copy",
                 "serial_ms_per_step": serial_ms},
     }
     if not args.no_cpu_baseline and world == 1:
