@@ -74,10 +74,10 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 965108224 + 1296313088,
+        "bytes": 967491584 + 1296482560,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "11b82b77ee8072be04d4a20ad638a78a8ab1d5603d37fd240f10b8d8b6bbca4c",
+                "89faa04c31cfabf0f93da99a036065a6ca120e3418738cca8941cec137914898",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
