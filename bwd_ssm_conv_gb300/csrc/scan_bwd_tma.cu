@@ -3,19 +3,21 @@
 //
 // Same arithmetic and workspace outputs as the general kernels in scan_bwd.cu.  A block =
 // 128 threads = 32 channels x 16 states (4 threads of 4 states per channel), one sequence,
-// one time segment.  Inputs arrive as [16 tokens][32 channels] tiles (x, dt, z, dy) and
-// [16 tokens][16] tiles (B, C) through a 3-stage ring filled by cp.async.bulk.tensor; dx,
-// dz, ddt leave as TMA-stored tiles.  Per tile, work that depends only on (token, channel)
-// -- delta, the gate, dy silu'(z), softplus' -- is done once by the whole block in a
-// prepass, so the per-state loops carry only the recurrence (packed f32x2 arithmetic);
-// the per-channel sums over states go through shared memory to an epilogue that writes
-// dx, dz and ddt, and the dB/dC sums over channels use a warp butterfly whose exchanges need no
-// lane-dependent selects (each thread's states sit in registers in a lane-permuted order).
+// one (chain, chunk) unit at a time when persistent, else one time segment.  Inputs arrive as
+// [16 tokens][32 channels] tiles (x, dt, z, dy) and [16 tokens][16] tiles (B, C) through a
+// 2-stage ring filled by cp.async.bulk.tensor; dx, dz, ddt leave as TMA-stored tiles.  Per
+// tile, work that depends only on (token, channel) -- delta, the gate, dy silu'(z),
+// softplus' -- is done once by the whole block in a prepass, so the per-state loops carry only
+// the recurrence (packed f32x2 arithmetic); the per-channel sums over states are added across
+// lane pairs and go through shared memory to an epilogue that writes dx, dz and ddt, and the
+// dB/dC sums over channels use a warp butterfly whose exchanges need no lane-dependent selects
+// (each thread's states sit in registers in a lane-permuted order).  Four blocks fit an SM
+// (about 120 registers, 55 KB of shared memory).
 //
 // Per chunk (last to first): level 1 walks the chunk's tiles forward from the checkpoint,
-// saving the state at every 8-token sub-chunk start (global scratch, re-read from L2);
-// level 2 walks the tiles in reverse, recomputes each sub-chunk's 8 states and decays in
-// registers and runs the adjoint over them.
+// saving the state at every 4-token sub-chunk start (global scratch); level 2 walks the tiles
+// in reverse, recomputes each sub-chunk's 4 states and decays in registers and runs the
+// adjoint over them, loading the next sub-chunk's start state one sub-chunk ahead.
 #include <type_traits>
 
 #include "scan_bwd.cuh"
