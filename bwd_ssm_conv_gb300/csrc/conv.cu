@@ -383,18 +383,22 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
     if (dd < D) part[(((long)b * nt + blockIdx.y) * D + dd) * (K + 1) + k] = v;
   }
   __syncthreads();
-  // d_sx rows: columns [i0, min(i0 + TT, W)), 16-byte aligned groups + scalar edges; lane =
-  // row, warp = group, as in rows_to_smem
+  // d_sx rows: columns [i0, min(i0 + TT, W)), 16-byte aligned groups + scalar edges.  8 lanes
+  // share a row (4 rows per warp, 8 warps: all 32 rows in one pass), so every warp store
+  // writes 4 runs of 128 contiguous bytes (measured faster than one row per lane, whose 32
+  // scattered 16-byte pieces per store cost more than the 2-way shared-memory conflicts here).
   constexpr int V = 16 / sizeof(IO);
   constexpr int NG = (kSegTT + V - 1) / V + 1;
+  constexpr int LPR = 8;
   const int n = (int)min((long)kSegTT, W - i0);
-  const int dd = d0 + lane;
+  const int r = wid * (32 / LPR) + lane / LPR;  // this lane's row of the tile
+  const int dd = d0 + r;
   IO* row = d_sx + ((long)b * D + dd) * W + i0;
   const int ph = (int)(((uintptr_t)row & 15) / sizeof(IO));
-  for (int gi = wid; gi < NG && dd < D; gi += kSegWarps) {
+  for (int gi = lane % LPR; gi < NG && dd < D; gi += LPR) {
     const int j0 = gi * V - ph;
     if (j0 >= n) break;
-    const float* src = s + lane * SO + j0;
+    const float* src = s + r * SO + j0;
     if (j0 >= 0 && j0 + V <= n) {
       float v[V];
 #pragma unroll
