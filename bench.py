@@ -77,7 +77,7 @@ TRAFFIC_CAPTURES = {
         "bytes": 967491584 + 1296482560,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "89faa04c31cfabf0f93da99a036065a6ca120e3418738cca8941cec137914898",
+                "43ff157b3b14b0a955d3ae9c4a20195b4a14df89edf120a418da4951d6f338ba",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
