@@ -68,3 +68,39 @@ def test_conv_full_config(i):
     r_sx, r_c, _ = oracle.conv_bwd(inp["sx"], inp["c"], dout, silu=True)
     assert_close("d_sx", d_sx, r_sx, tol(w.io, True))
     assert_close("d_c", d_c, r_c, tol(w.io, True))
+
+
+def _at(t, off):
+    """A CUDA copy of t that starts `off` elements into its buffer."""
+    flat = torch.empty(t.numel() + off, dtype=t.dtype, device="cuda")
+    v = flat[off:].view(t.shape)
+    v.copy_(t.cuda())
+    return v
+
+
+# (io, sx offset, d_sx offset, dout offset) in elements.  sx and d_sx rows in different 16-byte
+# phases take the general kernel; the same non-zero phase takes the row kernel with shifted
+# row starts; an unaligned dout is staged element by element.
+OFFSET_CASES = [
+    ("bf16", 1, 0, 0),
+    ("bf16", 3, 3, 1),
+    ("f32", 2, 2, 0),
+    ("f32", 0, 1, 3),
+]
+
+
+@pytest.mark.parametrize("case", OFFSET_CASES)
+def test_conv_bwd_offset_views(case):
+    io, o_sx, o_dsx, o_dout = case
+    n_s, d, L, K = 2, 40, 300, 4
+    inp = random_conv_inputs(n_s, d, L, K, io=io, bias=True, seed=17 + o_sx + o_dsx)
+    sx, dout = _at(inp["sx"], o_sx), _at(inp["dout"], o_dout)
+    d_sx = _at(torch.zeros_like(inp["sx"]), o_dsx)
+    d_c = torch.empty_like(inp["c"]).cuda()
+    d_b = torch.empty(d, dtype=torch.float32, device="cuda")
+    binding.ssm_conv_bwd(sx, inp["c"].cuda(), dout, inp["bias"].cuda(), silu=True,
+                         out=(d_sx, d_c, d_b))
+    r_sx, r_c, r_b = oracle.conv_bwd(inp["sx"], inp["c"], inp["dout"], bias=inp["bias"], silu=True)
+    assert_close("d_sx", d_sx, r_sx, tol(io, True))
+    assert_close("d_c", d_c, r_c, tol(io, True))
+    assert_close("d_bias", d_b, r_b, tol(io, True))
