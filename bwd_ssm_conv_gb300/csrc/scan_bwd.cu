@@ -444,8 +444,14 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   // launches they quantise into waves (e.g. 768 chains on 456 resident blocks = 1.68 waves).
   // The TMA path then runs persistent blocks over (chain, chunk) units instead: every chunk
   // is a segment, and no local adjoint pass is needed because each unit waits for the start
-  // adjoint of the chunk after it, which a unit taken earlier from the queue produces.
-  q.persist = q.tma_tt && S == 1 && q.nch_b >= 2;
+  // adjoint of the chunk after it, which a unit taken earlier from the queue produces.  A
+  // chain's units run one after another, so min(chains, resident blocks) blocks work at a
+  // time; time segments keep every block busy but add a local adjoint pass, about 1.37x the
+  // work (measured: 2 segments on 16 x 2048 x 1536 bf16).  So the persistent mode is also taken
+  // when the chains fill at least 3/4 of the resident blocks, though not 512 threads per SM.
+  const long chains = (long)p.ns * p.G * q.bpg;
+  const long resident = (long)num_sms * kBwdPersistBlocksPerSM;
+  q.persist = q.tma_tt && q.nch_b >= 2 && (S == 1 || 4 * chains >= 3 * resident);
   if (q.persist) S = q.nch_b;
   q.seg_chunks = (int)((q.nch_b + S - 1) / S);
   q.S = (q.nch_b + q.seg_chunks - 1) / q.seg_chunks;

@@ -99,9 +99,12 @@ def test_scan_backward_parity(case):
 # Enough (sequence, 32-channel block) chains to fill a 152-SM GPU without time segments (20 x 32
 # = 640): the backward then runs resident blocks over (chain, chunk) units, last chunk first,
 # each handing its chunk's start adjoint to the unit of the chunk before it.  Ragged last chunk.
+# 15 x 32 = 480 chains fill 3/4 of the 608 resident blocks but not 512 threads per SM: also
+# persistent, with some blocks waiting on the flag of a chunk still in progress.
 PERSIST_CASES = [
     ("persist_bf16", (20, 100, 1024, 1, 16, 1), "bf16", 32, False),
     ("persist_f32_softplus", (20, 72, 1024, 1, 16, 1), "f32", 16, True),
+    ("persist_partial_bf16", (15, 100, 1024, 1, 16, 1), "bf16", 32, False),
 ]
 
 
