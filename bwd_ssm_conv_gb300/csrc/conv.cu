@@ -10,6 +10,8 @@
 //   d_sx[i]    = sum_k gp[i-k] c[k]                 (0 <= i-k < L)
 //   d_c[d][k]  = sum_{b,t} gp[b][t][d] sx[b][d][t+k],   d_bias[d] = sum_{b,t} gp
 // d_c / d_bias are summed per tile into the workspace and reduced in a fixed order.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -152,22 +154,21 @@ conv_bwd_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
 }
 
 
-// ---- d_conv <= 4: one thread streams 32 tokens of one channel --------------------------
+// ---- d_conv <= 4, backward: one thread streams 32 tokens of one channel ----------------
 // A tile = 32 channels (one per lane) x 256 tokens (8 warps x 32).  Each thread walks its 32
-// tokens in order with the taps, the last d_conv inputs and (backward) the last d_conv input
-// gradients in registers, so every tap sum, SiLU (') and d_c term is computed once from
-// registers.  Lanes run along channels, so the channel-fastest out / dout rows are read and
-// written coalesced straight from global memory; the time-fastest sx (and d_sx) rows go
-// through shared memory, moved with aligned 16-byte accesses (row starts have any alignment:
-// a row holds L + d_conv - 1 elements) and scalar ones only at partial groups.
+// tokens in order with the taps, the last d_conv inputs and the last d_conv input gradients in
+// registers, so every tap sum, SiLU' and d_c term is computed once from registers.  Lanes run
+// along channels, so the channel-fastest dout rows are read coalesced straight from global
+// memory; the time-fastest sx and d_sx rows go through shared memory, moved with aligned
+// 16-byte accesses (row starts have any alignment: a row holds L + d_conv - 1 elements) and
+// scalar ones only at partial groups.
 constexpr int kSeg = 32;                       // tokens per thread
 constexpr int kSegWarps = 8;
 constexpr int kSegThreads = 32 * kSegWarps;
 constexpr int kSegTT = kSeg * kSegWarps;       // tokens per tile
 constexpr int kSegRows = 32;                   // channels per tile
 // Lanes per row when moving sx rows into shared memory (see rows_to_smem); measured best on
-// GB300 for each kernel.
-constexpr int kFwdLanesPerRow = 8;
+// GB300.
 constexpr int kBwdLanesPerRow = 1;
 
 template <typename IO>
@@ -245,50 +246,132 @@ __device__ __forceinline__ void rows_to_smem(const IO* base, int d0, int D, long
   }
 }
 
+// ---- d_conv <= 4, forward: one lane streams 16 tokens of two adjacent channels -----------
+// A tile = 64 channels (a pair per lane) x 128 tokens (8 warps x 16).  The pair's arithmetic
+// runs in packed fp32 pairs (fma/mul/add.rn.f32x2; each half rounds as the scalar sequence
+// would) and leaves as one 4-byte (bf16) or 8-byte (fp32) store per token, so a warp store
+// writes 128 or 256 contiguous bytes.  The time-fastest sx rows go through shared memory as
+// interleaved fp32 pairs (row 2p in .x, row 2p+1 in .y), one 8-byte read per token and lane;
+// the odd pair stride keeps each half-warp's reads on distinct banks.  Rows are moved one per
+// lane with aligned 16-byte loads (scalar ones only at partial groups).
+constexpr int kPairSeg = 16;                      // tokens per thread
+constexpr int kPairTT = kPairSeg * kSegWarps;     // tokens per tile
+constexpr int kPairRows = 64;                     // channels per tile
+
 template <typename IO, int K, bool SILU>
 __global__ void __launch_bounds__(kSegThreads)
-conv_fwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
-                    const float* __restrict__ bias, IO* __restrict__ out, int D, int L) {
-  constexpr int NC = kSegTT + K - 1, SP = NC | 1;  // odd stride: lanes read distinct banks
-  __shared__ float s[kSegRows * SP];
-  const int d0 = blockIdx.x * kSegRows, i0 = blockIdx.y * kSegTT, b = blockIdx.z;
-  const long W = (long)L + K - 1;
+conv_fwd_pair_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
+                     const float* __restrict__ bias, IO* __restrict__ out, int D, int L,
+                     int ovec) {
+  constexpr int NC = kPairTT + K - 1;             // staged columns i0 .. i0+NC-1
+  constexpr int SP = NC | 1;                      // pair stride (float2), odd
+  constexpr int V = 16 / sizeof(IO);
+  constexpr int NG = (NC + V - 1) / V + 1;        // groups covering NC columns at any alignment
+  __shared__ float2 s2[kPairRows / 2 * SP];
+  float* sf = reinterpret_cast<float*>(s2);
+  const int d0 = blockIdx.x * kPairRows, i0 = blockIdx.y * kPairTT, b = blockIdx.z;
+  const int W = L + K - 1;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  rows_to_smem<IO, NC, SP, kFwdLanesPerRow>(sx + (long)b * D * W, d0, D, i0, W, s, wid, lane);
+  // every load a thread makes is issued before the first shared store: slot (rp, k) = row
+  // lane + 32 rp, group wid + 8 k
+  constexpr int KG = (NG + kSegWarps - 1) / kSegWarps;
+  uint4 raw[kPairRows / 32][KG];
+  int ph[kPairRows / 32];
+#pragma unroll
+  for (int rp = 0; rp < kPairRows / 32; rp++) {
+    const int d = d0 + lane + 32 * rp;
+    const IO* row = sx + ((long)b * D + (d < D ? d : 0)) * W;
+    ph[rp] = (int)(((uintptr_t)(row + i0) & 15) / sizeof(IO));
+#pragma unroll
+    for (int k = 0; k < KG; k++) {
+      const int gi = wid + kSegWarps * k;
+      const int cs = i0 - ph[rp] + gi * V;        // column of the group's first element
+      raw[rp][k] = make_uint4(0u, 0u, 0u, 0u);
+      if (d >= D || gi >= NG || cs - i0 >= NC) continue;
+      if (cs >= 0 && cs + V <= W) {
+        raw[rp][k] = __ldg(reinterpret_cast<const uint4*>(row + cs));
+      } else {  // a partial group: its elements inside [0, W), the rest zero
+        using B = typename std::conditional<sizeof(IO) == 2, unsigned short, unsigned>::type;
+        const B* bits = reinterpret_cast<const B*>(row);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < V; e++) {
+          if (cs + e < 0 || cs + e >= W) continue;
+          const uint32_t v = __ldg(bits + cs + e);
+          if constexpr (sizeof(IO) == 2) w[e / 2] |= v << (16 * (e % 2));
+          else w[e] = v;
+        }
+        raw[rp][k] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int rp = 0; rp < kPairRows / 32; rp++) {
+    const int r = lane + 32 * rp;
+    if (d0 + r >= D) continue;
+    float* dst = sf + (r >> 1) * 2 * SP + (r & 1);  // column i0 + j at dst[2 j]
+#pragma unroll
+    for (int k = 0; k < KG; k++) {
+      const int gi = wid + kSegWarps * k;
+      const int j0 = gi * V - ph[rp];
+      if (gi >= NG || j0 >= NC) continue;
+      float v[V];
+      unpack16<IO>(raw[rp][k], v);
+#pragma unroll
+      for (int e = 0; e < V; e++)
+        if (j0 + e >= 0 && j0 + e < NC) dst[2 * (j0 + e)] = v[e];
+    }
+  }
   __syncthreads();
-  const int d = d0 + lane, s0 = i0 + wid * kSeg;
+  const int d = d0 + 2 * lane, s0 = i0 + wid * kPairSeg;
   if (d >= D || s0 >= L) return;
-  float w[K];
+  const bool has1 = d + 1 < D;
+  f2_t w2[K];
 #pragma unroll
-  for (int k = 0; k < K; k++) w[k] = __ldg(c + (long)d * K + k);
-  const float bv = bias ? __ldg(bias + d) : 0.0f;
-  const float* xr = s + lane * SP + wid * kSeg;  // column s0 + u + k at xr[u + k]
+  for (int k = 0; k < K; k++)
+    w2[k] = f2_pack(__ldg(c + (long)d * K + k), has1 ? __ldg(c + (long)(d + 1) * K + k) : 0.0f);
+  const f2_t b2 = bias ? f2_pack(__ldg(bias + d), has1 ? __ldg(bias + d + 1) : 0.0f) : 0ull;
+  const float2* xr = s2 + lane * SP + wid * kPairSeg;  // column s0 + u + k at xr[u + k]
   IO* o = out + ((long)b * L + s0) * D + d;
-  float xw[K];
+  const bool pair = ovec && has1;
+  f2_t xw[K];
 #pragma unroll
-  for (int k = 1; k < K; k++) xw[k] = xr[k - 1];
-  const int n = min(kSeg, L - s0);
-  if (n == kSeg) {
+  for (int k = 1; k < K; k++) xw[k] = f2_pack(xr[k - 1].x, xr[k - 1].y);
+  auto token = [&](int u) {
 #pragma unroll
-    for (int u = 0; u < kSeg; u++) {
+    for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
+    const float2 xv = xr[u + K - 1];
+    xw[K - 1] = f2_pack(xv.x, xv.y);
+    f2_t acc = b2;
 #pragma unroll
-      for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
-      xw[K - 1] = xr[u + K - 1];
-      float acc = bv;
-#pragma unroll
-      for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
-      st(o + (long)u * D, SILU ? siluf_(acc) : acc);
+    for (int k = 0; k < K; k++) acc = f2_fma(xw[k], w2[k], acc);
+    float lo, hi;
+    if constexpr (SILU) {  // silu(v) = v / (1 + 2^(-v log2 e)): the scalar steps, paired
+      float e0, e1;
+      f2_unpack(f2_mul(acc, f2_pack(-kLog2e, -kLog2e)), e0, e1);
+      f2_unpack(f2_add(f2_pack(ex2(e0), ex2(e1)), f2_pack(1.0f, 1.0f)), e0, e1);
+      acc = f2_mul(acc, f2_pack(rcp_approx(e0), rcp_approx(e1)));
     }
+    f2_unpack(acc, lo, hi);
+    IO* ot = o + (long)u * D;
+    if (pair) {
+      if constexpr (sizeof(IO) == 2) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // RNE, as st()
+        *reinterpret_cast<__nv_bfloat162*>(ot) = h;
+      } else {
+        *reinterpret_cast<float2*>(ot) = make_float2(lo, hi);
+      }
+    } else {
+      st(ot, lo);
+      if (has1) st(ot + 1, hi);
+    }
+  };
+  const int n = min(kPairSeg, L - s0);
+  if (n == kPairSeg) {
+#pragma unroll
+    for (int u = 0; u < kPairSeg; u++) token(u);
   } else {
-    for (int u = 0; u < n; u++) {
-#pragma unroll
-      for (int k = 0; k + 1 < K; k++) xw[k] = xw[k + 1];
-      xw[K - 1] = xr[u + K - 1];
-      float acc = bv;
-#pragma unroll
-      for (int k = 0; k < K; k++) acc = fmaf(xw[k], w[k], acc);
-      st(o + (long)u * D, SILU ? siluf_(acc) : acc);
-    }
+    for (int u = 0; u < n; u++) token(u);
   }
 }
 
@@ -450,21 +533,23 @@ static cudaError_t conv_fwd_t(const void* sx, const float* c, const float* bias,
   dim3 grid((D + kConvTD - 1) / kConvTD, (L + kConvTT - 1) / kConvTT, n_s);
   const IO* x = (const IO*)sx;
   IO* o = (IO*)out;
-  const dim3 gseg((D + kSegRows - 1) / kSegRows, (L + kSegTT - 1) / kSegTT, n_s);
+  const dim3 gpair((D + kPairRows - 1) / kPairRows, (L + kPairTT - 1) / kPairTT, n_s);
+  // a lane's two channels leave in one store when out and D keep every pair aligned
+  const int ovec = D % 2 == 0 && ((uintptr_t)out % (2 * sizeof(IO))) == 0;
+#define SSM_CONV_PAIR(KK)                                                                        \
+  silu ? conv_fwd_pair_kernel<IO, KK, true><<<gpair, kSegThreads, 0, st>>>(x, c, bias, o, D, L, ovec) \
+       : conv_fwd_pair_kernel<IO, KK, false><<<gpair, kSegThreads, 0, st>>>(x, c, bias, o, D, L, ovec)
   switch (K) {
-    case 1: silu ? conv_fwd_seg_kernel<IO, 1, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
-                 : conv_fwd_seg_kernel<IO, 1, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
-    case 2: silu ? conv_fwd_seg_kernel<IO, 2, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
-                 : conv_fwd_seg_kernel<IO, 2, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
-    case 3: silu ? conv_fwd_seg_kernel<IO, 3, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
-                 : conv_fwd_seg_kernel<IO, 3, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
-    case 4: silu ? conv_fwd_seg_kernel<IO, 4, true><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L)
-                 : conv_fwd_seg_kernel<IO, 4, false><<<gseg, kSegThreads, 0, st>>>(x, c, bias, o, D, L); break;
+    case 1: SSM_CONV_PAIR(1); break;
+    case 2: SSM_CONV_PAIR(2); break;
+    case 3: SSM_CONV_PAIR(3); break;
+    case 4: SSM_CONV_PAIR(4); break;
     default: {
       size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + K - 1) + kConvTD * odd_up(K));
       conv_fwd_kernel<IO><<<grid, kConvThreads, smem, st>>>(x, c, bias, o, D, L, K, silu);
     }
   }
+#undef SSM_CONV_PAIR
   count_launches(1);
   if (cs && K > 1) {
     long total = (long)n_s * D * (K - 1);
