@@ -167,9 +167,6 @@ constexpr int kSegWarps = 8;
 constexpr int kSegThreads = 32 * kSegWarps;
 constexpr int kSegTT = kSeg * kSegWarps;       // tokens per tile
 constexpr int kSegRows = 32;                   // channels per tile
-// Lanes per row when moving sx rows into shared memory (see rows_to_smem); measured best on
-// GB300.
-constexpr int kBwdLanesPerRow = 1;
 
 template <typename IO>
 __device__ __forceinline__ void unpack16(const uint4 u, float* v) {
@@ -203,46 +200,54 @@ __device__ __forceinline__ uint4 pack16(const float* v) {
 
 // Copies columns [c0, c0 + NC) of rows d0 .. d0+31 of a time-fastest [..][W] array into
 // s[r][0..NC) (row stride SP floats, odd) as fp32; zero outside [0, W) and for rows >= D.
-// 16-byte groups aligned in global memory; a group partly outside the row is read element by
-// element.  LPR lanes share a row: LPR = 1 gives one row per lane (32 rows per shared store
-// instruction, conflict-free with the odd stride); LPR = 8 gives 4 rows x 8 consecutive groups
-// (128-byte global runs, 2-way conflicts).
-template <typename IO, int NC, int SP, int LPR>
+// One row per lane (32 rows per shared store instruction, conflict-free with the odd stride),
+// groups gi = wid, wid + 8, ... of 16 bytes aligned in global memory; a group partly outside
+// the row is read element by element.  Every load of a thread is issued before its first
+// shared store, so the groups' round trips overlap.
+template <typename IO, int NC, int SP>
 __device__ __forceinline__ void rows_to_smem(const IO* base, int d0, int D, long c0, long W,
                                              float* s, int wid, int lane) {
   constexpr int V = 16 / sizeof(IO);
   constexpr int NG = (NC + V - 1) / V + 1;  // groups covering NC columns at any alignment
-  constexpr int RPW = 32 / LPR;             // rows per warp instruction
-  constexpr int ROW_PASSES = kSegRows / (RPW * kSegWarps) > 0 ? kSegRows / (RPW * kSegWarps) : 1;
-  constexpr int G0 = LPR == 1 ? kSegWarps : LPR;  // group stride of one lane
+  constexpr int KG = (NG + kSegWarps - 1) / kSegWarps;
+  const int d = d0 + lane;
+  const IO* row = base + (long)(d < D ? d : 0) * W;
+  const int ph = (int)(((uintptr_t)(row + c0) & 15) / sizeof(IO));
+  uint4 raw[KG];
 #pragma unroll
-  for (int rp = 0; rp < ROW_PASSES; rp++) {
-    const int r = LPR == 1 ? lane : (rp * kSegWarps + wid) * RPW + lane / LPR;
-    const int d = d0 + r;
-    if (r >= kSegRows || d >= D) continue;
-    const IO* row = base + (long)d * W;
-    const int ph = (int)(((uintptr_t)(row + c0) & 15) / sizeof(IO));
-    float* srow = s + r * SP;
-    for (int gi = (LPR == 1 ? wid : lane % LPR); gi < NG; gi += G0) {
-      const long cs = c0 - ph + (long)gi * V;  // column of the group's first element
-      const int j0 = (int)(cs - c0);           // its index in s
-      if (j0 >= NC) break;
-      float v[V];
-      if (cs >= 0 && cs + V <= W) {
-        unpack16<IO>(__ldg(reinterpret_cast<const uint4*>(row + cs)), v);
-      } else {
+  for (int k = 0; k < KG; k++) {
+    const int gi = wid + kSegWarps * k;
+    const long cs = c0 - ph + (long)gi * V;  // column of the group's first element
+    raw[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (d >= D || gi >= NG || cs - c0 >= NC) continue;
+    if (cs >= 0 && cs + V <= W) {
+      raw[k] = __ldg(reinterpret_cast<const uint4*>(row + cs));
+    } else {  // a partial group: its elements inside [0, W), the rest zero
+      using B = typename std::conditional<sizeof(IO) == 2, unsigned short, unsigned>::type;
+      const B* bits = reinterpret_cast<const B*>(row);
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int e = 0; e < V; e++) v[e] = (cs + e >= 0 && cs + e < W) ? ld(row + cs + e) : 0.0f;
+      for (int e = 0; e < V; e++) {
+        if (cs + e < 0 || cs + e >= W) continue;
+        const uint32_t v = __ldg(bits + cs + e);
+        if constexpr (sizeof(IO) == 2) w[e / 2] |= v << (16 * (e % 2));
+        else w[e] = v;
       }
-      if (j0 >= 0 && j0 + V <= NC) {
-#pragma unroll
-        for (int e = 0; e < V; e++) srow[j0 + e] = v[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < V; e++)
-          if (j0 + e >= 0 && j0 + e < NC) srow[j0 + e] = v[e];
-      }
+      raw[k] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+  if (d >= D) return;
+  float* srow = s + lane * SP;
+#pragma unroll
+  for (int k = 0; k < KG; k++) {
+    const int gi = wid + kSegWarps * k;
+    const int j0 = gi * V - ph;  // the group's first element's index in s
+    if (gi >= NG || j0 >= NC) continue;
+    float v[V];
+    unpack16<IO>(raw[k], v);
+#pragma unroll
+    for (int e = 0; e < V; e++)
+      if (j0 + e >= 0 && j0 + e < NC) srow[j0 + e] = v[e];
   }
 }
 
@@ -375,8 +380,9 @@ conv_fwd_pair_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
   }
 }
 
+// 4 blocks per SM for bf16; fp32's twice as many staging registers would spill there, so 3
 template <typename IO, int K, bool SILU>
-__global__ void __launch_bounds__(kSegThreads, 4)
+__global__ void __launch_bounds__(kSegThreads, sizeof(IO) == 2 ? 4 : 3)
 conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
                     const float* __restrict__ bias, const IO* __restrict__ dout,
                     IO* __restrict__ d_sx, float* __restrict__ part, int D, int L) {
@@ -406,7 +412,7 @@ conv_bwd_seg_kernel(const IO* __restrict__ sx, const float* __restrict__ c,
       dv[u] = (active && t >= 0 && t < L) ? ld(dout + ((long)b * L + t) * D + d) : 0.0f;
     }
   }
-  rows_to_smem<IO, NC, SP, kBwdLanesPerRow>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
+  rows_to_smem<IO, NC, SP>(sx + (long)b * D * W, d0, D, (long)i0 - (K - 1), W, s, wid, lane);
   __syncthreads();
   float ox[kSeg];
   float pk[K + 1];
