@@ -320,8 +320,12 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
     if (cs.lvl == 1) nxt = bnd_tile[(nsub - 1) * kScanThreads];
 
-    // ---- prepass, once per (token, channel) -----------------------------------------------
-    for (int idx = tid; idx < TT * CB; idx += kScanThreads) {
+    // ---- prepass, once per (token, channel); a compile-time item count lets the items'
+    // shared loads be in flight together -------------------------------------------------------
+    static_assert(TT * CB % kScanThreads == 0, "prepass items per thread");
+#pragma unroll
+    for (int u = 0; u < TT * CB / kScanThreads; u++) {
+      const int idx = tid + u * kScanThreads;
       const int c = idx % CB;
       const float raw = lds_f(sdt + idx);
       const float pre = raw + sPar[CB + c];

@@ -172,8 +172,12 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     const int t0 = t_begin + k * TT;
     const int cnt = min(TT, t_end - t0);
 
-    // ---- prepass (a tile that never arrived leaves stale but in-bounds shared memory) ------
-    for (int idx = tid; idx < TT * cb; idx += THR) {
+    // ---- prepass (a tile that never arrived leaves stale but in-bounds shared memory); a
+    // compile-time item count lets the items' shared loads be in flight together ------------
+    static_assert(TT * cb % THR == 0, "prepass items per thread");
+#pragma unroll
+    for (int u = 0; u < TT * cb / THR; u++) {
+      const int idx = tid + u * THR;
       const int c = idx % cb;
       float dl = lds1(sdt + idx);
       if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
