@@ -74,10 +74,10 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 967491584 + 1296482560,
+        "bytes": 961748224 + 1293426944,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "43ff157b3b14b0a955d3ae9c4a20195b4a14df89edf120a418da4951d6f338ba",
+                "b2a8a84d11cde03f9b8c3791fdc8f925c96e1988bd0ee5b2435c4171aeac1edb",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":

@@ -98,6 +98,10 @@ __device__ __forceinline__ const float* tile_rows_f32(const unsigned char* stage
 // Register slot j of a thread holds state n0 + (j ^ p), p = lane bits 3..4 (see the dB/dC sums
 // below).  B and C of a tile are kept as fp32 in 4 copies, copy p holding within every group of 4
 // states the order (j ^ p), so that each lane reads its slots with one 16-byte load.
+// Consecutive copies lie kPermPadF floats (64 bytes) more than a copy apart.  A warp reads 4
+// state groups from each of the 4 copies; unpadded (1024-byte copies) all four copies fall on
+// the same banks, and a 16-byte read took 4 shared-memory wavefronts instead of 2.
+constexpr int kPermPadF = 16;
 template <typename IO>
 __device__ __forceinline__ void tile_rows_perm(const unsigned char* stage_rows, float* dst, int count) {
   const IO* src = reinterpret_cast<const IO*>(stage_rows);
@@ -105,7 +109,7 @@ __device__ __forceinline__ void tile_rows_perm(const unsigned char* stage_rows, 
     const float v = lds_f(src + idx);
     const int base = idx & ~3, j = idx & 3;
 #pragma unroll
-    for (int pc = 0; pc < 4; pc++) dst[pc * count + base + (j ^ pc)] = v;
+    for (int pc = 0; pc < 4; pc++) dst[pc * (count + kPermPadF) + base + (j ^ pc)] = v;
   }
 }
 
@@ -122,7 +126,8 @@ __device__ __forceinline__ uint2 perm4_bf16(uint2 v, int pc) {
   return (pc & 2) ? make_uint2(v.y, v.x) : v;
 }
 // bf16 I/O: B and C of a tile as [4 copies][TT][N/4] records of 8 bf16 (B of 4 states, then C
-// of the same 4 states), copy pc in the order (j ^ pc); C is left out on level-1 tiles.
+// of the same 4 states), copy pc in the order (j ^ pc), copies kPermPadF / 4 records apart
+// beyond their size; C is left out on level-1 tiles.
 __device__ __forceinline__ void tile_bc_perm_bf16(const unsigned char* rb, const unsigned char* rc,
                                                   uint4* dst, int groups, bool with_c) {
   const uint2* b2 = reinterpret_cast<const uint2*>(rb);
@@ -132,7 +137,7 @@ __device__ __forceinline__ void tile_bc_perm_bf16(const unsigned char* rb, const
 #pragma unroll
     for (int pc = 0; pc < 4; pc++) {
       const uint2 pb = perm4_bf16(vb, pc), pcv = perm4_bf16(vc, pc);
-      dst[pc * groups + idx] = make_uint4(pb.x, pb.y, pcv.x, pcv.y);
+      dst[pc * (groups + kPermPadF / 4) + idx] = make_uint4(pb.x, pb.y, pcv.x, pcv.y);
     }
   }
 }
@@ -345,9 +350,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       sD2[idx] = make_float2(dl, dl * xv);
     }
     // B and C: this lane's permuted copy (bf16 records for bf16 I/O, fp32 rows otherwise)
-    const uint4* sBCq = reinterpret_cast<const uint4*>(smem + m.off_bf) + pm * (TT * N / 4);
-    const float* sBf = reinterpret_cast<const float*>(smem + m.off_bf) + pm * TT * N;
-    const float* sCf = reinterpret_cast<const float*>(smem + m.off_cf) + pm * TT * N;
+    const uint4* sBCq = reinterpret_cast<const uint4*>(smem + m.off_bf) + pm * (TT * N / 4 + kPermPadF / 4);
+    const float* sBf = reinterpret_cast<const float*>(smem + m.off_bf) + pm * (TT * N + kPermPadF);
+    const float* sCf = reinterpret_cast<const float*>(smem + m.off_cf) + pm * (TT * N + kPermPadF);
     if constexpr (sizeof(IO) == 2) {
       tile_bc_perm_bf16(base + m.off_b, base + m.off_c, reinterpret_cast<uint4*>(smem + m.off_bf),
                         TT * N / 4, cs.lvl == 1);
@@ -721,8 +726,8 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->off_e = take(TT * cb * 16);
   // B, C in 4 permuted copies: bf16 records (B and C together) or fp32 rows; off_cf also holds
   // the local kernel's fp32 C rows
-  m->off_bf = take(io == 2 ? 4 * TT * p.N * 4 : 4 * TT * p.N * 4);
-  m->off_cf = take(io == 2 ? TT * p.N * 4 : 4 * TT * p.N * 4);
+  m->off_bf = take(4 * (TT * p.N + kPermPadF) * 4);
+  m->off_cf = take(io == 2 ? TT * p.N * 4 : 4 * (TT * p.N + kPermPadF) * 4);
   m->off_part = take(3 * TT * (kScanThreads / 2) * 4);
   m->off_red = take(TT * kWarps * 2 * p.N * 4);
   m->out_tile = al(tile);
