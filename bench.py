@@ -74,10 +74,10 @@ FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 961748224 + 1293426944,
+        "bytes": 958956544 + 1293119744,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "b2a8a84d11cde03f9b8c3791fdc8f925c96e1988bd0ee5b2435c4171aeac1edb",
+                "0592b6cd43bced5da92b596baa0b110a78e293c3cfe4de2dd02ac366981512fa",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":

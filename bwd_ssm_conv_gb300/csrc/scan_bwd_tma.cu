@@ -301,15 +301,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 
   for (Pos cs = first(); cs.ck >= c_first; advance(cs), qpos++) {
     const int stg = qpos % kBwdStages;
+    // a tile that never arrived leaves stale but in-bounds shared memory: the prepass reads it,
+    // and the barrier after the prepass sends the whole block out
     const bool ok = mbar_wait(&full[stg], (uint32_t)(qpos / kBwdStages) & 1u);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        record_status(p.status, SSM_ERR_TIMEOUT);
-        for (int j = qpos; j < issued; j++) mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
-        tma_store_wait_all();
-      }
-      return;
-    }
     const unsigned char* base = smem + stg * m.stage_stride;
     const IO* sx = reinterpret_cast<const IO*>(base + m.off_x);
     const IO* sdt = reinterpret_cast<const IO*>(base + m.off_dt);
@@ -387,7 +381,14 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         C2[1] = f2_pack(w.z, w.w);
       }
     };
-    __syncthreads();
+    if (__syncthreads_or(!ok)) {  // the prepass and the B/C copies are complete
+      if (tid == 0) {
+        record_status(p.status, SSM_ERR_TIMEOUT);
+        for (int j = qpos; j < issued; j++) mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
+        tma_store_wait_all();
+      }
+      return;
+    }
 
     if (cs.lvl == 0) {
       // ---- level 1: walk the tile forward, keeping every sub-chunk's start state ----------
