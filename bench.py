@@ -9,7 +9,9 @@ bandwidth of the scan kernels.  Default workload: the training-shaped Mamba-1 la
 (16 x 2048 tokens, d_inner 1536, d_state 16, d_conv 4, bf16 I/O, fp32 state, z gate and D
 skip, checkpoints every 256 tokens).
 
-Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl reference]
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME | --config I]
+                        [--impl reference]
+--config I picks the I-th workload of bwd_ssm_conv_gb300.workloads.WORKLOADS.
 With N > 1 it is launched by torch.distributed.run, one process per GPU; each GPU runs an
 independent replica (the path has no cross-GPU exchange), value = all tokens / max time.
 """
@@ -31,10 +33,10 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from bwd_ssm_conv_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+from bwd_ssm_conv_gb300.workloads import WORKLOADS, make_inputs, workload  # noqa: E402
 
 METRIC = "selective-scan fwd+bwd tokens/s (B·L/s) and achieved HBM GB/s vs 8 TB/s"
-DEFAULT_CONFIG = 4
+DEFAULT_WORKLOAD = "mamba1_train_bf16_b16_l2048_d1536_n16"
 SPEC_HBM_GBS = 8000.0
 
 
@@ -481,12 +483,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[x.name for x in WORKLOADS])
+    ap.add_argument("--config", type=int, default=None,
+                    help="position of the workload in WORKLOADS (overrides --workload)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    w = CONFIGS[args.config]
+    w = WORKLOADS[args.config] if args.config is not None else workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
         return

@@ -64,8 +64,8 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five configurations of the benchmark, in order.
-CONFIGS = [
+# The five workloads of the benchmark, in order (`bench.py --config I` picks one by position).
+WORKLOADS = [
     Workload("mamba1_tiny_f32_b1_l64_d16_n4", 1, 64, 16, d_state=4, io="f32", seed=1000),
     Workload("mamba1_layer_f32_b8_l1024_d512_n16", 8, 1024, 512, d_state=16, io="f32", seed=1001),
     Workload("mamba2_scan_f32_b4_l2048_h24_p64_n128", 4, 2048, 24, head_dim=64, d_state=128,
@@ -78,8 +78,12 @@ CONFIGS = [
 ]
 
 
-def config(i: int) -> Workload:
-    return CONFIGS[i]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def workload(name: str) -> Workload:
+    """The benchmark workload of that name (KeyError for an unknown name)."""
+    return BY_NAME[name]
 
 
 def _round_io(t: torch.Tensor, io: str) -> torch.Tensor:
@@ -143,7 +147,7 @@ def make_inputs(w: Workload, seed: int | None = None, grad_seed_state: bool = Fa
 def random_scan_inputs(n_seqs, n_tok, n_head, head_dim, d_state, n_group=1, io="f32",
                        scalar_a=False, has_z=True, has_D=True, s0=True, seed=0,
                        dt_raw=False) -> dict:
-    """Small arbitrary-shape scan inputs for tests (same distributions as the configs).
+    """Small arbitrary-shape scan inputs for tests (same distributions as the workloads).
 
     ``dt_raw``: draw dt ~ U(-1, 1) (a raw pre-softplus value, as in ggmlR's scan gradcheck)."""
     g = torch.Generator(device="cpu")

@@ -4,14 +4,14 @@ import torch
 
 import oracle
 from bwd_ssm_conv_gb300 import binding
-from bwd_ssm_conv_gb300.workloads import CONFIGS, make_inputs, random_conv_inputs
+from bwd_ssm_conv_gb300.workloads import make_inputs, random_conv_inputs, workload
 from gpu_util import assert_close, tol
 
 pytestmark = pytest.mark.gpu
 
 # n_s, d_inner, n_t, d_conv, io, bias, silu
 CASES = [
-    (1, 16, 64, 4, "f32", False, True),     # config 0's shape
+    (1, 16, 64, 4, "f32", False, True),     # the tiny workload's shape
     (2, 37, 130, 3, "f32", True, True),     # ragged channels and time
     (3, 33, 65, 1, "f32", False, False),    # K = 1
     (2, 64, 200, 7, "bf16", True, True),
@@ -55,9 +55,12 @@ def test_conv_bwd_deterministic():
         assert torch.equal(u, v)
 
 
-@pytest.mark.parametrize("i", [0, 1, 3, 4])
-def test_conv_full_config(i):
-    w = CONFIGS[i]
+@pytest.mark.parametrize("name", ["mamba1_tiny_f32_b1_l64_d16_n4",
+                                  "mamba1_layer_f32_b8_l1024_d512_n16",
+                                  "mamba1_long_bf16_b1_l16384_d2048_n16",
+                                  "mamba1_train_bf16_b16_l2048_d1536_n16"])
+def test_conv_full_workload(name):
+    w = workload(name)
     inp = make_inputs(w)
     sx, c = inp["sx"].cuda(), inp["c"].cuda()
     out = binding.ssm_conv_fwd(sx, c, None, silu=True)

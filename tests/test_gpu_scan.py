@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from bwd_ssm_conv_gb300 import binding
-from bwd_ssm_conv_gb300.workloads import CONFIGS, make_inputs, random_scan_inputs
+from bwd_ssm_conv_gb300.workloads import make_inputs, random_scan_inputs, workload
 from gpu_util import (assert_close, channel_subset, gpu_bwd, gpu_fwd, oracle_bwd, oracle_fwd, tol)
 
 pytestmark = pytest.mark.gpu
@@ -216,10 +216,10 @@ def test_ggml_packing_roundtrip():
     assert torch.equal(packed[: y.numel()].view_as(y), y)
 
 
-# ---- full-size benchmark configurations ---------------------------------------------------
+# ---- full-size benchmark workloads ---------------------------------------------------------
 
-def _config_inputs(i):
-    w = CONFIGS[i]
+def _workload_inputs(name):
+    w = workload(name)
     inp = make_inputs(w, grad_seed_state=True)
     if inp["x"] is None:  # the conv prelude produces x; the scan parity needs only its shape
         g = torch.Generator().manual_seed(w.seed + 7)
@@ -227,9 +227,9 @@ def _config_inputs(i):
     return w, inp
 
 
-@pytest.mark.parametrize("i", [1])
-def test_config_full_parity(i):
-    w, inp = _config_inputs(i)
+@pytest.mark.parametrize("name", ["mamba1_layer_f32_b8_l1024_d512_n16"])
+def test_workload_full_parity(name):
+    w, inp = _workload_inputs(name)
     y, st, ck = gpu_fwd(inp, w.chunk)
     yo, so, co = oracle_fwd(inp, w.chunk)
     assert_close("y", y, yo, tol(w.io, False))
@@ -242,8 +242,8 @@ def test_config_full_parity(i):
             assert_close(k, g[k], o[k], tol(w.io, True))
 
 
-def test_config2_mamba2_forward_sampled_heads():
-    w, inp = _config_inputs(2)
+def test_mamba2_scan_forward_sampled_heads():
+    w, inp = _workload_inputs("mamba2_scan_f32_b4_l2048_h24_p64_n128")
     y, st, ck = gpu_fwd(inp, w.chunk)
     heads = [0, 11, 23]
     sub = dict(inp)
@@ -258,9 +258,10 @@ def test_config2_mamba2_forward_sampled_heads():
     assert_close("ckpt", ck[:, :, heads], co, tol(w.io, False))
 
 
-@pytest.mark.parametrize("i", [3, 4])
-def test_config_full_size_sampled_channels(i):
-    w, inp = _config_inputs(i)
+@pytest.mark.parametrize("name", ["mamba1_long_bf16_b1_l16384_d2048_n16",
+                                  "mamba1_train_bf16_b16_l2048_d1536_n16"])
+def test_workload_full_size_sampled_channels(name):
+    w, inp = _workload_inputs(name)
     D = w.n_head
     idx = torch.tensor(sorted({0, 1, 31, 32, 127, D // 2, D - 2, D - 1}), dtype=torch.long)
     y, st, ck = gpu_fwd(inp, w.chunk)
