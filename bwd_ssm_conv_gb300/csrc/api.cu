@@ -117,7 +117,7 @@ const char* ssm_status_string(int s) {
     case SSM_ERR_UNSUPPORTED: return "size beyond a documented limit of this library";
     case SSM_ERR_WORKSPACE: return "workspace missing or smaller than the *_workspace_size result";
     case SSM_ERR_CUDA: return "a CUDA launch failed";
-    case SSM_ERR_TIMEOUT: return "a bounded wait for a staged tile gave up; that block skipped the rest of its work";
+    case SSM_ERR_TIMEOUT: return "a bounded wait (for a staged tile, or for the next chunk's adjoint) gave up; that block skipped the rest of its work";
     case SSM_ERR_NONFINITE: return "a non-finite output was produced";
     default: return "unknown status";
   }

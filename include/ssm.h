@@ -74,7 +74,10 @@ enum {
   SSM_ERR_UNSUPPORTED = -2, /* size beyond a documented limit (d_conv, d_state, element counts) */
   SSM_ERR_WORKSPACE = -3,   /* ws is NULL or smaller than the *_workspace_size result */
   SSM_ERR_CUDA = -4,        /* a kernel launch failed (cudaGetLastError after enqueue) */
-  SSM_ERR_TIMEOUT = -5,     /* reserved: no kernel of this version waits, none can time out */
+  SSM_ERR_TIMEOUT = -5,     /* status word only: a bounded wait gave up (a staged tile that
+                               never arrived, or the next chunk's adjoint in the persistent
+                               backward); that block skipped the rest of its work, so the
+                               call's outputs are incomplete */
   SSM_ERR_NONFINITE = -6    /* SSM_CHECK_FINITE: an output element was NaN or +-Inf */
 };
 
@@ -149,6 +152,18 @@ int ssm_conv_bwd_noalloc(const void* sx, const float* c, const float* bias, cons
                          int d_conv, int io, unsigned flags, void* stream);
 
 /* ---- selective scan ---------------------------------------------------------------------
+ * Which kernels run depends on the shape and the pointers; every combination gives the same
+ * results up to summation order.
+ *   - Mamba-1 form (head_dim 1, one A per state): TMA-staged kernels when all of these hold:
+ *     - the activation pointers (x, dt, B, C, z, y, dy, d_x, d_dt, d_z) are 16-byte aligned;
+ *     - a token's row of each (H*P or G*N elements) is a multiple of 16 bytes;
+ *     - chunk is a multiple of 16;
+ *     - a group's channels fill whole blocks (32 channels for d_state 16).
+ *     The forward takes d_state a multiple of 4 up to 256; the backward takes d_state 16.
+ *   - Mamba-2 form (one A per head): head-tiled kernels for head_dim a multiple of 64 (forward)
+ *     or 32 (backward) with d_state 128.
+ *   - Anything else runs the general kernels, which are slower but take any alignment
+ *     of the element type and any size within the limits above.
  * Bytes of scratch ssm_scan_fwd (backward = 0) or ssm_scan_bwd (backward = 1) needs for this
  * descriptor on the current device; 0 if the descriptor is invalid.  Always >= 256 (the
  * status word lives there).  The backward size assumes ckpt may be NULL. */
@@ -206,8 +221,9 @@ int ssm_decode_step(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags,
                     float* state, void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* Reads the device status word of the last scan call that used `ws` (waits for `stream`).
- * Writes SSM_OK, SSM_ERR_INVALID_ARG (bad id) or SSM_ERR_NONFINITE to *status and returns
- * SSM_OK; returns SSM_ERR_INVALID_ARG for NULL pointers or SSM_ERR_CUDA. */
+ * Writes SSM_OK, SSM_ERR_INVALID_ARG (bad id), SSM_ERR_NONFINITE or SSM_ERR_TIMEOUT to
+ * *status and returns SSM_OK; returns SSM_ERR_INVALID_ARG for NULL pointers or SSM_ERR_CUDA.
+ * The first error recorded stays until the next call that uses `ws` clears it. */
 int ssm_scan_status(const void* ws, int* status, void* stream);
 
 /* Static description of a status code. */
