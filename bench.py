@@ -56,18 +56,21 @@ def alg_bytes(w) -> dict:
             "conv_bwd": conv_bwd}
 
 
-# Algorithmic FP32 flops per (token, channel, state) element of the scan kernels (an FMA counts
-# 2, a multiply 1; the SFU exponentials are counted separately).
+# Algorithmic FP32 flops per (token, channel, state) element of the method itself (an FMA
+# counts 2, a multiply 1; the SFU exponentials are counted separately), for the secondary ALU
+# view of the roofline:
 #   forward:  delta*A (1), (delta x)*B (1), h = a h + u (2), y += C h (2)                    = 6
-#   backward: two forward recomputes (4 each, without C h) + the adjoint: dh = gy C + carry (2),
-#             dC += gy h (1), sum dh B (2), dB = dh delta x (1), carry = a dh (1),
-#             w = carry h_prev (1), sum A w (2), dA += delta w (2), y_pre += C h (2)      = 22
-# With one A per head (the Mamba-2 form) delta*A is one product per (token, head), not per
-# element: 5 and 20.
-SCAN_FLOPS = {"scan_fwd": 6, "scan_bwd": 22}
-SCAN_FLOPS_SCALAR_A = {"scan_fwd": 5, "scan_bwd": 20}
+#   backward: one recompute of the state (4, as the forward without C h) and the adjoint:
+#             dh = gy C + carry (2), carry = a dh (1), w = carry h_prev (1), dA += delta w (2),
+#             sum A w (2), sum dh B (2), dB += dh delta x (2), dC += gy h (2), y_pre += C h (2)
+#                                                                                          = 20
+# With one A per head (the Mamba-2 form) delta*A is one product per (token, head): 5 and 19.
+SCAN_FLOPS = {"scan_fwd": 6, "scan_bwd": 20}
+SCAN_FLOPS_SCALAR_A = {"scan_fwd": 5, "scan_bwd": 19}
 FP32_LANES_PER_SM = 128   # measured: 128 FFMA lanes per SM per clock on GB300 (packed f32x2
                           # issues half the instructions at the same lane rate)
+# The two configurations the throughput target is stated on; the default run measures both.
+TARGET_WORKLOADS = ("mamba1_long_bf16_b1_l16384_d2048_n16", DEFAULT_WORKLOAD)
 
 
 # DRAM traffic of the dominant kernel per launch, from one ncu capture of this workload
@@ -407,75 +410,242 @@ def config_of(w, world: int) -> dict:
             "l2": "flushed before every step"}
 
 
-def oracle_sample(w, channels, seqs=1, seed=None):
-    """Runs the oracle's whole step on `seqs` sequences x all tokens x `channels` channels of
-    the workload; returns (seconds, channel-tokens processed)."""
-    import oracle
-    inp = make_inputs(w.with_(n_seqs=seqs, n_head=channels), seed=seed)
-    t0 = time.perf_counter()
-    dims = oracle.ScanDims(seqs, w.n_tok, channels, w.head_dim, w.d_state, n_group=w.n_group,
-                           a_per_state=0 if w.scalar_a else 1, chunk=w.chunk)
-    if w.d_conv:
-        x = oracle.conv_fwd(inp["sx"], inp["c"], None, silu=True)
-        x = x.reshape(seqs, w.n_tok, channels, w.head_dim)
-    else:
-        x = inp["x"]
-    _, _, ck = oracle.scan_fwd(dims, x=x, dt=inp["dt"], A=inp["A"], B=inp["B"], C=inp["C"],
-                               D=inp["D"], z=inp["z"], s0=inp["s0"])
-    if not w.fwd_only:
-        g = oracle.scan_bwd(dims, x=x, dt=inp["dt"], A=inp["A"], B=inp["B"], C=inp["C"],
-                            dy=inp["dy"], D=inp["D"], z=inp["z"], ckpt=ck)
+def host_cores() -> int:
+    """Host cores this process may run on (the oracle's threads use all of them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _f64(t):
+    import numpy as np
+    if t is None:
+        return None
+    return np.ascontiguousarray(t.detach().to("cpu").double().numpy())
+
+
+def oracle_slices(w, inp, seqs, parts):
+    """The first `seqs` sequences of a workload's inputs cut into independent slices for the
+    oracle: every slice holds whole sequences and whole tokens of a subset of channels (heads
+    in the scalar-A form), converted to float64 once, outside any timed region.  Channels are
+    independent except for the sums of dB and dC over channels, which each slice forms over
+    its own channels (the same work)."""
+    H, P = w.n_head, w.head_dim
+    step = max(1, -(-H // max(1, parts)))
+    out = []
+    for h0 in range(0, H, step):
+        h1 = min(H, h0 + step)
+        c0, c1 = h0 * P, h1 * P
+        sl = {"H": h1 - h0}
         if w.d_conv:
-            oracle.conv_bwd(inp["sx"], inp["c"], g["d_x"].reshape(seqs, w.n_tok, channels),
-                            silu=True)
-    return time.perf_counter() - t0, seqs * w.n_tok * channels
+            sl["sx"] = _f64(inp["sx"][:seqs, c0:c1])
+            sl["c"] = _f64(inp["c"][c0:c1])
+            sl["x"] = None
+        else:
+            sl["x"] = _f64(inp["x"][:seqs, :, h0:h1])
+        sl["dt"] = _f64(inp["dt"][:seqs, :, h0:h1])
+        sl["A"] = _f64(inp["A"][h0:h1])
+        sl["B"] = _f64(inp["B"][:seqs])
+        sl["C"] = _f64(inp["C"][:seqs])
+        sl["D"] = _f64(inp["D"][c0:c1]) if inp.get("D") is not None else None
+        sl["z"] = _f64(inp["z"][:seqs, :, h0:h1]) if inp.get("z") is not None else None
+        sl["s0"] = _f64(inp["s0"][:seqs, h0:h1]) if inp.get("s0") is not None else None
+        sl["dy"] = _f64(inp["dy"][:seqs, :, h0:h1])
+        out.append(sl)
+    return out
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """Oracle tokens/s at the workload's full width, from a bounded sample of the workload:
-    whole sequences of all channels when they fit the budget, else a channel subset."""
-    t, ct = oracle_sample(w, channels=4 * w.head_dim if w.head_dim > 1 else 4)
-    per_ct = t / ct
-    full_seq = per_ct * w.n_tok * w.n_head  # seconds for one sequence, all channels
-    if full_seq <= budget_s:
-        seqs = max(1, min(w.n_seqs, int(budget_s / full_seq)))
-        ch = w.n_head
-    else:
-        seqs, ch = 1, max(1, int(budget_s / (per_ct * w.n_tok)))
-    t, ct = oracle_sample(w, channels=ch, seqs=seqs)
-    tokens_per_s = ct / t / w.n_head  # every channel of every token
-    return {"value": tokens_per_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{seqs} of {w.n_seqs} sequences x {w.n_tok} tokens x {ch} of {w.n_head} "
-                      f"channels of the same workload, full step (conv fwd, scan fwd, scan bwd, "
-                      f"conv bwd), {t:.1f} s single-threaded f64; scaled to all channels"}
+def oracle_run(w, slices, seqs, threads):
+    """Runs the oracle's whole step -- conv fwd, scan fwd (checkpoints), scan bwd from the
+    checkpoints, conv bwd -- over `slices` on `threads` host threads (the oracle's C calls
+    release the GIL).  Returns (forward seconds, backward seconds), each a wall-clock time."""
+    import concurrent.futures as cf
+    import oracle
+
+    def dims(sl):
+        return oracle.ScanDims(seqs, w.n_tok, sl["H"], w.head_dim, w.d_state, n_group=w.n_group,
+                               a_per_state=0 if w.scalar_a else 1, chunk=w.chunk)
+
+    def fwd(sl):
+        x = sl["x"]
+        if w.d_conv:
+            x = oracle.conv_fwd(sl["sx"], sl["c"], None, silu=True)
+            x = x.reshape(seqs, w.n_tok, sl["H"], w.head_dim)
+        _, _, ck = oracle.scan_fwd(dims(sl), x=x, dt=sl["dt"], A=sl["A"], B=sl["B"], C=sl["C"],
+                                   D=sl["D"], z=sl["z"], s0=sl["s0"])
+        return x, ck
+
+    def bwd(sl, x, ck):
+        g = oracle.scan_bwd(dims(sl), x=x, dt=sl["dt"], A=sl["A"], B=sl["B"], C=sl["C"],
+                            dy=sl["dy"], D=sl["D"], z=sl["z"], s0=sl["s0"], ckpt=ck)
+        if w.d_conv:
+            oracle.conv_bwd(sl["sx"], sl["c"], g["d_x"].reshape(seqs, w.n_tok, -1), silu=True)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        mid = list(ex.map(fwd, slices))
+        t1 = time.perf_counter()
+        bw_s = 0.0
+        if not w.fwd_only:
+            list(ex.map(lambda a: bwd(*a), [(sl, x, ck) for sl, (x, ck) in zip(slices, mid)]))
+            bw_s = time.perf_counter() - t1
+    return t1 - t0, bw_s
+
+
+def oracle_seqs_for(w, inp, budget_cpu_s, cap=None):
+    """How many whole sequences of the workload the oracle can run within `budget_cpu_s`
+    seconds of CPU time (at least one), from a timed probe of one sequence x 2 channels."""
+    probe = w.with_(n_head=2)
+    f, b = oracle_run(probe, oracle_slices(probe, _probe_inputs(w, inp), 1, 1), 1, 1)
+    per_seq = (f + b) * w.n_head / 2.0
+    n = max(1, min(cap or w.n_seqs, int(budget_cpu_s / max(per_seq, 1e-9))))
+    return n, per_seq
+
+
+def _probe_inputs(w, inp):
+    """The first two channels of the workload's inputs (all tokens, every sequence)."""
+    H2, P = 2, w.head_dim
+    out = dict(inp)
+    for k in ("x", "z", "dy"):
+        if inp.get(k) is not None:
+            out[k] = inp[k][:, :, :H2]
+    out["dt"] = inp["dt"][:, :, :H2]
+    out["A"] = inp["A"][:H2]
+    if inp.get("D") is not None:
+        out["D"] = inp["D"][:H2 * P]
+    if inp.get("c") is not None:
+        out["c"] = inp["c"][:H2 * P]
+    if inp.get("s0") is not None:
+        out["s0"] = inp["s0"][:, :H2]
+    return out
+
+
+def oracle_baseline(w, inp, cores, budget_cpu_s):
+    """The oracle on `cores` host threads over whole sequences of the workload (all of them if
+    they fit the CPU-time budget), forward and backward timed separately."""
+    seqs, _ = oracle_seqs_for(w, inp, budget_cpu_s)
+    slices = oracle_slices(w, inp, seqs, 4 * cores if cores > 1 else 1)
+    f, b = oracle_run(w, slices, seqs, cores)
+    tok = seqs * w.n_tok
+    rec = {"value": tok / (f + b), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "fwd_s": f, "bwd_s": b, "fwd_tokens_s": tok / f,
+           "sample": (f"{seqs} of {w.n_seqs} sequences x {w.n_tok} tokens x all {w.channels} "
+                      f"channels of {w.name}: conv fwd + scan fwd (forward), scan bwd from the "
+                      f"checkpoints + conv bwd (backward); f64 oracle on {cores} host threads "
+                      f"over channel slices; inputs converted to f64 before timing")}
+    if not w.fwd_only:
+        rec["bwd_tokens_s"] = tok / b
+    return rec
+
+
+def cpu_baseline(w, inp, budget_cpu_s=30.0):
+    """The oracle timed on all host cores on the bench's workload (whole sequences, all of them
+    when they fit the budget), plus single-thread numbers on the two small configurations."""
+    cores = host_cores()
+    rec = oracle_baseline(w, inp, cores, budget_cpu_s)
+    single = {}
+    for small in WORKLOADS[:2]:
+        si = make_inputs(small)
+        r = oracle_baseline(small, si, 1, budget_cpu_s=1e9)
+        single[small.name] = {k: r[k] for k in ("value", "fwd_s", "bwd_s") if k in r}
+    rec["single_thread"] = single
+    return rec
 
 
 def run_reference(args, w):
+    """The reference arm: the oracle, on all host cores, timed on whole sequences of the
+    workload; each step runs the same sample, sized so that warm-up and timed steps end within
+    about two minutes.  The line's value and ms_per_step are those of the steps it timed."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    # size each step so that warmup + steps finish in about two minutes
-    t, ct = oracle_sample(w, channels=2)
-    per_ct = t / ct
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    ch = max(1, min(w.n_head, int(budget / (per_ct * w.n_tok))))
+    inp = make_inputs(w, grad_seed_state=False)
+    cores = host_cores()
+    budget_cpu = 120.0 * cores / max(1, args.steps + args.warmup)
+    seqs, _ = oracle_seqs_for(w, inp, budget_cpu)
+    slices = oracle_slices(w, inp, seqs, 4 * cores if cores > 1 else 1)
     for _ in range(args.warmup):
-        oracle_sample(w, channels=ch)
-    times = [oracle_sample(w, channels=ch)[0] for _ in range(args.steps)]
+        oracle_run(w, slices, seqs, cores)
+    times = [sum(oracle_run(w, slices, seqs, cores)) for _ in range(args.steps)]
     t_mean = sum(times) / len(times)
-    value = (ch * w.n_tok / t_mean) / w.n_head
-    sample = (f"each step: 1 sequence x {w.n_tok} tokens x {ch} of {w.n_head} channels, full "
-              f"step, single-threaded f64 oracle; tokens/s scaled to all channels")
+    value = seqs * w.n_tok / t_mean
+    sample = (f"each step: {seqs} of {w.n_seqs} sequences x {w.n_tok} tokens x all "
+              f"{w.channels} channels, full step (conv fwd, scan fwd, scan bwd, conv bwd), f64 "
+              f"oracle on {cores} host threads; value and ms_per_step are of these steps")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * w.n_seqs * w.n_tok / value, "higher_is_better": True,
+            "ms_per_step": 1000.0 * t_mean, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, args.gpus),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+def stage_record(w, stage_ms, peaks) -> dict:
+    """Per-stage time, achieved algorithmic GB/s and its fraction of the measured copy peak and
+    of the 8 TB/s spec, for one workload."""
+    ab = alg_bytes(w)
+    tokens = w.n_seqs * w.n_tok
+    gbs = {k: ab[k] * tokens / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
+    return {"stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "stage_hbm_gbs": {k: round(v, 1) for k, v in gbs.items()},
+            "stage_frac_of_measured": {k: round(v / peaks["hbm_gbs"], 4) for k, v in gbs.items()},
+            "stage_frac_of_8tbs": {k: round(v / SPEC_HBM_GBS, 4) for k, v in gbs.items()}}
+
+
+def roofline_of(w, stage_ms, peaks, peak_src, sms, mhz) -> dict:
+    """Roofline of the dominant stage: algorithmic bytes per launch over its mean CUDA-event
+    time against the measured HBM copy peak.  The ALU view (the method's own FP32 flops against
+    the SMs' FP32 lanes at the sampled clock) rides along as a secondary field."""
+    ab = alg_bytes(w)
+    tokens = w.n_seqs * w.n_tok
+    dom = max(stage_ms, key=stage_ms.get)
+    dom_bytes = ab[dom] * tokens
+    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
+    traffic, traffic_kernel = captured_traffic(dom)
+    roof = {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "peak_source": peak_src, "traffic": traffic, "traffic_kernel": traffic_kernel,
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "algorithmic_bytes_per_token": ab[dom]}
+    if dom in SCAN_FLOPS:
+        elems = tokens * w.channels * w.d_state
+        flops = (SCAN_FLOPS_SCALAR_A if w.scalar_a else SCAN_FLOPS)[dom] * elems
+        fp32_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        ach_tf = flops / (stage_ms[dom] * 1e-3) / 1e12
+        roof["alu"] = {"achieved": ach_tf, "peak": fp32_peak, "unit": "TFLOP/s",
+                       "frac": ach_tf / fp32_peak, "algorithmic_flops_per_launch": flops,
+                       "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                                      f"x {mhz:.0f} MHz (sampled)"}
+    return roof
+
+
+def measure_target(w, dev, flush, steps, warmup, peaks, with_oracle) -> dict:
+    """Stage times of another workload on this GPU (device-timed as the main line, L2 flushed
+    before every step), with its own clock record and, optionally, its oracle baseline."""
+    inp = make_inputs(w, grad_seed_state=False)
+    step = Step(w, dev, inp)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    total, per_stage, launches = time_device(step, steps, warmup, flush)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    ms = sum(total) / len(total)
+    stage_ms = {k: sum(v) / len(v) for k, v in per_stage.items()}
+    rec = {"value": w.n_seqs * w.n_tok / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+           "steps": steps, "warmup": warmup, **stage_record(w, stage_ms, peaks),
+           "gpu_launches": int(launches), "clocks": clocks}
+    del step
+    if with_oracle:
+        rec["cpu_baseline"] = oracle_baseline(w, inp, host_cores(), budget_cpu_s=30.0)
+    return rec
 
 
 def main():
@@ -489,6 +659,8 @@ def main():
                     help="position of the workload in WORKLOADS (overrides --workload)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the second target configuration's sub-record")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.config] if args.config is not None else workload(args.workload)
@@ -541,44 +713,17 @@ def main():
     tokens = w.n_seqs * w.n_tok
     value = job_throughput(tokens, world, ms)
     peaks, peak_src = _measured_peaks()
-    ab = alg_bytes(w)
     stage_ms = {k: sum(v) / len(v) for k, v in per_stage.items()}
-    dom = max(stage_ms, key=stage_ms.get)
-    dom_bytes = ab[dom] * tokens
-    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9
-    stage_gbs = {k: ab[k] * tokens / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
     props = torch.cuda.get_device_properties(dev)
     mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
-    fp32_peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12  # TFLOP/s
-    traffic, traffic_kernel = captured_traffic(dom)
-    if dom in SCAN_FLOPS:
-        # The scan kernels are bound by FP32 arithmetic, not HBM: per element the backward needs
-        # ~22 flops for ~0.9 bytes, far above the GB300 ridge (~12 flops/byte).
-        elems = tokens * w.channels * w.d_state
-        flops = (SCAN_FLOPS_SCALAR_A if w.scalar_a else SCAN_FLOPS)[dom] * elems
-        ach_tf = flops / (stage_ms[dom] * 1e-3) / 1e12
-        roofline = {"kernel": f"ssm_{dom}", "bound": "alu", "achieved": ach_tf,
-                    "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach_tf / fp32_peak,
-                    "peak_source": f"derived: SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz",
-                    "traffic": traffic, "traffic_kernel": traffic_kernel,
-                    "algorithmic_flops_per_launch": flops,
-                    "hbm": {"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src,
-                            "algorithmic_bytes_per_launch": dom_bytes}}
-    else:
-        roofline = {"kernel": f"ssm_{dom}", "bound": "hbm", "achieved": achieved,
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "peak_source": peak_src, "traffic": traffic, "traffic_kernel": traffic_kernel,
-                    "algorithmic_bytes_per_launch": dom_bytes}
+    roofline = roofline_of(w, stage_ms, peaks, peak_src, props.multi_processor_count, mhz)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.io == "bf16" else "f32", "data": "synthetic",
         "config": config_of(w, world),
-        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "stage_hbm_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
-        "stage_frac_of_8tbs": {k: round(v / SPEC_HBM_GBS, 4) for k, v in stage_gbs.items()},
+        **stage_record(w, stage_ms, peaks),
         "roofline": roofline,
         "gpu_launches": int(launches),
         "clocks": clocks,
@@ -587,8 +732,17 @@ def main():
                 "pipelined": "2 buffer sets, copies of steps i+1 / i-1 overlap step i; inputs and results each one packed copy",
                 "serial_ms_per_step": serial_ms},
     }
+    if world == 1 and not args.no_targets and w.name in TARGET_WORKLOADS:
+        line["targets"] = {w.name: {k: line[k] for k in ("stage_ms", "stage_hbm_gbs",
+                                                         "stage_frac_of_measured",
+                                                         "stage_frac_of_8tbs")}}
+        for name in TARGET_WORKLOADS:
+            if name != w.name:
+                line["targets"][name] = measure_target(workload(name), dev, flush,
+                                                       min(args.steps, 50), args.warmup,
+                                                       peaks, not args.no_cpu_baseline)
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -527,9 +527,14 @@ conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ d_c,
 }
 
 // ---- host launchers ----------------------------------------------------------------------
+// One partial of d_c and d_bias per (sequence, time tile, channel): the tile is the one
+// conv_bwd_t launches with (kSegTT tokens for d_conv <= 4, kConvTT above).
+static int conv_bwd_tile(int K) { return K <= 4 ? kSegTT : kConvTT; }
+
 size_t conv_bwd_ws_bytes(int n_s, int D, int L, int K) {
   long W = (long)L + K - 1;
-  long nt = (W + kConvTT - 1) / kConvTT;
+  const int tt = conv_bwd_tile(K);
+  long nt = (W + tt - 1) / tt;
   return align_up(sizeof(float) * (size_t)n_s * nt * D * (K + 1), 256);
 }
 
@@ -571,7 +576,7 @@ static cudaError_t conv_bwd_t(const void* sx, const float* c, const float* bias,
                               void* d_sx, float* d_c, float* d_bias, void* ws, int n_s, int D,
                               int L, int K, int silu, cudaStream_t st) {
   long W = (long)L + K - 1;
-  const int tt = K <= 4 ? kSegTT : kConvTT;
+  const int tt = conv_bwd_tile(K);
   int nt = (int)((W + tt - 1) / tt);
   dim3 grid((D + kConvTD - 1) / kConvTD, nt, n_s);
   size_t smem = sizeof(float) * (kConvTD * odd_up(kConvTT + 2 * K - 2) +

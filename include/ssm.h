@@ -145,7 +145,9 @@ int ssm_conv_bwd(const void* sx, const float* c, const float* bias, const void* 
  * that device current; make that first call before any stream capture.  All calls on a
  * device share the array and it keeps the last call's contents (each call overwrites what it
  * reads), so calls that overlap on the GPU -- on different streams or threads -- race: keep
- * them ordered on one stream.  Allocates and frees nothing. */
+ * them ordered on one stream.  The looked-up address belongs to the device's current context:
+ * calls after cudaDeviceReset (or anything else that replaces the primary context) are not
+ * supported.  Allocates and frees nothing. */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 int ssm_conv_bwd_noalloc(const void* sx, const float* c, const float* bias, const void* dout,
                          void* d_sx, float* d_c, float* d_bias, int n_s, int d_inner, int n_t,

@@ -163,3 +163,15 @@ def test_decode_step_rejects_bad_arguments(L):
     # valid arguments reach the workspace check: K = 1 needs no conv state
     assert L.ssm_decode_step(*_decode_args(one, K=1, conv_state=None)) == WS
     assert L.ssm_decode_step(*_decode_args(one, ws=FAKE, ws_bytes=128)) == WS
+
+
+def test_conv_workspace_is_one_partial_per_launched_tile(L):
+    """d_conv <= 4 runs 256-token tiles, larger d_conv 64-token tiles: one fp32 partial of d_c
+    (K values) and d_bias per (sequence, tile, channel), rounded up to 256 bytes."""
+    def expect(n_s, d, L_, K, tile):
+        n = n_s * (-(-(L_ + K - 1) // tile)) * d * (K + 1) * 4
+        return -(-n // 256) * 256
+    assert binding.ssm_conv_workspace_size(16, 1024, 4096, 4) == expect(16, 1024, 4096, 4, 256)
+    assert binding.ssm_conv_workspace_size(2, 37, 130, 3) == expect(2, 37, 130, 3, 256)
+    assert binding.ssm_conv_workspace_size(2, 37, 130, 9) == expect(2, 37, 130, 9, 64)
+    assert binding.ssm_conv_workspace_size(0, 37, 130, 4) == 0
