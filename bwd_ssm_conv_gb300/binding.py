@@ -20,6 +20,7 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_WORKSPACE = 0, -1, -2, -3
 SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NONFINITE = -4, -5, -6
 SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE, SSM_A_LOG = 1, 2, 4, 8
+SSM_DEBUG_NO_WAIT = 16  # tests of the timeout path only (include/ssm.h)
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
             "ssm_scan_fwd", "ssm_scan_bwd", "ssm_decode_step", "ssm_scan_status",
@@ -185,13 +186,13 @@ class ScanShape:
 
 
 def scan_shape(x, dt, A, B, s0=None, chunk=256, softplus=False, check_finite=False,
-               state_rows=0, a_log=False) -> ScanShape:
+               state_rows=0, a_log=False, debug_flags=0) -> ScanShape:
     n_s, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     a_per_state = 1 if A.dim() == 2 else 0
     rows = state_rows if state_rows else (s0.shape[0] if s0 is not None else 0)
     flags = ((SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0) |
-             (SSM_A_LOG if a_log else 0))
+             (SSM_A_LOG if a_log else 0) | debug_flags)
     return ScanShape(n_s, L, H, P, N, G, a_per_state, rows, chunk, _io_of(x), flags)
 
 
@@ -265,10 +266,12 @@ GRAD_NAMES = ("d_s0", "d_x", "d_dt", "d_A", "d_B", "d_C", "d_D", "d_z", "d_dt_bi
 
 def ssm_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, s0=None, ids=None, ckpt=None,
                  d_state_out=None, chunk=256, softplus=False, check_finite=False, state_rows=0,
-                 want_ds0=True, ws=None, out=None, stream=None, a_log=False):
+                 want_ds0=True, ws=None, out=None, stream=None, a_log=False, debug_flags=0):
     """Returns a dict keyed by GRAD_NAMES (None where not requested / not applicable).
-    ``a_log``: A holds A_log and d_A is dL/dA_log."""
-    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
+    ``a_log``: A holds A_log and d_A is dL/dA_log.  ``debug_flags``: SSM_DEBUG_NO_WAIT (tests
+    of the timeout path only)."""
+    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log,
+                    debug_flags)
     io = x.dtype
     dev = x.device
     if out is None:

@@ -21,6 +21,7 @@ struct ScanProblem {
   int a_per_state, softplus, check_finite;
   int state_rows, chunk, n_chunks;
   int io;
+  int debug_flags;  // kDebugNoWait: cross-block waits give up at once (tests of the timeout path)
   const float* s0;
   const int* ids;
   const void* x;
@@ -33,6 +34,8 @@ struct ScanProblem {
   const float* dt_bias;
   int* status;  // device status word
 };
+
+constexpr int kDebugNoWait = 1;
 
 // Forward.  y may be NULL (states / checkpoints only), state_out may be NULL, ckpt may be NULL.
 // launch_scan_fwd takes a TMA-staged path when one applies: scan_fwd_tma.cu (head_dim 1) or

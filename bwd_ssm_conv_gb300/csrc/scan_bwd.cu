@@ -183,7 +183,10 @@ scan_bwd_kernel(const BwdArgs a) {
           dD_acc = fmaf(gy, xs[i], dD_acc);
           if (l.sg == 0 && l.valid) {
             st((IO*)a.g.d_x + tok * p.HP + l.ch, dxv);
-            if (z && a.g.d_z) st((IO*)a.g.d_z + tok * p.HP + l.ch, dyv * ypre * silu_gradf_(zv));
+            const float dzv = z ? dyv * ypre * silu_gradf_(zv) : 0.0f;
+            if (p.check_finite && !(isfinite(dxv) && isfinite(ddl) && isfinite(dzv)))
+              record_status(p.status, SSM_ERR_NONFINITE);
+            if (z && a.g.d_z) st((IO*)a.g.d_z + tok * p.HP + l.ch, dzv);
             if (p.P == 1) st((IO*)a.g.d_dt + tok * p.H + l.h, ddt);
             else a.ddt_part[tok * p.HP + l.ch] = ddl;
             dtb_acc += ddt;
@@ -432,14 +435,17 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
     S = base >= kBwdHeadsBlocksPerSM * num_sms
             ? 1 : (kBwdHeadsBlocksPerSM * num_sms + base - 1) / base;
   } else {
-    const long base_threads = (long)p.ns * p.G * q.bpg * kScanThreads;
+    q.tma_tt = bwd_tma_tile(p, q.chunk_b, q.gc);
+    // the TMA path's blocks hold more channels (fewer, longer chains)
+    const long blocks = q.tma_tt ? (long)p.ns * p.G * (q.gc / bwd_tma_channels_per_block())
+                                 : (long)p.ns * p.G * q.bpg;
+    const long base_threads = blocks * kScanThreads;
     const long target = (long)num_sms * kBwdTargetThreadsPerSM;
     S = base_threads >= (long)num_sms * kBwdNoSplitThreadsPerSM
             ? 1 : (target + base_threads - 1) / base_threads;
   }
   if (S > q.nch_b) S = q.nch_b;
   if (S < 1) S = 1;
-  q.tma_tt = q.heads ? 0 : bwd_tma_tile(p, q.chunk_b, q.tpc, q.gc);
   // Without time segments the (sequence, channel block) chains alone fill the GPU, but as whole
   // launches they quantise into waves (e.g. 768 chains on 456 resident blocks = 1.68 waves).
   // The TMA path then runs persistent blocks over (chain, chunk) units instead: every chunk
@@ -449,8 +455,8 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   // time; time segments keep every block busy but add a local adjoint pass, about 1.37x the
   // work (measured: 2 segments on 16 x 2048 x 1536 bf16).  So the persistent mode is also taken
   // when the chains fill at least 3/4 of the resident blocks, though not 512 threads per SM.
-  const long chains = (long)p.ns * p.G * q.bpg;
-  const long resident = (long)num_sms * kBwdPersistBlocksPerSM;
+  const long chains = q.tma_tt ? (long)p.ns * p.G * (q.gc / bwd_tma_channels_per_block()) : 0;
+  const long resident = (long)num_sms * kBwdTmaBlocksPerSM;
   q.persist = q.tma_tt && q.nch_b >= 2 && (S == 1 || 4 * chains >= 3 * resident);
   if (q.persist) S = q.nch_b;
   q.seg_chunks = (int)((q.nch_b + S - 1) / S);
@@ -477,10 +483,10 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.off_ddt = take(p.P > 1 ? F * (size_t)p.ns * p.L * p.HP : 0);
   q.off_dh0 = take(F * (size_t)p.ns * p.HP * p.N);
   if (q.tma_tt) {
-    const size_t units = (size_t)p.G * q.bpg * q.S * p.ns;
-    const size_t slots = (size_t)num_sms * kBwdPersistBlocksPerSM;
+    const size_t units = (size_t)chains * q.S;
+    const size_t slots = (size_t)num_sms * kBwdTmaBlocksPerSM;
     const size_t blocks = q.persist && slots < units ? slots : units;  // one per resident block
-    q.off_bnd = take(sizeof(float4) * blocks * (q.chunk_b / kTsubTma) * kScanThreads);
+    q.off_bnd = take(bwd_tma_scratch_bytes(q, blocks));
     if (q.persist) q.off_queue = take(sizeof(int) * (1 + units));  // counter, then unit flags
   }
   if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));
@@ -501,11 +507,12 @@ static int blocks_for(long total) {
 }
 
 template <typename IO, bool SCALAR_A, bool FULL>
-static cudaError_t launch_bwd_t(const BwdArgs& a, const BwdPlan& q, char* w, cudaStream_t st) {
+static cudaError_t launch_bwd_t(BwdArgs a, const BwdPlan& q, char* w, cudaStream_t st) {
   const ScanProblem& p = a.p;
   // the persistent TMA path needs no local adjoint pass; if its pointers do not allow TMA, the
   // general kernels take the same segments with one
-  const bool persist = q.persist && bwd_tma_ready(a, q);
+  const bool tma = bwd_tma_ready(a, q);
+  const bool persist = q.persist && tma;
   if (a.S > 1 && !persist) {
     cudaError_t e = q.tma_tt ? launch_bwd_tma_local(a, q, w, st) : cudaErrorNotSupported;
     if (e == cudaErrorNotSupported) {
@@ -523,7 +530,13 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const BwdPlan& q, char* w, cud
       reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
     return cudaGetLastError();
   }
-  cudaError_t e = q.tma_tt ? launch_bwd_tma_main(a, q, w, st) : cudaErrorNotSupported;
+  cudaError_t e = cudaErrorNotSupported;
+  if (tma) {
+    BwdArgs at = a;
+    at.bpg = a.gc / bwd_tma_channels_per_block();  // its dB/dC partials are per block
+    e = launch_bwd_tma_main(at, q, w, st);
+    if (e == cudaSuccess) a.bpg = at.bpg;
+  }
   if (e == cudaErrorNotSupported) {
     auto kern = scan_bwd_kernel<IO, SCALAR_A, FULL>;
     if (q.smem > 48 * 1024) {

@@ -9,7 +9,6 @@ namespace ssm {
 
 constexpr int kBwdNS = 4;          // states per thread
 constexpr int kTsub = 8;           // tokens of state history held in registers
-constexpr int kTsubTma = 4;        // the same for the TMA-staged Mamba-1 kernel
 constexpr int kMaxBwdChunk = 512;  // larger checkpoint intervals are re-checkpointed at 256
 constexpr int kDefaultChunk = 256;
 
@@ -94,8 +93,9 @@ struct BwdPlan {
   size_t off_fwd, fwd_bytes, off_ckpt, off_dhloc, off_segend, off_sumd, off_part_bc, off_dA,
       off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, off_queue, bytes, smem;
 };
-// Resident blocks per SM the persistent path is sized for (the kernel's launch bound).
-constexpr int kBwdPersistBlocksPerSM = 4;
+// Resident blocks per SM the TMA-staged backward is built for (its launch bound); the
+// persistent path and its scratch are sized by it.
+constexpr int kBwdTmaBlocksPerSM = 4;
 
 // Mamba-2-form backward (scan_bwd_heads.cu): one A per head, head_dim % 32 == 0, d_state 128.
 bool bwd_heads_applies(const ScanProblem& p, int chunk_b);
@@ -105,7 +105,12 @@ cudaError_t launch_bwd_heads(const BwdArgs& a, float* scratch, cudaStream_t st);
 
 // TMA-staged backward kernels (scan_bwd_tma.cu), Mamba-1 layout with d_state 16.
 // bwd_tma_tile: the tile size this shape would use, 0 if the path cannot take it.
-int bwd_tma_tile(const ScanProblem& p, int chunk_b, int tpc, int gc);
+int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc);
+// Channels per block of the TMA-staged main kernel (its per-block dB/dC partials are per
+// this many channels).
+int bwd_tma_channels_per_block();
+// Scratch of the TMA-staged main kernel for `blocks` blocks.
+size_t bwd_tma_scratch_bytes(const BwdPlan& q, size_t blocks);
 // Both return cudaErrorNotSupported, launching nothing, when the pointers do not allow the
 // path; the caller then runs the general kernels.
 cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st);

@@ -408,8 +408,12 @@ scan_bwd_heads_kernel(const BhArgs A) {
         const float sB = S.q[i][c][0], yp = S.q[i][c][1], xv = S.x[i][c], gy = S.gy[i][c];
         const float Dv = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
         const long off = (tok0 + i) * p.HP + ch0 + c;
-        st(reinterpret_cast<IO*>(a.g.d_x) + off, fmaf(gy, Dv, S.tc[i][1] * sB));
-        if (p.z && a.g.d_z) st(reinterpret_cast<IO*>(a.g.d_z) + off, S.dyg[i][c] * fmaf(Dv, xv, yp));
+        const float dxv = fmaf(gy, Dv, S.tc[i][1] * sB);
+        const float dzv = p.z ? S.dyg[i][c] * fmaf(Dv, xv, yp) : 0.0f;
+        if (p.check_finite && !(isfinite(dxv) && isfinite(dzv)))
+          record_status(p.status, SSM_ERR_NONFINITE);
+        st(reinterpret_cast<IO*>(a.g.d_x) + off, dxv);
+        if (p.z && a.g.d_z) st(reinterpret_cast<IO*>(a.g.d_z) + off, dzv);
         dD_acc = fmaf(gy, xv, dD_acc);
       }
       for (int i = warp; i < cnt; i += kBhWarps) {

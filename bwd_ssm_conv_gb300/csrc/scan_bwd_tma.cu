@@ -26,7 +26,8 @@
 namespace ssm {
 
 constexpr int kBwdStages = 2;
-constexpr int kBwdTile = 16;                  // tokens per staged tile (two sub-chunks)
+constexpr int kBwdTile = 16;                  // tokens per staged tile (four sub-chunks)
+constexpr int kTsubTma = 4;                   // tokens of state history held in registers
 constexpr int kCB = kScanThreads / 4;         // channels per block
 constexpr int kWarps = kScanThreads / 32;
 
@@ -41,14 +42,15 @@ struct BwdTma {
   int* counter;
   int* flags;
   int units, chains, gx;
+  uint32_t flag_spin;  // polls of a unit flag before the wait gives up
 };
 
-constexpr uint32_t kFlagSpin = 1u << 22;  // polls of a unit flag before the wait gives up
+constexpr uint32_t kFlagSpin = 1u << 22;
 
 // Waits (bounded) until another block has published *flag; gives up at once when any block has
 // recorded an error in the status word, so that one failure cannot chain into long waits.
-__device__ __forceinline__ bool wait_unit_flag(const int* flag, const int* status) {
-  for (uint32_t i = 0; i < kFlagSpin; i++) {
+__device__ __forceinline__ bool wait_unit_flag(const int* flag, const int* status, uint32_t spin) {
+  for (uint32_t i = 0; i < spin; i++) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
     if (v) return true;
@@ -62,12 +64,16 @@ __device__ __forceinline__ void publish_unit_flag(int* flag) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
 }
 
-int bwd_tma_tile(const ScanProblem& p, int chunk_b, int tpc, int gc) {
+int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc) {
   const int io = p.io == SSM_BF16 ? 2 : 4;
-  if (p.P == 1 && p.a_per_state && p.N == 16 && tpc == 4 && (p.HP * io) % 16 == 0 &&
-      gc % kCB == 0 && chunk_b % kBwdTile == 0)
+  if (p.P == 1 && p.a_per_state && p.N == 16 && (p.HP * io) % 16 == 0 && gc % kCB == 0 &&
+      chunk_b % kBwdTile == 0)
     return kBwdTile;
   return 0;
+}
+int bwd_tma_channels_per_block() { return kCB; }
+size_t bwd_tma_scratch_bytes(const BwdPlan& q, size_t blocks) {
+  return sizeof(float4) * blocks * (size_t)(q.chunk_b / kTsubTma) * kScanThreads;
 }
 
 template <typename IO>
@@ -169,7 +175,7 @@ __device__ __forceinline__ f2_t reduce_bc_warp(f2_t dB01, f2_t dB23, f2_t dC01, 
 // taken from the queue `chains` units earlier by a running block.  Otherwise one block = one
 // (sequence, channel block, segment) of whole chunks, as given by the grid.
 template <typename IO, bool PERSIST>
-__global__ void __launch_bounds__(kScanThreads, kBwdPersistBlocksPerSM)
+__global__ void __launch_bounds__(kScanThreads, kBwdTmaBlocksPerSM)
 scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;
   constexpr int TT = kBwdTile, CB = kCB, N = 16;
@@ -276,10 +282,21 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     // carry pass, or (persistent) from the unit of the next chunk once it has published it
     const bool from_next = a.S > 1 && s < a.S - 1;
     if (PERSIST && from_next) {
-      if (tid == 0 &&
-          !wait_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s, p.status))
-        record_status(p.status, SSM_ERR_TIMEOUT);
-      __syncthreads();
+      bool ok = true;
+      if (tid == 0) {
+        ok = wait_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s, p.status, m.flag_spin);
+        if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
+      }
+      // the flag's outcome reaches every thread; on a give-up the block waits (bounded) for its
+      // tile copies in flight and skips the rest of its work
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+          for (int j = qpos; j < issued; j++)
+            mbar_wait(&full[j % kBwdStages], (uint32_t)(j / kBwdStages) & 1u);
+          tma_store_wait_all();
+        }
+        return;
+      }
     }
     float cv[4], av[4];
 #pragma unroll
@@ -523,8 +540,11 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       const float D = sPar[c];
       const float ddl = fmaf(e4.x, sBt, sAwt);
       const float ddt = p.softplus ? ddl * e4.w : ddl;
-      sts_f(odx + idx, fmaf(e4.y, D, dl * sBt));
-      sts_f(odz + idx, e4.z * fmaf(D, e4.x, ypt));
+      const float dxv = fmaf(e4.y, D, dl * sBt), dzv = e4.z * fmaf(D, e4.x, ypt);
+      if (p.check_finite && !(isfinite(dxv) && isfinite(dzv) && isfinite(ddt)))
+        record_status(p.status, SSM_ERR_NONFINITE);
+      sts_f(odx + idx, dxv);
+      sts_f(odz + idx, dzv);
       sts_f(oddt + idx, ddt);
       dD_acc = fmaf(e4.y, e4.x, dD_acc);
       dtb_acc += ddt;
@@ -742,6 +762,7 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
   m->bytes_loc = (2 + (p.z ? 1 : 0)) * tile + row;
   m->bnd = w ? reinterpret_cast<float4*>(w + q.off_bnd) : nullptr;
+  m->flag_spin = (p.debug_flags & kDebugNoWait) ? 0u : kFlagSpin;
   return true;
 }
 
@@ -770,7 +791,7 @@ static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, 
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kScanThreads, m.smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorNotSupported;
-  if (per_sm > kBwdPersistBlocksPerSM) per_sm = kBwdPersistBlocksPerSM;  // the scratch is sized so
+  if (per_sm > kBwdTmaBlocksPerSM) per_sm = kBwdTmaBlocksPerSM;  // the scratch is sized so
   m.gx = p.G * a.bpg;
   m.chains = m.gx * p.ns;
   m.units = m.chains * a.nch_b;

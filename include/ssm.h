@@ -51,8 +51,12 @@
  * outside [0, state_rows), or a non-finite output when SSM_CHECK_FINITE is set) are
  * recorded in a status word inside the workspace; the offending element is skipped (an
  * out-of-range row reads as a zero state and receives no gradient), never read or written
- * out of bounds.  Read it with ssm_scan_status after the call.  No kernel of this library
- * waits on another block, so no call can hang.
+ * out of bounds.  Read it with ssm_scan_status after the call.
+ * Waits: a block waits only for its own tile copies and, in the persistent backward (see
+ * ssm_scan_bwd), for the block that computes the adjoint at the end of its chunk.  Both waits
+ * are bounded.  A wait that gives up records SSM_ERR_TIMEOUT; the block then waits (bounded)
+ * for its own copies in flight and skips the rest of its work, and every other block gives up
+ * at its next wait or unit once the status word is set.  No call can hang.
  */
 #ifndef SSM_GB300_H
 #define SSM_GB300_H
@@ -85,11 +89,15 @@ enum {
   SSM_CONV_SILU = 1u,    /* conv: apply SiLU after the convolution (+bias) */
   SSM_DT_SOFTPLUS = 2u,  /* scan: delta = softplus(dt + dt_bias) instead of delta = dt */
   SSM_CHECK_FINITE = 4u, /* scan: record SSM_ERR_NONFINITE in the status word on a non-finite output */
-  SSM_A_LOG = 8u         /* scan: the A argument holds A_log and the scan uses A = -exp(A_log)
+  SSM_A_LOG = 8u,        /* scan: the A argument holds A_log and the scan uses A = -exp(A_log)
                             (infotheory's mamba1 parameterisation); d_A returns dL/dA_log =
                             dL/dA * A.  The workspace grows by a buffer for A: the
                             *_workspace_size results include it; ssm_decode_step then needs
                             ws_bytes >= 256 + 4 * (elements of A) rounded up to 256. */
+  SSM_DEBUG_NO_WAIT = 16u /* scan, for tests of the error path only: every wait of a block on
+                            another block gives up at once, as if its bound had run out; the
+                            call then records SSM_ERR_TIMEOUT and its outputs are incomplete.
+                            Waits for this block's own copies keep their normal bound. */
 };
 
 /* Limits (checked on the host; SSM_ERR_UNSUPPORTED beyond them).  Every tensor must also
@@ -109,7 +117,7 @@ typedef struct {
   int state_rows;   /* rows of s0 / d_s0; 0 means n_seqs.  Without ids, must be >= n_seqs */
   int chunk;        /* checkpoint interval in tokens; 0 means 256 */
   int io;           /* ssm_dtype of the activations */
-  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG */
+  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG | SSM_DEBUG_NO_WAIT */
 } ssm_scan_desc;
 
 /* ---- causal depthwise conv1d (+bias, +SiLU) --------------------------------------------

@@ -5,7 +5,7 @@ import torch
 import oracle
 from bwd_ssm_conv_gb300 import binding
 from bwd_ssm_conv_gb300.workloads import make_inputs, random_conv_inputs, workload
-from gpu_util import assert_close, tol
+from gpu_util import assert_close, nan_like, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -29,13 +29,16 @@ def _run(n_s, d, L, K, io, bias, silu, seed):
     inp = random_conv_inputs(n_s, d, L, K, io=io, bias=bias, seed=seed)
     sx, c = inp["sx"].cuda(), inp["c"].cuda()
     bv = inp["bias"].cuda() if bias else None
-    out, cs = binding.ssm_conv_fwd(sx, c, bv, silu=silu, want_state=True)
+    # NaN-filled outputs: an element the kernels never write fails the check
+    out, cs = binding.ssm_conv_fwd(sx, c, bv, silu=silu, want_state=True,
+                                   out=nan_like(sx, (n_s, L, d)))
     ref, cs_ref = oracle.conv_fwd(inp["sx"], inp["c"], inp["bias"], silu=silu, want_state=True)
     assert_close("out", out, ref, tol(io, False))
     if K > 1:
         assert torch.equal(cs.cpu(), inp["sx"][:, :, -(K - 1):])
     d_sx, d_c, d_b = binding.ssm_conv_bwd(sx, c, inp["dout"].cuda(), bv, silu=silu,
-                                          want_bias_grad=True)
+                                          out=(nan_like(sx), nan_like(c),
+                                               nan_like(None, (d,), torch.float32)))
     r_sx, r_c, r_b = oracle.conv_bwd(inp["sx"], inp["c"], inp["dout"], bias=inp["bias"], silu=silu)
     assert_close("d_sx", d_sx, r_sx, tol(io, True))
     assert_close("d_c", d_c, r_c, tol(io, True))
@@ -63,11 +66,13 @@ def test_conv_full_workload(name):
     w = workload(name)
     inp = make_inputs(w)
     sx, c = inp["sx"].cuda(), inp["c"].cuda()
-    out = binding.ssm_conv_fwd(sx, c, None, silu=True)
+    out = binding.ssm_conv_fwd(sx, c, None, silu=True,
+                               out=nan_like(sx, (w.n_seqs, w.n_tok, w.channels)))
     ref = oracle.conv_fwd(inp["sx"], inp["c"], None, silu=True)
     assert_close("out", out, ref, tol(w.io, False))
     dout = inp["dy"].view(w.n_seqs, w.n_tok, w.channels)
-    d_sx, d_c, _ = binding.ssm_conv_bwd(sx, c, dout.cuda(), None, silu=True)
+    d_sx, d_c, _ = binding.ssm_conv_bwd(sx, c, dout.cuda(), None, silu=True,
+                                        out=(nan_like(sx), nan_like(c), None))
     r_sx, r_c, _ = oracle.conv_bwd(inp["sx"], inp["c"], dout, silu=True)
     assert_close("d_sx", d_sx, r_sx, tol(w.io, True))
     assert_close("d_c", d_c, r_c, tol(w.io, True))
@@ -98,9 +103,9 @@ def test_conv_bwd_offset_views(case):
     n_s, d, L, K = 2, 40, 300, 4
     inp = random_conv_inputs(n_s, d, L, K, io=io, bias=True, seed=17 + o_sx + o_dsx)
     sx, dout = _at(inp["sx"], o_sx), _at(inp["dout"], o_dout)
-    d_sx = _at(torch.zeros_like(inp["sx"]), o_dsx)
-    d_c = torch.empty_like(inp["c"]).cuda()
-    d_b = torch.empty(d, dtype=torch.float32, device="cuda")
+    d_sx = _at(torch.full_like(inp["sx"], float("nan")), o_dsx)
+    d_c = nan_like(inp["c"])
+    d_b = nan_like(None, (d,), torch.float32)
     binding.ssm_conv_bwd(sx, inp["c"].cuda(), dout, inp["bias"].cuda(), silu=True,
                          out=(d_sx, d_c, d_b))
     r_sx, r_c, r_b = oracle.conv_bwd(inp["sx"], inp["c"], inp["dout"], bias=inp["bias"], silu=True)

@@ -93,7 +93,8 @@ def test_fused_decode_step_matches_oracle(io, P, N, G, scalar_a, softplus):
         x_new.to(t_io).view(n_s, H, P).cuda(), cs_g, c.cuda(), sc["dt"][:, 0].contiguous().cuda(),
         sc["A"].cuda(), sc["B"][:, 0].contiguous().cuda(), sc["C"][:, 0].contiguous().cuda(),
         st_g, bias=bias.cuda(), D=sc["D"].cuda(), z=sc["z"][:, 0].contiguous().cuda(),
-        dt_bias=None if dt_bias is None else dt_bias.cuda(), ids=ids.cuda(), softplus=softplus)
+        dt_bias=None if dt_bias is None else dt_bias.cuda(), ids=ids.cuda(), softplus=softplus,
+        out=torch.full((n_s, H, P), float("nan"), dtype=t_io, device="cuda"))
     torch.cuda.synchronize()
     t = tol(io, grad=False)
     assert_close("y", y, np.asarray(yo).reshape(n_s, H, P), t)

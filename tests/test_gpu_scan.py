@@ -32,10 +32,14 @@ CASES = [
     ("single_token", (2, 1, 3, 1, 16, 1), "f32", False, 256, False, False),
     ("n128_mamba2", (1, 40, 2, 4, 128, 1), "f32", True, 16, False, False),
     # shapes that take the TMA-staged kernels (channels a multiple of 32, d_state 16)
+    # (the backward's TMA kernel takes groups of a multiple of 32 channels and chunks of a
+    # multiple of 16 tokens; a 24-token chunk runs its general kernels)
     ("tma_f32_ragged_multiseg", (2, 300, 64, 1, 16, 1), "f32", False, 64, False, False),
-    ("tma_bf16_softplus", (3, 520, 96, 1, 16, 1), "bf16", False, 128, True, False),
+    ("tma_bf16_softplus", (3, 520, 128, 1, 16, 1), "bf16", False, 128, True, False),
     ("tma_chunk24_tile8", (1, 200, 32, 1, 16, 1), "f32", False, 24, False, False),
     ("tma_groups", (2, 100, 64, 1, 16, 2), "bf16", False, 32, False, False),
+    ("tma_groups64_chunk48", (2, 200, 128, 1, 16, 2), "bf16", False, 48, False, False),
+    ("tma_f32_pieces", (2, 333, 64, 1, 16, 1), "f32", False, 208, True, False),
     # Mamba-2 form (one A per head) with several heads per channel block, two groups
     ("mamba2_f32_heads", (2, 200, 16, 8, 32, 2), "f32", True, 32, False, False),
     # ... bf16 with softplus(dt + dt_bias)
@@ -96,15 +100,17 @@ def test_scan_backward_parity(case):
     assert binding.ssm_scan_status(g["_ws"]) == 0
 
 
-# Enough (sequence, 32-channel block) chains to fill a 152-SM GPU without time segments (20 x 32
-# = 640): the backward then runs resident blocks over (chain, chunk) units, last chunk first,
-# each handing its chunk's start adjoint to the unit of the chunk before it.  Ragged last chunk.
-# 15 x 32 = 480 chains fill 3/4 of the 608 resident blocks but not 512 threads per SM: also
-# persistent, with some blocks waiting on the flag of a chunk still in progress.
+# Enough (sequence, 32-channel block) chains to fill a 152-SM GPU without time segments (40 x 32
+# = 1280 chains, 4 resident blocks per SM): the backward then runs resident blocks over (chain,
+# chunk) units, last chunk first, each handing its chunk's start adjoint to the unit of the
+# chunk before it.  Ragged last chunk.  22 x 32 = 704 chains fill 3/4 of the 608 resident
+# blocks but not all: also persistent, with some blocks waiting on the flag of a chunk still in
+# progress.
 PERSIST_CASES = [
-    ("persist_bf16", (20, 100, 1024, 1, 16, 1), "bf16", 32, False),
-    ("persist_f32_softplus", (20, 72, 1024, 1, 16, 1), "f32", 16, True),
-    ("persist_partial_bf16", (15, 100, 1024, 1, 16, 1), "bf16", 32, False),
+    ("persist_bf16", (40, 100, 1024, 1, 16, 1), "bf16", 32, False),
+    ("persist_f32_softplus", (24, 72, 1024, 1, 16, 1), "f32", 16, True),
+    ("persist_partial_bf16", (22, 100, 1024, 1, 16, 1), "bf16", 32, False),
+    ("persist_pieces_bf16", (24, 300, 1024, 1, 16, 1), "bf16", 144, False),
 ]
 
 
@@ -129,7 +135,7 @@ def test_persistent_backward_parity_and_determinism(case):
 def test_persistent_backward_ids_without_final_state_gradient():
     """The persistent path seeds the last chunk with zero when no final-state gradient is given
     and sums d_s0 over the sequences that share an initial-state row."""
-    ns, L, H = 20, 80, 1024
+    ns, L, H = 24, 80, 1024
     inp = _inputs((ns, L, H, 1, 16, 1), "bf16", False, False, seed=41)
     rows = 3
     inp["s0"] = 0.5 * torch.randn(rows, H, 1, 16)
