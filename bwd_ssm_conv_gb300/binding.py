@@ -23,8 +23,9 @@ SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE, SSM_A_LOG = 1, 2, 4, 8
 SSM_DEBUG_NO_WAIT = 16  # tests of the timeout path only (include/ssm.h)
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
-            "ssm_scan_fwd", "ssm_scan_bwd", "ssm_decode_step", "ssm_scan_status",
-            "ssm_status_string", "ssm_abi_version", "ssm_kernel_launches")
+            "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv_scan_workspace_size", "ssm_conv_scan_fwd",
+            "ssm_conv_scan_bwd", "ssm_decode_step", "ssm_scan_status", "ssm_status_string",
+            "ssm_abi_version", "ssm_kernel_launches")
 
 
 class SsmError(RuntimeError):
@@ -64,6 +65,12 @@ def lib():
         L.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanDesc)] + [_vp] * 23 + [_sz, _vp]
         L.ssm_decode_step.argtypes = ([ctypes.POINTER(ScanDesc), _i, _u] + [_vp] * 15 +
                                       [_sz, _vp])
+        L.ssm_conv_scan_workspace_size.argtypes = [ctypes.POINTER(ScanDesc), _i, _i]
+        L.ssm_conv_scan_workspace_size.restype = _sz
+        L.ssm_conv_scan_fwd.argtypes = ([ctypes.POINTER(ScanDesc), _i, _u] + [_vp] * 16 +
+                                        [_sz, _vp])
+        L.ssm_conv_scan_bwd.argtypes = ([ctypes.POINTER(ScanDesc), _i, _u] + [_vp] * 27 +
+                                        [_sz, _vp])
         L.ssm_scan_status.argtypes = [_vp, ctypes.POINTER(_i), _vp]
         L.ssm_status_string.argtypes = [_i]
         L.ssm_status_string.restype = ctypes.c_char_p
@@ -299,6 +306,98 @@ def ssm_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, s0=None, ids=
         _ptr(g["d_D"], f32, "d_D"), _ptr(g["d_z"], io, "d_z"), _ptr(g["d_dt_bias"], f32, "d_dt_bias"),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("ssm_scan_bwd", rc)
+    g["_ws"] = ws
+    return g
+
+
+# ---- conv1d + scan in one call ------------------------------------------------------------
+
+def conv_scan_shape(sx, c, dt, A, B, s0=None, chunk=256, softplus=False, check_finite=False,
+                    state_rows=0, a_log=False) -> ScanShape:
+    """The scan descriptor of a fused call: d_inner = sx.shape[1] channels, head_dim 1."""
+    n_s, d, w = sx.shape
+    L = w - c.shape[1] + 1
+    G, N = B.shape[2], B.shape[3]
+    rows = state_rows if state_rows else (s0.shape[0] if s0 is not None else 0)
+    flags = ((SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0) |
+             (SSM_A_LOG if a_log else 0))
+    return ScanShape(n_s, L, d, 1, N, G, 1 if A.dim() == 2 else 0, rows, chunk, _io_of(sx), flags)
+
+
+def ssm_conv_scan_workspace_size(shape: ScanShape, d_conv: int, backward: bool) -> int:
+    d = shape.desc()
+    return int(lib().ssm_conv_scan_workspace_size(ctypes.byref(d), d_conv, 1 if backward else 0))
+
+
+def ssm_conv_scan_fwd(sx, c, dt, A, B, C, bias=None, silu=True, D=None, z=None, dt_bias=None,
+                      s0=None, ids=None, chunk=256, softplus=False, check_finite=False,
+                      want_ckpt=True, state_rows=0, ws=None, out=None, stream=None, a_log=False):
+    """conv1d(+bias, SiLU) of sx fused into the scan forward; returns (y, state_out, ckpt) with
+    y [n_s][L][d_inner][1].  sx [n_s][d_inner][K-1+L], c [d_inner][K]; the rest as in
+    ssm_scan_fwd with head_dim 1."""
+    sh = conv_scan_shape(sx, c, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
+    io, dev, K = sx.dtype, sx.device, c.shape[1]
+    if out is None:
+        y = torch.empty(sh.n_seqs, sh.n_tok, sh.n_head, 1, dtype=io, device=dev)
+        st = torch.empty(sh.n_seqs, sh.n_head, 1, sh.d_state, dtype=torch.float32, device=dev)
+        ck = (torch.empty(sh.n_seqs, sh.n_chunks, sh.n_head, 1, sh.d_state, dtype=torch.float32,
+                          device=dev) if want_ckpt else None)
+    else:
+        y, st, ck = out
+    ws = _workspace(ssm_conv_scan_workspace_size(sh, K, False), dev, ws)
+    d = sh.desc()
+    f32 = torch.float32
+    rc = lib().ssm_conv_scan_fwd(
+        ctypes.byref(d), K, SSM_CONV_SILU if silu else 0, _ptr(sx, io, "sx"), _ptr(c, f32, "c"),
+        _ptr(bias, f32, "bias"), _ptr(s0, f32, "s0"), _ptr(ids, torch.int32, "ids"),
+        _ptr(dt, io, "dt"), _ptr(A, f32, "A"), _ptr(B, io, "B"), _ptr(C, io, "C"),
+        _ptr(D, f32, "D"), _ptr(z, io, "z"), _ptr(dt_bias, f32, "dt_bias"), _ptr(y, io, "y"),
+        _ptr(st, f32, "state_out"), _ptr(ck, f32, "ckpt"), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("ssm_conv_scan_fwd", rc)
+    return y, st, ck
+
+
+CONV_SCAN_GRAD_NAMES = ("d_s0", "d_sx", "d_c", "d_bias", "d_dt", "d_A", "d_B", "d_C", "d_D",
+                        "d_z", "d_dt_bias")
+
+
+def ssm_conv_scan_bwd(sx, c, dt, A, B, C, dy, bias=None, silu=True, D=None, z=None,
+                      dt_bias=None, s0=None, ids=None, ckpt=None, d_state_out=None, chunk=256,
+                      softplus=False, check_finite=False, state_rows=0, want_ds0=True,
+                      want_bias_grad=None, ws=None, out=None, stream=None, a_log=False):
+    """Backward of ssm_conv_scan_fwd; returns a dict keyed by CONV_SCAN_GRAD_NAMES."""
+    sh = conv_scan_shape(sx, c, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
+    io, dev, K = sx.dtype, sx.device, c.shape[1]
+    f32 = torch.float32
+    if out is None:
+        rows = sh.state_rows if sh.state_rows else sh.n_seqs
+        want_b = want_bias_grad if want_bias_grad is not None else bias is not None
+        g = dict(
+            d_s0=(torch.empty(rows, sh.n_head, 1, sh.d_state, dtype=f32, device=dev)
+                  if want_ds0 else None),
+            d_sx=torch.empty_like(sx), d_c=torch.empty_like(c),
+            d_bias=torch.empty(sh.n_head, dtype=f32, device=dev) if want_b else None,
+            d_dt=torch.empty_like(dt), d_A=torch.empty_like(A), d_B=torch.empty_like(B),
+            d_C=torch.empty_like(C), d_D=torch.empty_like(D) if D is not None else None,
+            d_z=torch.empty_like(z) if z is not None else None,
+            d_dt_bias=torch.empty_like(dt_bias) if (dt_bias is not None and softplus) else None)
+    else:
+        g = out
+    ws = _workspace(ssm_conv_scan_workspace_size(sh, K, True), dev, ws)
+    d = sh.desc()
+    rc = lib().ssm_conv_scan_bwd(
+        ctypes.byref(d), K, SSM_CONV_SILU if silu else 0, _ptr(sx, io, "sx"), _ptr(c, f32, "c"),
+        _ptr(bias, f32, "bias"), _ptr(s0, f32, "s0"), _ptr(ids, torch.int32, "ids"),
+        _ptr(dt, io, "dt"), _ptr(A, f32, "A"), _ptr(B, io, "B"), _ptr(C, io, "C"),
+        _ptr(D, f32, "D"), _ptr(z, io, "z"), _ptr(dt_bias, f32, "dt_bias"),
+        _ptr(ckpt, f32, "ckpt"), _ptr(dy, io, "dy"), _ptr(d_state_out, f32, "d_state_out"),
+        _ptr(g["d_s0"], f32, "d_s0"), _ptr(g["d_sx"], io, "d_sx"), _ptr(g["d_c"], f32, "d_c"),
+        _ptr(g["d_bias"], f32, "d_bias"), _ptr(g["d_dt"], io, "d_dt"), _ptr(g["d_A"], f32, "d_A"),
+        _ptr(g["d_B"], io, "d_B"), _ptr(g["d_C"], io, "d_C"), _ptr(g["d_D"], f32, "d_D"),
+        _ptr(g["d_z"], io, "d_z"), _ptr(g["d_dt_bias"], f32, "d_dt_bias"), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("ssm_conv_scan_bwd", rc)
     g["_ws"] = ws
     return g
 

@@ -236,6 +236,154 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// ---- fused conv1d + scan --------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+// Workspace of the fused calls: the scan's own scratch (with the A_LOG buffer), then the conv
+// output x (used only when the fused forward kernel does not apply, and by the backward), then
+// (backward) dL/dx and the conv backward's partial sums.
+struct ConvScanWs {
+  size_t scan, x, dx, conv, bytes;
+};
+
+ConvScanWs conv_scan_ws(const ssm_scan_desc* d, const ScanProblem& p, int K, int backward,
+                        int sms) {
+  ConvScanWs w{};
+  const size_t base = backward ? ssm::scan_bwd_ws_bytes(p, sms) : ssm::scan_fwd_ws_bytes(p, sms);
+  w.scan = a_log_of(d) ? ssm::align_up(base, 256) + a_bytes(p) : base;
+  const size_t xb = (size_t)p.ns * p.L * p.HP * io_size(p.io);
+  w.x = ssm::align_up(w.scan, 256);
+  size_t off = ssm::align_up(w.x + xb, 256);
+  if (backward) {
+    w.dx = off;
+    off = ssm::align_up(w.dx + xb, 256);
+    w.conv = off;
+    off = ssm::align_up(w.conv + ssm::conv_bwd_ws_bytes(p.ns, p.HP, p.L, K), 256);
+  }
+  w.bytes = off;
+  return w;
+}
+
+int conv_scan_check(const ssm_scan_desc* d, int K, unsigned conv_flags, const void* sx,
+                    const float* c, const float* cb, int backward, ScanProblem* p) {
+  int rc = scan_problem(d, backward, p);
+  if (rc != SSM_OK) return rc;
+  if (K <= 0 || conv_flags & ~(unsigned)SSM_CONV_SILU) return SSM_ERR_INVALID_ARG;
+  if (K > SSM_MAX_D_CONV) return SSM_ERR_UNSUPPORTED;
+  rc = conv_check(sx, c, sx, p->ns, p->HP, p->L, K, p->io);
+  if (rc != SSM_OK) return rc;
+  if (cb && !aligned(cb, 4)) return SSM_ERR_INVALID_ARG;
+  return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_conv_scan_workspace_size(const ssm_scan_desc* desc, int d_conv, int backward) {
+  ScanProblem p;
+  if (scan_problem(desc, backward, &p) != SSM_OK) return 0;
+  if (d_conv <= 0 || d_conv > SSM_MAX_D_CONV) return 0;
+  const int sms = num_sms_current();
+  if (sms <= 0) return 0;
+  return conv_scan_ws(desc, p, d_conv, backward, sms).bytes;
+}
+
+int ssm_conv_scan_fwd(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags, const void* sx,
+                      const float* conv_w, const float* conv_b, const float* s0,
+                      const int32_t* ids, const void* dt, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* dt_bias,
+                      void* y, float* state_out, float* ckpt, void* ws, size_t ws_bytes,
+                      void* stream) {
+  ScanProblem p;
+  int rc = conv_scan_check(desc, d_conv, conv_flags, sx, conv_w, conv_b, 0, &p);
+  if (rc != SSM_OK) return rc;
+  if (!dt || !A || !B || !C || !y || !state_out) return SSM_ERR_INVALID_ARG;
+  const int io = p.io;
+  if (!check_act(dt, io) || !check_act(B, io) || !check_act(C, io) || !check_act(y, io) ||
+      (z && !check_act(z, io)) || !aligned(A, 4) || !aligned(state_out, 4) ||
+      (s0 && !aligned(s0, 4)) || (ids && !aligned(ids, 4)) || (D && !aligned(D, 4)) ||
+      (dt_bias && !aligned(dt_bias, 4)) || (ckpt && !aligned(ckpt, 4)))
+    return SSM_ERR_INVALID_ARG;
+  if (!ids && s0 && p.state_rows < p.ns) return SSM_ERR_INVALID_ARG;
+  const int sms = num_sms_current();
+  if (sms <= 0) return SSM_ERR_CUDA;
+  const ConvScanWs w = conv_scan_ws(desc, p, d_conv, 0, sms);
+  if (!ws || ws_bytes < w.bytes || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
+  p.s0 = s0; p.ids = ids; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.dt_bias = dt_bias;
+  p.status = (int*)ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((rc = stage_a(desc, &p, ws, ssm::scan_fwd_ws_bytes(p, sms), st)) != SSM_OK) return rc;
+  const int silu = (conv_flags & SSM_CONV_SILU) ? 1 : 0;
+  // the fused kernel: x is computed from sx inside the scan and never stored
+  ScanProblem pf = p;
+  pf.sx = sx; pf.conv_w = conv_w; pf.conv_b = conv_b; pf.d_conv = d_conv; pf.conv_silu = silu;
+  cudaError_t e = ssm::launch_scan_fwd_tma(pf, y, state_out, ckpt, ws, sms, st);
+  if (e == cudaErrorNotSupported) {  // otherwise the conv into the workspace, then the scan
+    void* x = (char*)ws + w.x;
+    e = ssm::launch_conv_fwd(sx, conv_w, conv_b, x, nullptr, p.ns, p.HP, p.L, d_conv, io, silu, st);
+    p.x = x;
+    if (e == cudaSuccess) e = ssm::launch_scan_fwd(p, y, state_out, ckpt, ws, sms, st);
+  }
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_conv_scan_bwd(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags, const void* sx,
+                      const float* conv_w, const float* conv_b, const float* s0,
+                      const int32_t* ids, const void* dt, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* dt_bias,
+                      const float* ckpt, const void* dy, const float* d_state_out, float* d_s0,
+                      void* d_sx, float* d_conv_w, float* d_conv_b, void* d_dt, float* d_A,
+                      void* d_B, void* d_C, float* d_D, void* d_z, float* d_dt_bias, void* ws,
+                      size_t ws_bytes, void* stream) {
+  ScanProblem p;
+  int rc = conv_scan_check(desc, d_conv, conv_flags, sx, conv_w, conv_b, 1, &p);
+  if (rc != SSM_OK) return rc;
+  if (!dt || !A || !B || !C || !dy || !d_sx || !d_conv_w || !d_dt || !d_A || !d_B || !d_C)
+    return SSM_ERR_INVALID_ARG;
+  if ((d_D && !D) || (d_z && !z) || (d_dt_bias && !p.softplus)) return SSM_ERR_INVALID_ARG;
+  const int io = p.io;
+  if (!check_act(dt, io) || !check_act(B, io) || !check_act(C, io) || !check_act(dy, io) ||
+      !check_act(d_sx, io) || !check_act(d_dt, io) || !check_act(d_B, io) ||
+      !check_act(d_C, io) || (z && !check_act(z, io)) || (d_z && !check_act(d_z, io)) ||
+      !aligned(A, 4) || !aligned(d_A, 4) || !aligned(d_conv_w, 4) ||
+      (d_conv_b && !aligned(d_conv_b, 4)) || (s0 && !aligned(s0, 4)) ||
+      (ids && !aligned(ids, 4)) || (D && !aligned(D, 4)) || (d_D && !aligned(d_D, 4)) ||
+      (dt_bias && !aligned(dt_bias, 4)) || (d_dt_bias && !aligned(d_dt_bias, 4)) ||
+      (ckpt && !aligned(ckpt, 4)) || (d_state_out && !aligned(d_state_out, 4)) ||
+      (d_s0 && !aligned(d_s0, 4)))
+    return SSM_ERR_INVALID_ARG;
+  if (!ids && (s0 || d_s0) && p.state_rows < p.ns) return SSM_ERR_INVALID_ARG;
+  const int sms = num_sms_current();
+  if (sms <= 0) return SSM_ERR_CUDA;
+  const ConvScanWs w = conv_scan_ws(desc, p, d_conv, 1, sms);
+  if (!ws || ws_bytes < w.bytes || !aligned(ws, 256)) return SSM_ERR_WORKSPACE;
+  p.s0 = s0; p.ids = ids; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.dt_bias = dt_bias;
+  p.status = (int*)ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((rc = stage_a(desc, &p, ws, ssm::scan_bwd_ws_bytes(p, sms), st)) != SSM_OK) return rc;
+  const int silu = (conv_flags & SSM_CONV_SILU) ? 1 : 0;
+  // x recomputed from sx, the scan's backward into dL/dx, then the conv's backward
+  void* x = (char*)ws + w.x;
+  void* dx = (char*)ws + w.dx;
+  cudaError_t e = ssm::launch_conv_fwd(sx, conv_w, conv_b, x, nullptr, p.ns, p.HP, p.L, d_conv,
+                                       io, silu, st);
+  p.x = x;
+  ScanGrads g{dy, d_state_out, d_s0, dx, d_dt, d_A, d_B, d_C, d_D, d_z, d_dt_bias};
+  if (e == cudaSuccess) e = ssm::launch_scan_bwd(p, ckpt, g, ws, sms, st);
+  if (e == cudaSuccess && a_log_of(desc)) e = ssm::launch_scale_dA(d_A, p.A, a_count(p), st);
+  if (e == cudaSuccess)
+    e = ssm::launch_conv_bwd(sx, conv_w, conv_b, dx, d_sx, d_conv_w, d_conv_b, (char*)ws + w.conv,
+                             p.ns, p.HP, p.L, d_conv, io, silu, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 int ssm_decode_step(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags,
                     const int32_t* ids, const void* x_new, void* conv_state, const float* c,
                     const float* bias, const void* dt, const float* A, const void* B,

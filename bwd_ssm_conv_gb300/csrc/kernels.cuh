@@ -33,6 +33,13 @@ struct ScanProblem {
   const void* z;
   const float* dt_bias;
   int* status;  // device status word
+  // Fused conv1d prelude (ssm_conv_scan_fwd): when sx is set, x is not read from memory but
+  // computed as act(sum_k sx[b][ch][t+k] conv_w[ch][k] + conv_b[ch]) (act = SiLU when conv_silu)
+  // and rounded to the io type, as ssm_conv_fwd would store it.  sx is [ns][HP][L + d_conv - 1].
+  const void* sx;
+  const float* conv_w;
+  const float* conv_b;
+  int d_conv, conv_silu;
 };
 
 constexpr int kDebugNoWait = 1;

@@ -5,14 +5,14 @@
 
 namespace ssm {
 
-#define SSM_EXTERN_F32(NS, TPC, SA, THR) \
-  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR>(FwdTmaArgs&, size_t, cudaStream_t);
+#define SSM_EXTERN_F32(NS, TPC, SA, THR, CK) \
+  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, cudaStream_t);
 SSM_FWD_TMA_VARIANTS(SSM_EXTERN_F32)
 #undef SSM_EXTERN_F32
 
-static bool instantiated(int ns, int tpc, bool scalar_a, int thr = 128) {
-#define SSM_MATCH(NS, TPC, SA, THR) \
-  if (ns == NS && tpc == TPC && scalar_a == SA && thr == THR) return true;
+static bool instantiated(int ns, int tpc, bool scalar_a, int ck, int thr = 128) {
+#define SSM_MATCH(NS, TPC, SA, THR, CK) \
+  if (ns == NS && tpc == TPC && scalar_a == SA && thr == THR && ck == CK) return true;
   SSM_FWD_TMA_VARIANTS(SSM_MATCH)
 #undef SSM_MATCH
   return false;
@@ -35,11 +35,14 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   if (p.P != 1 || p.N % 4 != 0 || p.N > 256 || (p.N * io) % 16 != 0 || (p.HP * io) % 16 != 0 ||
       p.chunk % kFwdTile != 0)
     return q;
+  // the fused conv prelude comes with its own instances
+  const int ck = p.sx ? p.d_conv : 0;
+  if (p.sx && (ck < 1 || ck > 4)) return q;
   // largest states-per-thread that still gives four blocks per SM without time segments
   // (the recurrence is latency-bound: more warps per SM beat fewer instructions per state)
   int ns = 0;
   for (int cand = 16; cand >= 4; cand >>= 1) {
-    if (p.N % cand != 0 || !instantiated(cand, p.N / cand, sa)) continue;
+    if (p.N % cand != 0 || !instantiated(cand, p.N / cand, sa, ck)) continue;
     ns = cand;
     const int cb = kScanThreads / (p.N / cand);
     if ((long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) break;
@@ -70,8 +73,8 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
     q.off_sumdelta = off; off = align_up(off + sizeof(float) * (size_t)p.ns * q.S * p.HP, 256);
   }
   q.bytes = off;
-  q.ok = aligned16(p.x) && aligned16(p.dt) && aligned16(p.B) && aligned16(p.C) &&
-         (!p.z || aligned16(p.z));
+  q.ok = (p.sx ? (uintptr_t)p.sx % io == 0 : aligned16(p.x)) && aligned16(p.dt) &&
+         aligned16(p.B) && aligned16(p.C) && (!p.z || aligned16(p.z));
   return q;
 }
 
@@ -86,6 +89,7 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
                                 void* ws, int num_sms, cudaStream_t st) {
   const FwdTmaPlan q = plan_fwd_tma(p, num_sms);
   if (!q.ok || (y && !aligned16(y)) || (ckpt && !aligned16(ckpt))) return cudaErrorNotSupported;
+  if (!p.sx && !p.x) return cudaErrorNotSupported;  // no tensor map over a missing input
   const int io = p.io == SSM_BF16 ? 2 : 4;
   FwdTmaArgs a;
   memset(&a, 0, sizeof(a));
@@ -99,7 +103,8 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
     a.sumdelta = (float*)(w + q.off_sumdelta);
   }
   const uint64_t C = p.HP, L = p.L, NSq = p.ns, GN = (uint64_t)p.G * p.N;
-  bool ok = encode_tmap_3d(&a.mx, p.x, io, C, L, NSq, C, C * L, q.cb, q.tt, 1) &&
+  const int ck = p.sx ? p.d_conv : 0;  // the fused conv computes x: no tensor map for it
+  bool ok = (ck > 0 || encode_tmap_3d(&a.mx, p.x, io, C, L, NSq, C, C * L, q.cb, q.tt, 1)) &&
             encode_tmap_3d(&a.mdt, p.dt, io, C, L, NSq, C, C * L, q.cb, q.tt, 1) &&
             encode_tmap_3d(&a.mb, p.B, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1) &&
             encode_tmap_3d(&a.mc, p.C, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1);
@@ -120,18 +125,22 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_bf = a.off_dd + al((uint32_t)(q.tt * q.cb * 8));
   a.off_cf = a.off_bf + frow;
   a.off_par = a.off_cf + frow;
-  a.off_y = a.off_par + al((uint32_t)(2 * q.cb * 4));
+  // D, dt_bias; with the fused conv also the conv bias and weights
+  a.off_y = a.off_par + al((uint32_t)((2 + (ck ? 1 + ck : 0)) * q.cb * 4));
   a.y_stride = al(tile);
-  a.off_bar = a.off_y + 2 * a.y_stride;
+  a.off_sxs = a.off_y + 2 * a.y_stride;
+  const uint32_t pitch = (uint32_t)((q.tt + ck - 1) | 1);
+  a.off_bar = a.off_sxs + (ck > 0 ? al((uint32_t)(q.cb * pitch * 4)) : 0u);
   const size_t smem = a.off_bar + 64;
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
-  a.bytes_local = 2 * tile + row;
-  a.bytes_main = (2 + (p.z ? 1 : 0)) * tile + 2 * row;
+  // the fused conv's x slot in a stage is written by the prepass, not copied
+  a.bytes_local = (ck > 0 ? 1 : 2) * tile + row;
+  a.bytes_main = ((ck > 0 ? 1 : 2) + (p.z ? 1 : 0)) * tile + 2 * row;
   const bool sa = !p.a_per_state;
-#define SSM_DISPATCH(NS, TPC, SA, THR)                                              \
-  if (q.ns_state == NS && q.tpc == TPC && sa == SA && q.thr == THR)                 \
-    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA, THR>(a, smem, st) \
-                   : launch_fwd_tma_t<float, NS, TPC, SA, THR>(a, smem, st);
+#define SSM_DISPATCH(NS, TPC, SA, THR, CK)                                              \
+  if (q.ns_state == NS && q.tpc == TPC && sa == SA && q.thr == THR && ck == CK)         \
+    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA, THR, CK>(a, smem, st) \
+                   : launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(a, smem, st);
   SSM_FWD_TMA_VARIANTS(SSM_DISPATCH)
 #undef SSM_DISPATCH
   return cudaErrorNotSupported;

@@ -52,7 +52,16 @@ struct FwdTmaArgs {
   uint32_t bytes_main, bytes_local;        // expected transaction bytes per stage
   uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride;  // inside a stage
   uint32_t off_dd, off_bf, off_cf, off_par, off_y, y_stride, off_bar;
+  uint32_t off_sxs;  // fused conv: [cb][odd pitch] fp32 sx columns of a tile
 };
+
+// Columns of sx a tile of the fused conv reads (TT tokens and the K-1 before the first) and
+// the odd row pitch of their fp32 staging buffer (a warp reading 32 channels at one column
+// then touches 32 different banks).
+template <int CK>
+__host__ __device__ constexpr int conv_cols() { return 16 + CK - 1; }
+template <int CK>
+__host__ __device__ constexpr int conv_pitch() { return conv_cols<CK>() | 1; }
 
 template <typename IO>
 __device__ __forceinline__ float lds1(const IO* p) {
@@ -82,13 +91,25 @@ __device__ __forceinline__ float group_reduce_scatter(float (&v)[TPC], int sg) {
 // A block = THR threads = (THR / TPC) channels x N states, NS = N / TPC states per thread, one
 // sequence, one time segment.  SCALAR_A: one A per channel (the head of head_dim 1).
 //
+// CK > 0 (the fused conv1d of width CK): x is not copied from memory but computed in the
+// prepass from sx, x = act(sum_k sx[t+k] w[k] + bias), rounded to the io type as ssm_conv_fwd
+// stores it, and written into the stage's x slot, so that everything after the prepass reads
+// it as it would read a copied tile.  A tile's sx columns are loaded into registers one tile
+// ahead with plain loads (a row of L + CK - 1 elements starts at any alignment, which TMA
+// cannot copy) and stored to shared memory once the prepass has read the previous ones.
+//
 // Per tile: a prepass writes (delta, delta x) once per (token, channel) and, for bf16 I/O, B and
 // C as fp32 rows (fp32 I/O reads the staged rows as they are).  The recurrence then runs over
 // groups of TPC tokens; after each group the lanes of a channel reduce-scatter their partial
 // C . h sums so that lane sg holds token sg's total and writes that token's
 // y = (C . h + D x) silu(z) into the output tile itself.
-template <typename IO, int NS, int TPC, int THR, bool LOCAL, bool SCALAR_A>
-__global__ void __launch_bounds__(THR)
+//
+// Registers: without the conv the compiler's own choice is kept (a minimum of 0 blocks per SM
+// states none: 64 for the d_state 16 layout, where a minimum of one block would let it spend
+// 120 and the grid would no longer fit in one wave).  The fused conv's staging would take that
+// layout past 64; its bound keeps the 8 blocks per SM that time segments aim for.
+template <typename IO, int NS, int TPC, int THR, bool LOCAL, bool SCALAR_A, int CK>
+__global__ void __launch_bounds__(THR, CK > 0 ? kFwdTargetBlocksPerSM : 0)
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;  // accurate decay form for fp32 I/O
   constexpr int TT = kFwdTile;
@@ -120,6 +141,39 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   for (int c = tid; c < cb; c += THR) {
     sPar[c] = p.D ? __ldg(p.D + ch0 + c) : 0.0f;
     sPar[cb + c] = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + ch0 + c) : 0.0f;
+    if constexpr (CK > 0) {  // conv bias, then weights [cb][CK]
+      sPar[2 * cb + c] = p.conv_b ? __ldg(p.conv_b + ch0 + c) : 0.0f;
+#pragma unroll
+      for (int k = 0; k < CK; k++)
+        sPar[3 * cb + c * CK + k] = __ldg(p.conv_w + (long)(ch0 + c) * CK + k);
+    }
+  }
+  // ---- fused conv: a tile's sx columns, loaded into registers one tile ahead ---------------
+  constexpr int SXW = CK > 0 ? conv_cols<CK>() : 1, SXP = CK > 0 ? conv_pitch<CK>() : 1;
+  constexpr int SXN = (cb * SXW + THR - 1) / THR;  // staged elements per thread
+  const long sx_row = (long)p.L + CK - 1;
+  const IO* sxg = CK > 0 ? reinterpret_cast<const IO*>(p.sx) + ((long)b * p.HP + ch0) * sx_row
+                         : nullptr;
+  float* sxs = reinterpret_cast<float*>(smem + a.off_sxs);
+  IO sxv[SXN];
+  auto sx_load = [&](int t0) {
+#pragma unroll
+    for (int u = 0; u < SXN; u++) {
+      const int e = tid + u * THR, row = e / SXW, col = e - row * SXW;
+      const bool in = (cb * SXW % THR == 0 || e < cb * SXW) && t0 + col < sx_row;
+      sxv[u] = in ? sxg[row * sx_row + t0 + col] : IO(0.0f);
+    }
+  };
+  auto sx_store = [&]() {
+#pragma unroll
+    for (int u = 0; u < SXN; u++) {
+      const int e = tid + u * THR, row = e / SXW, col = e - row * SXW;
+      if (cb * SXW % THR == 0 || e < cb * SXW) sxs[row * SXP + col] = static_cast<float>(sxv[u]);
+    }
+  };
+  if constexpr (CK > 0) {
+    sx_load(t_begin);
+    sx_store();
   }
   __syncthreads();
   auto issue = [&](int k) {  // tile k -> stage k % kFwdStages (thread 0 only)
@@ -127,7 +181,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     unsigned char* base = smem + stg * a.stage_stride;
     const int t0 = t_begin + k * TT;
     mbar_expect_tx(&full[stg], bytes);
-    tma_load_3d(base + a.off_x, &a.mx, ch0, t0, b, &full[stg]);
+    if constexpr (CK == 0) tma_load_3d(base + a.off_x, &a.mx, ch0, t0, b, &full[stg]);
     tma_load_3d(base + a.off_dt, &a.mdt, ch0, t0, b, &full[stg]);
     tma_load_3d(base + a.off_b, &a.mb, g * N, t0, b, &full[stg]);
     if (!LOCAL) {
@@ -164,6 +218,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   for (int k = 0; k < ntiles; k++) {
     const int stg = k % kFwdStages;
     if (want_y && tid == 0) tma_store_wait_read<1>();  // store k-2 has read its y buffer
+    if constexpr (CK > 0)
+      if (k + 1 < ntiles) sx_load(t_begin + (k + 1) * TT);  // lands while this tile runs
     const bool ok = mbar_wait(&full[stg], (uint32_t)(k / kFwdStages) & 1u);
     unsigned char* base = smem + stg * a.stage_stride;
     const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
@@ -181,7 +237,21 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       const int c = idx % cb;
       float dl = lds1(sdt + idx);
       if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
-      sDD[idx] = make_float2(dl, dl * lds1(sx + idx));
+      float xv;
+      if constexpr (CK == 0) {
+        xv = lds1(sx + idx);
+      } else {  // the conv of token idx / cb; x into the stage's x slot for the epilogue
+        const int i = idx / cb;
+        float acc = sPar[2 * cb + c];
+#pragma unroll
+        for (int kk = 0; kk < CK; kk++)
+          acc = fmaf(sxs[c * SXP + i + kk], sPar[3 * cb + c * CK + kk], acc);
+        if (p.conv_silu) acc = siluf_(acc);
+        const IO xr = static_cast<IO>(acc);  // as ssm_conv_fwd would store it
+        const_cast<IO*>(sx)[idx] = xr;
+        xv = static_cast<float>(xr);
+      }
+      sDD[idx] = make_float2(dl, dl * xv);
     }
     if constexpr (sizeof(IO) == 2) {
       const uint2* rb = reinterpret_cast<const uint2*>(base + a.off_b);
@@ -210,6 +280,10 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     }
     const float* Bf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_b) : sBf;
     const float* Cf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_c) : sCf;
+    // the next tile's sx columns: the prepass above has read these (barrier), and the next
+    // prepass reads them after the barrier that ends this tile
+    if constexpr (CK > 0)
+      if (k + 1 < ntiles) sx_store();
 
     // ---- the recurrence: per thread, its channel's NS states over the tile ------------------
     if (!LOCAL && a.ckpt && t0 % p.chunk == 0) {  // checkpoints fall on tile starts
@@ -359,10 +433,10 @@ __global__ void scan_fwd_tma_carry_kernel(const __grid_constant__ FwdTmaArgs a) 
   }
 }
 
-template <typename IO, int NS, int TPC, bool SCALAR_A, int THR>
+template <typename IO, int NS, int TPC, bool SCALAR_A, int THR, int CK>
 cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
-  auto km = scan_fwd_tma_kernel<IO, NS, TPC, THR, false, SCALAR_A>;
-  auto kl = scan_fwd_tma_kernel<IO, NS, TPC, THR, true, SCALAR_A>;
+  auto km = scan_fwd_tma_kernel<IO, NS, TPC, THR, false, SCALAR_A, CK>;
+  auto kl = scan_fwd_tma_kernel<IO, NS, TPC, THR, true, SCALAR_A, CK>;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -377,11 +451,13 @@ cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The (states per thread, threads per channel, A form, block threads) combinations instantiated
-// for each I/O type; X(NS, TPC, SCALAR_A, THR).
+// The (states per thread, threads per channel, A form, block threads, fused conv width)
+// combinations instantiated for each I/O type; X(NS, TPC, SCALAR_A, THR, CK).  The fused conv
+// (CK > 0) comes with the layout d_state 16 takes (4 states x 4 threads per channel).
 #define SSM_FWD_TMA_VARIANTS(X) \
-  X(16, 1, false, 128) X(8, 2, false, 128) X(4, 4, false, 128) X(16, 2, false, 128) \
-  X(8, 4, false, 128) X(16, 4, false, 128) X(16, 8, true, 128) X(8, 4, true, 128) \
-  X(16, 4, true, 128) X(4, 4, true, 128)
+  X(16, 1, false, 128, 0) X(8, 2, false, 128, 0) X(4, 4, false, 128, 0) X(16, 2, false, 128, 0) \
+  X(8, 4, false, 128, 0) X(16, 4, false, 128, 0) X(16, 8, true, 128, 0) X(8, 4, true, 128, 0) \
+  X(16, 4, true, 128, 0) X(4, 4, true, 128, 0) \
+  X(4, 4, false, 128, 1) X(4, 4, false, 128, 2) X(4, 4, false, 128, 3) X(4, 4, false, 128, 4)
 
 }  // namespace ssm

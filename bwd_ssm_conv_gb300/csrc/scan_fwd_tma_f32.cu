@@ -4,8 +4,8 @@
 
 namespace ssm {
 
-#define SSM_INSTANTIATE_F32(NS, TPC, SA, THR) \
-  template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR>(FwdTmaArgs&, size_t, cudaStream_t);
+#define SSM_INSTANTIATE_F32(NS, TPC, SA, THR, CK) \
+  template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, cudaStream_t);
 SSM_FWD_TMA_VARIANTS(SSM_INSTANTIATE_F32)
 #undef SSM_INSTANTIATE_F32
 

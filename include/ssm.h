@@ -203,6 +203,41 @@ int ssm_scan_bwd(const ssm_scan_desc* desc, const float* s0, const int32_t* ids,
                  void* d_B, void* d_C, float* d_D, void* d_z, float* d_dt_bias, void* ws,
                  size_t ws_bytes, void* stream);
 
+/* ---- conv1d + scan in one call ----------------------------------------------------------
+ * The Mamba layer's prelude and scan without the conv output x ever reaching memory in the
+ * forward: x = act(conv1d(sx) + bias) (act = SiLU with SSM_CONV_SILU) is computed inside the
+ * scan kernel from the staged sx columns, as a conv -> silu -> scan per token does in
+ * infotheory mamba1/model.rs forward_impl, and as lattice gdn_backward.rs conv1d_silu_fwd feeds
+ * its recurrence.  x is rounded to the io type, exactly as ssm_conv_fwd would store it, so the
+ * results equal ssm_conv_fwd followed by ssm_scan_fwd (up to summation order).
+ *   sx, c, bias, d_conv, conv_flags   as in ssm_conv_fwd, with d_inner = H * P
+ *   the scan arguments                as in ssm_scan_fwd, without x
+ * When the fused kernel does not apply (it takes the shapes and pointers of the TMA-staged
+ * Mamba-1 forward with d_state 16 and d_conv <= 4), x is computed by the conv kernel into the
+ * workspace and scanned from there.
+ * Workspace: ssm_conv_scan_workspace_size(desc, d_conv, 0) bytes (it includes room for x). */
+size_t ssm_conv_scan_workspace_size(const ssm_scan_desc* desc, int d_conv, int backward);
+int ssm_conv_scan_fwd(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags, const void* sx,
+                      const float* c, const float* bias, const float* s0, const int32_t* ids,
+                      const void* dt, const float* A, const void* B, const void* C,
+                      const float* D, const void* z, const float* dt_bias, void* y,
+                      float* state_out, float* ckpt, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of ssm_conv_scan_fwd: recomputes x from sx (the conv is not stored by the forward),
+ * runs the scan's backward into dL/dx and the conv's backward into d_sx, d_c and (when non-NULL)
+ * d_bias.  Scan arguments and outputs as in ssm_scan_bwd (ckpt: the forward's checkpoints, or
+ * NULL); d_x is replaced by d_sx [n_s][d_inner][K-1+L].  Workspace:
+ * ssm_conv_scan_workspace_size(desc, d_conv, 1) bytes (x, dL/dx and the conv's partial sums
+ * live there).  Every output is overwritten; reductions run in a fixed order. */
+int ssm_conv_scan_bwd(const ssm_scan_desc* desc, int d_conv, unsigned conv_flags, const void* sx,
+                      const float* c, const float* bias, const float* s0, const int32_t* ids,
+                      const void* dt, const float* A, const void* B, const void* C,
+                      const float* D, const void* z, const float* dt_bias, const float* ckpt,
+                      const void* dy, const float* d_state_out, float* d_s0, void* d_sx,
+                      float* d_c, float* d_bias, void* d_dt, float* d_A, void* d_B, void* d_C,
+                      float* d_D, void* d_z, float* d_dt_bias, void* ws, size_t ws_bytes,
+                      void* stream);
+
 /* ---- single-token decode step -----------------------------------------------------------
  * One token per sequence in one launch: the conv ring-state roll, conv1d(+bias, SiLU) of the
  * new input column, and one step of the scan.  This is the per-token loop of infotheory's

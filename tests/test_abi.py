@@ -175,3 +175,34 @@ def test_conv_workspace_is_one_partial_per_launched_tile(L):
     assert binding.ssm_conv_workspace_size(2, 37, 130, 3) == expect(2, 37, 130, 3, 256)
     assert binding.ssm_conv_workspace_size(2, 37, 130, 9) == expect(2, 37, 130, 9, 64)
     assert binding.ssm_conv_workspace_size(0, 37, 130, 4) == 0
+
+
+def test_conv_scan_rejects_bad_arguments(L):
+    """The fused conv + scan calls check their conv arguments on the host, like ssm_conv_fwd."""
+    d = _desc()
+    p = ctypes.c_void_p(FAKE)
+    assert binding.lib().ssm_conv_scan_workspace_size(ctypes.byref(d), 0, 0) == 0
+    assert binding.lib().ssm_conv_scan_workspace_size(ctypes.byref(d), 65, 1) == 0
+
+    def fwd(K=4, flags=1, sx=p, c=p, dt=p, y=p):
+        return binding.lib().ssm_conv_scan_fwd(ctypes.byref(d), K, flags, sx, c, None, None, None,
+                                               dt, p, p, p, None, None, None, y, p, None, p,
+                                               1 << 30, None)
+    assert fwd(K=0) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(K=65) == binding.SSM_ERR_UNSUPPORTED
+    assert fwd(flags=2) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(sx=None) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(c=None) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(dt=None) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(y=None) == binding.SSM_ERR_INVALID_ARG
+    assert fwd(sx=ctypes.c_void_p(FAKE + 1)) == binding.SSM_ERR_INVALID_ARG  # misaligned fp32
+
+    names = ("sx c bias s0 ids dt A B C D z dt_bias ckpt dy d_state_out d_s0 d_sx d_c d_bias "
+             "d_dt d_A d_B d_C d_D d_z d_dt_bias").split()
+    required = set("sx c dt A B C dy d_sx d_c d_dt d_A d_B d_C".split())
+
+    def bwd(ws_bytes=1 << 30, **override):
+        args = [override.get(n, p if n in required else None) for n in names]
+        return binding.lib().ssm_conv_scan_bwd(ctypes.byref(d), 4, 1, *args, p, ws_bytes, None)
+    assert bwd(d_sx=None) == binding.SSM_ERR_INVALID_ARG
+    assert bwd(d_c=None) == binding.SSM_ERR_INVALID_ARG
