@@ -185,6 +185,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pm = (lane >> 3) & 3;  // slot j holds state n0 + (j ^ pm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
+  // L2 policies: tiles read or written for the last time leave first; the sub-chunk state
+  // scratch, written at level 1 and read back at level 2 of the same chunk, stays
+  const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
   if (tid == 0) {
     for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
     fence_barrier_init();
@@ -260,14 +263,14 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
       tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
       tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
-    } else {
+    } else {  // the last read of these tiles: first out of L2, ahead of the state scratch
       mbar_expect_tx(&full[stg], m.bytes_l2);
-      tma_load_3d(base + m.off_x, &m.mx, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_dy, &m.mdy, ch0, t0, b, &full[stg]);
-      if (p.z) tma_load_3d(base + m.off_z, &m.mz, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg]);
-      tma_load_3d(base + m.off_c, &m.mc, l.g * N, t0, b, &full[stg]);
+      tma_load_3d_hint(base + m.off_x, &m.mx, ch0, t0, b, &full[stg], pol_first);
+      tma_load_3d_hint(base + m.off_dt, &m.mdt, ch0, t0, b, &full[stg], pol_first);
+      tma_load_3d_hint(base + m.off_dy, &m.mdy, ch0, t0, b, &full[stg], pol_first);
+      if (p.z) tma_load_3d_hint(base + m.off_z, &m.mz, ch0, t0, b, &full[stg], pol_first);
+      tma_load_3d_hint(base + m.off_b, &m.mb, l.g * N, t0, b, &full[stg], pol_first);
+      tma_load_3d_hint(base + m.off_c, &m.mc, l.g * N, t0, b, &full[stg], pol_first);
     }
     issued++;
     advance(pp);
@@ -334,7 +337,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     const int nsub = (cnt + kTsubTma - 1) / kTsubTma;
     const float4* bnd_tile = bnd + cs.j * (TT / kTsubTma) * kScanThreads + tid;
     float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (cs.lvl == 1) nxt = bnd_tile[(nsub - 1) * kScanThreads];
+    if (cs.lvl == 1) nxt = ld_global_hint(bnd_tile + (nsub - 1) * kScanThreads, pol_last);
 
     // ---- prepass, once per (token, channel); a compile-time item count lets the items'
     // shared loads be in flight together -------------------------------------------------------
@@ -419,7 +422,8 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
           float h0, h1, h2, h3;
           f2_unpack(hp[0], h0, h1);
           f2_unpack(hp[1], h2, h3);
-          bnd[(cs.j * (TT / kTsubTma) + i / kTsubTma) * kScanThreads + tid] = make_float4(h0, h1, h2, h3);
+          st_global_hint(bnd + (cs.j * (TT / kTsubTma) + i / kTsubTma) * kScanThreads + tid,
+                         make_float4(h0, h1, h2, h3), pol_last);
         }
         const float2 d2 = sD2[i * CB + cl];
         const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
@@ -513,7 +517,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     };
     for (int k = nsub - 1; k >= 0; k--) {
       const float4 cur = nxt;
-      if (k > 0) nxt = bnd_tile[(k - 1) * kScanThreads];  // hide the scratch latency
+      if (k > 0) nxt = ld_global_hint(bnd_tile + (k - 1) * kScanThreads, pol_last);  // ahead
       const int c8 = min(kTsubTma, cnt - k * kTsubTma);
       if (c8 == kTsubTma) sub_chunk(k, c8, cur, std::true_type{});
       else sub_chunk(k, c8, cur, std::false_type{});
@@ -556,7 +560,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 #pragma unroll
       for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
       const long tok = (long)b * p.L + t0 + i;
-      a.part_bc[((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r] = v;
+      st_global_hint(a.part_bc + ((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r, v, pol_first);
     };
     if (cnt == TT) {  // full tile: a compile-time item count, so the items interleave
 #pragma unroll
@@ -570,9 +574,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     fence_async_shared();
     __syncthreads();  // out tiles complete; stage fully read
     if (tid == 0) {
-      tma_store_3d(&m.mdx, odx, ch0, t0, b);
-      if (p.z && a.g.d_z) tma_store_3d(&m.mdz, odz, ch0, t0, b);
-      tma_store_3d(&m.mddt, oddt, ch0, t0, b);
+      tma_store_3d_hint(&m.mdx, odx, ch0, t0, b, pol_first);
+      if (p.z && a.g.d_z) tma_store_3d_hint(&m.mdz, odz, ch0, t0, b, pol_first);
+      tma_store_3d_hint(&m.mddt, oddt, ch0, t0, b, pol_first);
       tma_store_commit();
       if (pp.ck >= c_first) issue();
     }
@@ -627,7 +631,7 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
   const int s = blockIdx.y + 1, b = blockIdx.z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  float4* sP = reinterpret_cast<float4*>(smem + m.off_e);
+  float2* sP = reinterpret_cast<float2*>(smem + m.off_e);  // [TT][CB] (delta, gy)
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);
   const int t_begin = s * a.seg_chunks * a.chunk_b;
   const int t_end = min(p.L, t_begin + a.seg_chunks * a.chunk_b);
@@ -682,15 +686,15 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       const float dl = p.softplus ? softplusf_(raw + sPar[CB + c]) : raw;
       float gy = lds_f(sdy + idx);
       if (p.z) gy *= siluf_(lds_f(sz + idx));
-      sP[idx] = make_float4(dl, 0.0f, gy, 0.0f);
+      sP[idx] = make_float2(dl, gy);
     }
     const float* sCf = tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N);
     __syncthreads();
 #pragma unroll
     for (int r = TT - 1; r >= 0; r--) {
       if (r < cnt) {
-        const float4 p4 = sP[r * CB + cl];
-        const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.z, p4.z);
+        const float2 p4 = sP[r * CB + cl];
+        const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.y, p4.y);
         const float4 cv = *reinterpret_cast<const float4*>(sCf + r * N + n0);
         c2[0] = apply2<ACC>(decay2<ACC>(dl2, A2p[0]), f2_fma(gy2, f2_pack(cv.x, cv.y), c2[0]));
         c2[1] = apply2<ACC>(decay2<ACC>(dl2, A2p[1]), f2_fma(gy2, f2_pack(cv.z, cv.w), c2[1]));

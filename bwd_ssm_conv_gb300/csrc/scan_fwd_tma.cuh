@@ -149,27 +149,34 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     }
   }
   // ---- fused conv: a tile's sx columns, loaded into registers one tile ahead ---------------
+  // Thread tid stages row tid / 4 of the block's cb = THR / 4 rows, columns tid % 4 + 4u.
   constexpr int SXW = CK > 0 ? conv_cols<CK>() : 1, SXP = CK > 0 ? conv_pitch<CK>() : 1;
-  constexpr int SXN = (cb * SXW + THR - 1) / THR;  // staged elements per thread
+  constexpr int SXU = (SXW + 3) / 4;  // staged elements per thread
+  static_assert(CK == 0 || (cb * 4 == THR && TT == 16 && THR == 128), "fused conv layout");
   const long sx_row = (long)p.L + CK - 1;
-  const IO* sxg = CK > 0 ? reinterpret_cast<const IO*>(p.sx) + ((long)b * p.HP + ch0) * sx_row
-                         : nullptr;
+  const int sx_r = tid >> 2, sx_q = tid & 3;
+  const IO* sx_rowp = CK > 0 ? reinterpret_cast<const IO*>(p.sx) +
+                                   ((long)b * p.HP + ch0 + sx_r) * sx_row + sx_q
+                             : nullptr;
   float* sxs = reinterpret_cast<float*>(smem + a.off_sxs);
-  IO sxv[SXN];
+  IO sxv[SXU];
   auto sx_load = [&](int t0) {
+    const IO* q = sx_rowp + t0;
+    if (t0 + SXW <= sx_row) {  // every column of the tile exists
 #pragma unroll
-    for (int u = 0; u < SXN; u++) {
-      const int e = tid + u * THR, row = e / SXW, col = e - row * SXW;
-      const bool in = (cb * SXW % THR == 0 || e < cb * SXW) && t0 + col < sx_row;
-      sxv[u] = in ? sxg[row * sx_row + t0 + col] : IO(0.0f);
+      for (int u = 0; u < SXU; u++)
+        if (SXW % 4 == 0 || 4 * u + sx_q < SXW) sxv[u] = q[4 * u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < SXU; u++)
+        sxv[u] = (4 * u + sx_q < SXW && t0 + 4 * u + sx_q < sx_row) ? q[4 * u] : IO(0.0f);
     }
   };
   auto sx_store = [&]() {
 #pragma unroll
-    for (int u = 0; u < SXN; u++) {
-      const int e = tid + u * THR, row = e / SXW, col = e - row * SXW;
-      if (cb * SXW % THR == 0 || e < cb * SXW) sxs[row * SXP + col] = static_cast<float>(sxv[u]);
-    }
+    for (int u = 0; u < SXU; u++)
+      if (SXW % 4 == 0 || 4 * u + sx_q < SXW)
+        sxs[sx_r * SXP + 4 * u + sx_q] = static_cast<float>(sxv[u]);
   };
   if constexpr (CK > 0) {
     sx_load(t_begin);
@@ -231,27 +238,39 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     // ---- prepass (a tile that never arrived leaves stale but in-bounds shared memory); a
     // compile-time item count lets the items' shared loads be in flight together ------------
     static_assert(TT * cb % THR == 0, "prepass items per thread");
+    if constexpr (CK == 0) {
 #pragma unroll
-    for (int u = 0; u < TT * cb / THR; u++) {
-      const int idx = tid + u * THR;
-      const int c = idx % cb;
-      float dl = lds1(sdt + idx);
-      if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
-      float xv;
-      if constexpr (CK == 0) {
-        xv = lds1(sx + idx);
-      } else {  // the conv of token idx / cb; x into the stage's x slot for the epilogue
-        const int i = idx / cb;
-        float acc = sPar[2 * cb + c];
-#pragma unroll
-        for (int kk = 0; kk < CK; kk++)
-          acc = fmaf(sxs[c * SXP + i + kk], sPar[3 * cb + c * CK + kk], acc);
-        if (p.conv_silu) acc = siluf_(acc);
-        const IO xr = static_cast<IO>(acc);  // as ssm_conv_fwd would store it
-        const_cast<IO*>(sx)[idx] = xr;
-        xv = static_cast<float>(xr);
+      for (int u = 0; u < TT * cb / THR; u++) {
+        const int idx = tid + u * THR;
+        const int c = idx % cb;
+        float dl = lds1(sdt + idx);
+        if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
+        sDD[idx] = make_float2(dl, dl * lds1(sx + idx));
       }
-      sDD[idx] = make_float2(dl, dl * xv);
+    } else {
+      // the conv: warp w takes tokens 4w .. 4w+3 of channel `lane`, a sliding window over
+      // its sx columns; x goes into the stage's x slot (rounded to the io type, as
+      // ssm_conv_fwd stores it) for the epilogue
+      const int c = tid & 31, i0 = (tid >> 5) * 4;
+      float wk[CK], win[4 + CK - 1];
+#pragma unroll
+      for (int kk = 0; kk < CK; kk++) wk[kk] = sPar[3 * cb + c * CK + kk];
+#pragma unroll
+      for (int m = 0; m < 4 + CK - 1; m++) win[m] = sxs[c * SXP + i0 + m];
+      const float cbias = sPar[2 * cb + c], dtb = sPar[cb + c];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int idx = (i0 + u) * cb + c;
+        float dl = lds1(sdt + idx);
+        if (p.softplus) dl = softplusf_(dl + dtb);
+        float acc = cbias;
+#pragma unroll
+        for (int kk = 0; kk < CK; kk++) acc = fmaf(win[u + kk], wk[kk], acc);
+        if (p.conv_silu) acc = siluf_(acc);
+        const IO xr = static_cast<IO>(acc);
+        const_cast<IO*>(sx)[idx] = xr;
+        sDD[idx] = make_float2(dl, dl * static_cast<float>(xr));
+      }
     }
     if constexpr (sizeof(IO) == 2) {
       const uint2* rb = reinterpret_cast<const uint2*>(base + a.off_b);
