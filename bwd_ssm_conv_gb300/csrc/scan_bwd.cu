@@ -482,13 +482,8 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.off_dtb = take(segch);
   q.off_ddt = take(p.P > 1 ? F * (size_t)p.ns * p.L * p.HP : 0);
   q.off_dh0 = take(F * (size_t)p.ns * p.HP * p.N);
-  if (q.tma_tt) {
-    const size_t units = (size_t)chains * q.S;
-    const size_t slots = (size_t)num_sms * kBwdTmaBlocksPerSM;
-    const size_t blocks = q.persist && slots < units ? slots : units;  // one per resident block
-    q.off_bnd = take(bwd_tma_scratch_bytes(q, blocks));
-    if (q.persist) q.off_queue = take(sizeof(int) * (1 + units));  // counter, then unit flags
-  }
+  if (q.tma_tt && q.persist)  // queue counter, then unit flags
+    q.off_queue = take(sizeof(int) * (1 + (size_t)chains * q.S));
   if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));
   q.bytes = off;
   const int nsub_max = (q.chunk_b + kTsub - 1) / kTsub;

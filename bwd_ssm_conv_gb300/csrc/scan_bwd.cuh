@@ -91,10 +91,10 @@ struct BwdPlan {
   // of the chunk before it (see scan_bwd_tma.cu).
   bool persist;
   size_t off_fwd, fwd_bytes, off_ckpt, off_dhloc, off_segend, off_sumd, off_part_bc, off_dA,
-      off_dD, off_dtb, off_ddt, off_dh0, off_bnd, off_mh, off_queue, bytes, smem;
+      off_dD, off_dtb, off_ddt, off_dh0, off_mh, off_queue, bytes, smem;
 };
-// Resident blocks per SM the TMA-staged backward is built for (its launch bound); the
-// persistent path and its scratch are sized by it.
+// Resident blocks per SM the TMA-staged backward is built for (its launch bound; each block
+// also holds a quarter of the SM's tensor memory).
 constexpr int kBwdTmaBlocksPerSM = 4;
 
 // Mamba-2-form backward (scan_bwd_heads.cu): one A per head, head_dim % 32 == 0, d_state 128.
@@ -109,8 +109,6 @@ int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc);
 // Channels per block of the TMA-staged main kernel (its per-block dB/dC partials are per
 // this many channels).
 int bwd_tma_channels_per_block();
-// Scratch of the TMA-staged main kernel for `blocks` blocks.
-size_t bwd_tma_scratch_bytes(const BwdPlan& q, size_t blocks);
 // Both return cudaErrorNotSupported, launching nothing, when the pointers do not allow the
 // path; the caller then runs the general kernels.
 cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st);

@@ -12,24 +12,32 @@
 // lane pairs and go through shared memory to an epilogue that writes dx, dz and ddt, and the
 // dB/dC sums over channels use a warp butterfly whose exchanges need no lane-dependent selects
 // (each thread's states sit in registers in a lane-permuted order).  Four blocks fit an SM
-// (about 120 registers, 55 KB of shared memory).
+// (at most 128 registers, about 54 KB of shared memory).
 //
 // Per chunk (last to first): level 1 walks the chunk's tiles forward from the checkpoint,
-// saving the state at every 4-token sub-chunk start (global scratch); level 2 walks the tiles
-// in reverse, recomputes each sub-chunk's 4 states and decays in registers and runs the
-// adjoint over them, loading the next sub-chunk's start state one sub-chunk ahead.
+// saving each tile's start state in tensor memory; level 2 walks the tiles in reverse,
+// recomputes the tile's 16 states into tensor memory and runs the adjoint over them in reverse,
+// reading them back four tokens at a time and recomputing each token's decays.  The state
+// history never leaves the SM.
 #include <type_traits>
 
 #include "scan_bwd.cuh"
 #include "tma.cuh"
+#include "tmem.cuh"
 
 namespace ssm {
 
 constexpr int kBwdStages = 2;
-constexpr int kBwdTile = 16;                  // tokens per staged tile (four sub-chunks)
-constexpr int kTsubTma = 4;                   // tokens of state history held in registers
+constexpr int kBwdTile = 16;                  // tokens per staged tile
 constexpr int kCB = kScanThreads / 4;         // channels per block
 constexpr int kWarps = kScanThreads / 32;
+// Tensor memory of a block: 128 columns (a quarter of the SM's; shared memory keeps a block's
+// SM to 4 blocks).  Per thread (lane), 4 columns per state record of its 4 states:
+// columns [0, 64): the recomputed states of the current level-2 tile, record k = the state
+// before token k; columns [64, 128): level 1's tile start states, record j = tile j of the chunk.
+constexpr uint32_t kTmCols = 128;
+constexpr uint32_t kTmHist = 0, kTmStart = 64;
+constexpr int kTmChunkTiles = 16;             // tile starts that fit: chunks of <= 256 tokens
 
 struct BwdTma {
   CUtensorMap mx, mdt, mz, mdy, mb, mc, mdx, mdz, mddt;
@@ -37,7 +45,6 @@ struct BwdTma {
   uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
   uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
-  float4* bnd;
   // persistent mode: unit queue counter, per-unit ready flags, units, chains, chain stride
   int* counter;
   int* flags;
@@ -67,14 +74,11 @@ __device__ __forceinline__ void publish_unit_flag(int* flag) {
 int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc) {
   const int io = p.io == SSM_BF16 ? 2 : 4;
   if (p.P == 1 && p.a_per_state && p.N == 16 && (p.HP * io) % 16 == 0 && gc % kCB == 0 &&
-      chunk_b % kBwdTile == 0)
+      chunk_b % kBwdTile == 0 && chunk_b <= kTmChunkTiles * kBwdTile)
     return kBwdTile;
   return 0;
 }
 int bwd_tma_channels_per_block() { return kCB; }
-size_t bwd_tma_scratch_bytes(const BwdPlan& q, size_t blocks) {
-  return sizeof(float4) * blocks * (size_t)(q.chunk_b / kTsubTma) * kScanThreads;
-}
 
 template <typename IO>
 __device__ __forceinline__ float lds_f(const IO* p) {
@@ -185,15 +189,24 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pm = (lane >> 3) & 3;  // slot j holds state n0 + (j ^ pm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  // L2 policies: tiles read or written for the last time leave first; the sub-chunk state
-  // scratch, written at level 1 and read back at level 2 of the same chunk, stays
-  const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
+  // L2 policy of the tiles read or written for the last time: first out
+  const uint64_t pol_first = l2_policy_evict_first();
+  __shared__ uint32_t sTmem;
   if (tid == 0) {
     for (int i = 0; i < kBwdStages; i++) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
+  __syncwarp();
+  if (warp == 0) tmem_alloc(&sTmem, kTmCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tm = sTmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
   // ring cursors run on across units: a stage's barrier phase follows the count of its uses
   int issued = 0, qpos = 0, n_l2 = 0;
+  // the units; every way out (done, or a wait that gave up) returns from here to the release
+  // of the tensor memory below
+  [&]() {
   for (int round = 0;; round++) {
   int ux, s, b;
   if constexpr (PERSIST) {
@@ -224,10 +237,6 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   float* red = reinterpret_cast<float*>(smem + m.off_red);       // [TT][warps][2N]
   float* sPar = reinterpret_cast<float*>(smem + m.off_par);      // D[CB], dt_bias[CB]
   float* sAcc = reinterpret_cast<float*>(smem + m.off_acc);      // [warps][CB][2]
-  const int nsub_max = a.chunk_b / kTsubTma;
-  float4* bnd = m.bnd + (PERSIST ? (long)blockIdx.x
-                                 : ((long)(b * a.S + s) * gridDim.x + blockIdx.x)) *
-                            nsub_max * kScanThreads;
   const int c_first = s * a.seg_chunks;
   const int c_last = min(a.nch_b, c_first + a.seg_chunks) - 1;
 
@@ -332,12 +341,6 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     const int t0c = cs.ck * a.chunk_b, t1c = min(p.L, t0c + a.chunk_b);
     const int t0 = t0c + cs.j * TT;
     const int cnt = min(TT, t1c - t0);
-    // level 2: the start state of the tile's last sub-chunk, loaded before the prepass so that
-    // its latency overlaps it (scratch written by level 1 may have left L2)
-    const int nsub = (cnt + kTsubTma - 1) / kTsubTma;
-    const float4* bnd_tile = bnd + cs.j * (TT / kTsubTma) * kScanThreads + tid;
-    float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (cs.lvl == 1) nxt = ld_global_hint(bnd_tile + (nsub - 1) * kScanThreads, pol_last);
 
     // ---- prepass, once per (token, channel); a compile-time item count lets the items'
     // shared loads be in flight together -------------------------------------------------------
@@ -411,20 +414,19 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
 
     if (cs.lvl == 0) {
-      // ---- level 1: walk the tile forward, keeping every sub-chunk's start state ----------
+      // ---- level 1: walk the tile forward from its start state, which goes to tensor memory
       if (cs.j == 0) {
         const float* src = a.ckpt + (((long)b * a.nch_b + cs.ck) * p.HP + ch) * N + n0;
         hp[0] = f2_pack(src[0 ^ pm], src[1 ^ pm]);
         hp[1] = f2_pack(src[2 ^ pm], src[3 ^ pm]);
       }
+      {
+        float h0, h1, h2, h3;
+        f2_unpack(hp[0], h0, h1);
+        f2_unpack(hp[1], h2, h3);
+        tmem_st4(tm + kTmStart + 4 * cs.j, h0, h1, h2, h3);
+      }
       auto token = [&](int i) {
-        if (i % kTsubTma == 0) {
-          float h0, h1, h2, h3;
-          f2_unpack(hp[0], h0, h1);
-          f2_unpack(hp[1], h2, h3);
-          st_global_hint(bnd + (cs.j * (TT / kTsubTma) + i / kTsubTma) * kScanThreads + tid,
-                         make_float4(h0, h1, h2, h3), pol_last);
-        }
         const float2 d2 = sD2[i * CB + cl];
         const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
         f2_t B2[2];
@@ -445,83 +447,103 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       continue;
     }
 
-    // ---- level 2: sub-chunks last to first: recompute 8 states, then the adjoint ------------
-    // One sub-chunk; FULL (all kTsubTma tokens present) drops the per-token branches.
-    // v: the sub-chunk's start state (loaded one sub-chunk ahead by the caller)
-    auto sub_chunk = [&](int k, int c8, float4 v, auto full_tag) {
-      constexpr bool FULL = decltype(full_tag)::value;
-      const int i0 = k * kTsubTma;
-      f2_t hh[kTsubTma + 1][2], aa[kTsubTma][2];
-      hh[0][0] = f2_pack(v.x, v.y);
-      hh[0][1] = f2_pack(v.z, v.w);
+    // ---- level 2: recompute the tile's states into tensor memory, then the adjoint in reverse
+    tmem_wait_st();  // the tile start states of level 1 have landed
+    f2_t hcur[2];
+    {
+      float v[4];
+      tmem_ld4(tm + kTmStart + 4 * cs.j, v);
+      hcur[0] = f2_pack(v[0], v[1]);
+      hcur[1] = f2_pack(v[2], v[3]);
+    }
+    // One token of the adjoint: hcur = the state after token i, hprev = the state before it;
+    // the decays are recomputed (a second copy of the history would not fit tensor memory).
+    auto adjoint = [&](int i, const f2_t (&hcur)[2], const f2_t (&hprev)[2]) {
+        const float2 d2 = sD2[i * CB + cl];
+        const float gyv = sGy[i * CB + cl];
+        const f2_t dl2 = f2_pack(d2.x, d2.x), gy2 = f2_pack(gyv, gyv);
+        const f2_t dlx2 = f2_pack(d2.y, d2.y);
+        f2_t B2[2], C2[2];
+        ld_bc(i, B2, C2);
+        f2_t sB2 = 0ull, sAw2 = 0ull, yp2 = 0ull, dB2[2], dC2[2];
 #pragma unroll
-      for (int r = 0; r < kTsubTma; r++) {
-        if (FULL || r < c8) {
-          const float2 d2 = sD2[(i0 + r) * CB + cl];
-          const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
-          f2_t B2[2];
-          ld_b(i0 + r, B2);
-          aa[r][0] = decay2<ACC>(dl2, A2p[0]);
-          aa[r][1] = decay2<ACC>(dl2, A2p[1]);
-          hh[r + 1][0] = step2<ACC>(aa[r][0], hh[r][0], f2_mul(dx2, B2[0]));
-          hh[r + 1][1] = step2<ACC>(aa[r][1], hh[r][1], f2_mul(dx2, B2[1]));
-        } else {
-          aa[r][0] = aa[r][1] = 0ull;
-          hh[r + 1][0] = hh[r][0];
-          hh[r + 1][1] = hh[r][1];
+        for (int q = 0; q < 2; q++) {
+          const f2_t dh2 = f2_fma(gy2, C2[q], carry2[q]);
+          dC2[q] = f2_mul(gy2, hcur[q]);
+          sB2 = f2_fma(dh2, B2[q], sB2);
+          dB2[q] = f2_mul(dh2, dlx2);
+          const f2_t cn2 = apply2<ACC>(decay2<ACC>(dl2, A2p[q]), dh2);
+          const f2_t w2 = f2_mul(cn2, hprev[q]);
+          sAw2 = f2_fma(Anp[q], w2, sAw2);
+          dA2[q] = f2_fma(dl2, w2, dA2[q]);
+          yp2 = f2_fma(C2[q], hcur[q], yp2);
+          carry2[q] = cn2;
         }
+        {  // sum the lane pair (states n0 .. n0+3 and the neighbour's 4), one store per sum
+          float vb = f2_sum(sB2), va = f2_sum(sAw2), vy = f2_sum(yp2);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+          va += __shfl_xor_sync(0xffffffffu, va, 1);
+          vy += __shfl_xor_sync(0xffffffffu, vy, 1);
+          const int q = i * (kScanThreads / 2) + (tid >> 1);
+          if (tid & 1) {
+            sPY[q] = vy;
+          } else {
+            sPB[q] = vb;
+            sPA[q] = va;
+          }
+        }
+        float tb, tc;
+        f2_unpack(reduce_bc_warp(dB2[0], dB2[1], dC2[0], dC2[1]), tb, tc);
+        const int hi = (lane >> 2) & 1;  // of the lane pair: 0 writes dB, 1 writes dC
+        red[(i * kWarps + warp) * 2 * N + hi * N + n0 + pm] = hi ? tc : tb;
+    };
+    // FULL (all TT tokens present) drops the per-token branches
+    auto level2 = [&](auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
+      // records 4g .. 4g+3 (the states before tokens 4g .. 4g+3) go out in one store; one
+      // group at a time (unrolled, the groups' registers would overlap)
+#pragma unroll 1
+      for (int g = 0; g < TT / 4; g++) {
+        if (!FULL && 4 * g >= cnt) break;
+        float rec[16];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          f2_unpack(hcur[0], rec[4 * u], rec[4 * u + 1]);
+          f2_unpack(hcur[1], rec[4 * u + 2], rec[4 * u + 3]);
+          const int i = 4 * g + u;
+          if (FULL || i < cnt) {
+            const float2 d2 = sD2[i * CB + cl];
+            const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
+            f2_t B2[2];
+            ld_b(i, B2);
+            hcur[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hcur[0], f2_mul(dx2, B2[0]));
+            hcur[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hcur[1], f2_mul(dx2, B2[1]));
+          }
+        }
+        tmem_st16(tm + kTmHist + 16 * g, rec);
       }
+      tmem_wait_st();
+      // hcur: the state after the tile's last token
+#pragma unroll 1
+      for (int g = TT / 4 - 1; g >= 0; g--) {
+        if (!FULL && 4 * g >= cnt) continue;
+        float rec[16];
+        tmem_ld16(tm + kTmHist + 16 * g, rec);
 #pragma unroll
-      for (int r = kTsubTma - 1; r >= 0; r--) {
-        if (FULL || r < c8) {  // uniform over the block
-          const int i = i0 + r;
-          const float2 d2 = sD2[i * CB + cl];
-          const float gyv = sGy[i * CB + cl];
-          const f2_t dl2 = f2_pack(d2.x, d2.x), gy2 = f2_pack(gyv, gyv);
-          const f2_t dlx2 = f2_pack(d2.y, d2.y);
-          f2_t B2[2], C2[2];
-          ld_bc(i, B2, C2);
-          f2_t sB2 = 0ull, sAw2 = 0ull, yp2 = 0ull, dB2[2], dC2[2];
-#pragma unroll
-          for (int q = 0; q < 2; q++) {
-            const f2_t dh2 = f2_fma(gy2, C2[q], carry2[q]);
-            dC2[q] = f2_mul(gy2, hh[r + 1][q]);
-            sB2 = f2_fma(dh2, B2[q], sB2);
-            dB2[q] = f2_mul(dh2, dlx2);
-            const f2_t cn2 = apply2<ACC>(aa[r][q], dh2);
-            const f2_t w2 = f2_mul(cn2, hh[r][q]);
-            sAw2 = f2_fma(Anp[q], w2, sAw2);
-            dA2[q] = f2_fma(dl2, w2, dA2[q]);
-            yp2 = f2_fma(C2[q], hh[r + 1][q], yp2);
-            carry2[q] = cn2;
+        for (int u = 3; u >= 0; u--) {
+          const int i = 4 * g + u;
+          if (FULL || i < cnt) {  // uniform over the block
+            const f2_t hprev[2] = {f2_pack(rec[4 * u], rec[4 * u + 1]),
+                                   f2_pack(rec[4 * u + 2], rec[4 * u + 3])};
+            adjoint(i, hcur, hprev);
+            hcur[0] = hprev[0];
+            hcur[1] = hprev[1];
           }
-          {  // sum the lane pair (states n0 .. n0+3 and the neighbour's 4), one store per sum
-            float vb = f2_sum(sB2), va = f2_sum(sAw2), vy = f2_sum(yp2);
-            vb += __shfl_xor_sync(0xffffffffu, vb, 1);
-            va += __shfl_xor_sync(0xffffffffu, va, 1);
-            vy += __shfl_xor_sync(0xffffffffu, vy, 1);
-            const int q = i * (kScanThreads / 2) + (tid >> 1);
-            if (tid & 1) {
-              sPY[q] = vy;
-            } else {
-              sPB[q] = vb;
-              sPA[q] = va;
-            }
-          }
-          float tb, tc;
-          f2_unpack(reduce_bc_warp(dB2[0], dB2[1], dC2[0], dC2[1]), tb, tc);
-          const int hi = (lane >> 2) & 1;  // of the lane pair: 0 writes dB, 1 writes dC
-          red[(i * kWarps + warp) * 2 * N + hi * N + n0 + pm] = hi ? tc : tb;
         }
       }
     };
-    for (int k = nsub - 1; k >= 0; k--) {
-      const float4 cur = nxt;
-      if (k > 0) nxt = ld_global_hint(bnd_tile + (k - 1) * kScanThreads, pol_last);  // ahead
-      const int c8 = min(kTsubTma, cnt - k * kTsubTma);
-      if (c8 == kTsubTma) sub_chunk(k, c8, cur, std::true_type{});
-      else sub_chunk(k, c8, cur, std::false_type{});
-    }
+    if (cnt == TT) level2(std::true_type{});
+    else level2(std::false_type{});
     if (tid == 0) tma_store_wait_read<0>();  // the previous tile's stores have read `out`
     __syncthreads();  // sPart and red complete; `out` free
 
@@ -616,6 +638,11 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     if (tid == 0) publish_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s - 1);
   }
   }  // units
+  }();
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 0) tmem_dealloc(sTmem, kTmCols);
 }
 
 // Local adjoint of segments 1..S-1 (zero adjoint at the segment end), tiles in reverse.
@@ -765,7 +792,6 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->bytes_l1 = 2 * tile + row;
   m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
   m->bytes_loc = (2 + (p.z ? 1 : 0)) * tile + row;
-  m->bnd = w ? reinterpret_cast<float4*>(w + q.off_bnd) : nullptr;
   m->flag_spin = (p.debug_flags & kDebugNoWait) ? 0u : kFlagSpin;
   return true;
 }
@@ -780,6 +806,28 @@ __global__ void bwd_queue_reset_kernel(int* q, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) q[i] = 0;
 }
 
+// Blocks of a main kernel resident on an SM, from its registers and shared memory, capped at
+// the 512 / kTmCols that share the SM's tensor memory (a block beyond that would wait in the
+// allocation until one ends).  The runtime's occupancy query counts one block per SM for a
+// kernel that allocates tensor memory, whatever it takes.
+static int resident_blocks(const void* fn, size_t dyn_smem) {
+  cudaFuncAttributes fa;
+  int dev = 0, regs_sm = 0, smem_sm = 0, reserved = 0;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+    return 0;
+  const int warps = kScanThreads / 32;
+  const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp in 256s
+  const int by_regs = regs_sm / (warp_regs * warps);
+  const size_t block_smem = fa.sharedSizeBytes + dyn_smem + (size_t)reserved;
+  const int by_smem = (int)((size_t)smem_sm / block_smem);
+  int n = by_regs < by_smem ? by_regs : by_smem;
+  if (n > (int)(512u / kTmCols)) n = (int)(512u / kTmCols);
+  return n;
+}
+
 template <typename IO, bool PERSIST>
 static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, int num_sms,
                                  cudaStream_t st) {
@@ -787,15 +835,12 @@ static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, 
   auto k = scan_bwd_tma_kernel<IO, PERSIST>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
   if (e != cudaSuccess) return e;
+  const int per_sm = resident_blocks(reinterpret_cast<const void*>(k), m.smem);
+  if (per_sm < 1) return cudaErrorNotSupported;
   if (!PERSIST) {
     k<<<dim3(p.G * a.bpg, a.S, p.ns), kScanThreads, m.smem, st>>>(m, a), count_launches(1);
     return cudaGetLastError();
   }
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kScanThreads, m.smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorNotSupported;
-  if (per_sm > kBwdTmaBlocksPerSM) per_sm = kBwdTmaBlocksPerSM;  // the scratch is sized so
   m.gx = p.G * a.bpg;
   m.chains = m.gx * p.ns;
   m.units = m.chains * a.nch_b;

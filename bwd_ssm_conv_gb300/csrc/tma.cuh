@@ -71,16 +71,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// L2 eviction policies for the hinted copies below: evict_first for data read or written for
-// the last time (streamed tiles), evict_last for data that will be read again soon.
+// L2 eviction policy for the hinted copies below: evict_first, for data read or written for
+// the last time (streamed tiles), so that it leaves L2 ahead of data that is read again.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
@@ -115,22 +110,9 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const 
       : "memory");
 }
 
-// Global stores (16 or 4 bytes) and a 16-byte load with an L2 eviction policy.
-__device__ __forceinline__ void st_global_hint(float4* p, float4 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
-               : "memory");
-}
+// A 4-byte global store with an L2 eviction policy.
 __device__ __forceinline__ void st_global_hint(float* p, float v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
-}
-__device__ __forceinline__ float4 ld_global_hint(const float4* p, uint64_t pol) {
-  float4 v;
-  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p), "l"(pol)
-               : "memory");
-  return v;
 }
 
 __device__ __forceinline__ void tma_store_commit() {
