@@ -52,8 +52,9 @@ def alg_bytes(w) -> dict:
     scan_bwd = (D + H + zc + D) * io + bc + ck + (D + H + zc) * io + bc  # + dy in; dx dt dz dB dC
     conv_fwd = 2 * D * io if w.d_conv else 0
     conv_bwd = 3 * D * io if w.d_conv else 0
+    # the fused calls read sx where the scan reads x and write d_sx where it writes dx
     return {"conv_fwd": conv_fwd, "scan_fwd": scan_fwd, "scan_bwd": scan_bwd,
-            "conv_bwd": conv_bwd}
+            "conv_bwd": conv_bwd, "conv_scan_fwd": scan_fwd, "conv_scan_bwd": scan_bwd}
 
 
 # Algorithmic FP32 flops per (token, channel, state) element of the method itself (an FMA
@@ -79,14 +80,18 @@ TARGET_WORKLOADS = ("mamba1_long_bf16_b1_l16384_d2048_n16", DEFAULT_WORKLOAD)
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 958956544 + 1293119744,
+        "bytes": 422653696 + 472961280,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "0592b6cd43bced5da92b596baa0b110a78e293c3cfe4de2dd02ac366981512fa",
+                "002fc5a97d7695593c0b457849190d343e69fef2776ce838d83ee07a9862fda8",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
-                "561a4c86d7706877ace6dfe08a6a6e6b2fec8fd6789769f1024dd61a739393f2",
+                "42d6cfde6338fb1d9fa0db2c74aae2f3108949b3c94f1e463dc38801cd9c8584",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
                 "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
+            "bwd_ssm_conv_gb300/csrc/tmem.cuh":
+                "7460dfcf5836cbb974ca8c84ec19c0858a2376bf6f308206f2db15ba286874db",
+            "bwd_ssm_conv_gb300/csrc/tma.cuh":
+                "b34d036a83829241c4d9054142a9f1af16468fc28db91019d9abeea76186950b",
         },
     },
 }
@@ -184,13 +189,17 @@ def packed(specs, dev):
 
 
 class Step:
-    """Device buffers for one step of the hot path and the calls that run it."""
+    """Device buffers for one step of the hot path and the calls that run it.  path "split":
+    ssm_conv_fwd -> ssm_scan_fwd -> ssm_scan_bwd -> ssm_conv_bwd, x kept between the forward
+    and the backward; "fused": ssm_conv_scan_fwd -> ssm_conv_scan_bwd, x never stored by the
+    forward (the backward recomputes it)."""
 
-    def __init__(self, w, dev, inp):
+    def __init__(self, w, dev, inp, path="split"):
         from bwd_ssm_conv_gb300 import binding as B
         self.B = B
         self.w = w
         self.dev = dev
+        self.path = path if w.d_conv else "split"
         self.in_keys = [k for k in (["sx", "c"] if w.d_conv else ["x"]) +
                         ["dt", "A", "B", "C", "D", "z", "s0", "dy", "d_state_out"]
                         if inp.get(k) is not None]
@@ -241,9 +250,28 @@ class Step:
                                     dtype=torch.uint8, device=dev)
             self.d_sx = o["d_sx"]
             self.d_c = o["d_c"]
+        if self.path == "fused":
+            csh = B.conv_scan_shape(d["sx"], d["c"], d["dt"], d["A"], d["B"], d["s0"], w.chunk)
+            self.ws_cf = torch.empty(B.ssm_conv_scan_workspace_size(csh, w.d_conv, False),
+                                     dtype=torch.uint8, device=dev)
+            self.ws_cb = torch.empty(B.ssm_conv_scan_workspace_size(csh, w.d_conv, True),
+                                     dtype=torch.uint8, device=dev)
+            if not w.fwd_only:
+                self.gf = dict(self.g, d_sx=self.d_sx, d_c=self.d_c, d_bias=None)
+                del self.gf["d_x"]
 
     def stages(self):
         B, w, d = self.B, self.w, self.d
+        if self.path == "fused":
+            out = [("conv_scan_fwd", lambda: B.ssm_conv_scan_fwd(
+                d["sx"], d["c"], d["dt"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                s0=d["s0"], chunk=w.chunk, ws=self.ws_cf, out=(self.y, self.st, self.ck)))]
+            if not w.fwd_only:
+                out.append(("conv_scan_bwd", lambda: B.ssm_conv_scan_bwd(
+                    d["sx"], d["c"], d["dt"], d["A"], d["B"], d["C"], d["dy"], D=d["D"],
+                    z=d["z"], s0=d["s0"], ckpt=self.ck, d_state_out=d["d_state_out"],
+                    chunk=w.chunk, ws=self.ws_cb, out=self.gf)))
+            return out
         out = []
         if w.d_conv:
             out.append(("conv_fwd", lambda: B.ssm_conv_fwd(d["sx"], d["c"], None, silu=True,
@@ -624,11 +652,12 @@ def roofline_of(w, stage_ms, peaks, peak_src, sms, mhz) -> dict:
     return roof
 
 
-def measure_target(w, dev, flush, steps, warmup, peaks, with_oracle) -> dict:
-    """Stage times of another workload on this GPU (device-timed as the main line, L2 flushed
-    before every step), with its own clock record and, optionally, its oracle baseline."""
+def measure_target(w, dev, flush, steps, warmup, peaks, with_oracle, path="split") -> dict:
+    """Stage times of another workload (or of the other path) on this GPU (device-timed as the
+    main line, L2 flushed before every step), with its own clock record and, optionally, its
+    oracle baseline."""
     inp = make_inputs(w, grad_seed_state=False)
-    step = Step(w, dev, inp)
+    step = Step(w, dev, inp, path)
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
@@ -640,7 +669,8 @@ def measure_target(w, dev, flush, steps, warmup, peaks, with_oracle) -> dict:
     ms = sum(total) / len(total)
     stage_ms = {k: sum(v) / len(v) for k, v in per_stage.items()}
     rec = {"value": w.n_seqs * w.n_tok / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-           "steps": steps, "warmup": warmup, **stage_record(w, stage_ms, peaks),
+           "path": step.path, "steps": steps, "warmup": warmup,
+           **stage_record(w, stage_ms, peaks),
            "gpu_launches": int(launches), "clocks": clocks}
     del step
     if with_oracle:
@@ -660,7 +690,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-targets", action="store_true",
-                    help="skip the second target configuration's sub-record")
+                    help="skip the second target configuration's and the other path's sub-records")
+    ap.add_argument("--path", default="split", choices=["split", "fused"],
+                    help="split: conv fwd, scan fwd, scan bwd, conv bwd as four calls; fused: "
+                         "the conv1d+scan calls (x not kept between forward and backward)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.config] if args.config is not None else workload(args.workload)
@@ -684,7 +717,7 @@ def main():
         dist.barrier()
 
     inp = make_inputs(w, grad_seed_state=False)
-    step = Step(w, dev, inp)
+    step = Step(w, dev, inp, args.path)
     flush = l2_flush_buffer(dev)
 
     sampler = ClockSampler(local)
@@ -703,7 +736,7 @@ def main():
 
     e2e_steps = max(3, min(args.steps, 20))
     serial_ms = reduce_max(time_e2e_serial(step, e2e_steps, 2), dist, dev)
-    e2e_ms, h2d, d2h = time_e2e((step, Step(w, dev, inp)), e2e_steps, 2)
+    e2e_ms, h2d, d2h = time_e2e((step, Step(w, dev, inp, args.path)), e2e_steps, 2)
     e2e_ms = reduce_max(e2e_ms, dist, dev)
 
     if rank != 0:
@@ -722,7 +755,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.io == "bf16" else "f32", "data": "synthetic",
-        "config": config_of(w, world),
+        "config": config_of(w, world), "path": step.path,
         **stage_record(w, stage_ms, peaks),
         "roofline": roofline,
         "gpu_launches": int(launches),
@@ -741,6 +774,10 @@ def main():
                 line["targets"][name] = measure_target(workload(name), dev, flush,
                                                        min(args.steps, 50), args.warmup,
                                                        peaks, not args.no_cpu_baseline)
+    if world == 1 and not args.no_targets and w.d_conv and not w.fwd_only:
+        other = "fused" if step.path == "split" else "split"
+        line["other_path"] = measure_target(w, dev, flush, min(args.steps, 50), args.warmup,
+                                            peaks, False, other)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(line))

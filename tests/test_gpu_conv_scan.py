@@ -153,11 +153,14 @@ def test_conv_scan_backward_parity(case):
     assert binding.ssm_scan_status(g["_ws"]) == 0
 
 
-@pytest.mark.parametrize("name", ["mamba1_long_bf16_b1_l16384_d2048_n16",
+@pytest.mark.parametrize("name", ["mamba1_layer_f32_b8_l1024_d512_n16",
+                                  "mamba1_long_bf16_b1_l16384_d2048_n16",
                                   "mamba1_train_bf16_b16_l2048_d1536_n16"])
 def test_conv_scan_full_size_sampled_channels(name):
-    """The benchmark workloads at full size through the fused calls; the oracle runs the
-    sampled channels (each channel's conv and scan are independent of the others)."""
+    """The Mamba-1 workloads (d_inner 512 x 8 x 1024 fp32, 2048 x 1 x 16384 and 1536 x 16 x
+    2048 bf16) at full size through the fused calls, in the launch configuration the benchmark
+    uses; the oracle runs the sampled channels (each channel's conv and scan are independent of
+    the others)."""
     w = workload(name)
     inp = make_inputs(w, grad_seed_state=True)
     d = _gpu(inp)
