@@ -5,9 +5,11 @@
 // A block = 128 threads = 32 channels of one head x 128 states, one sequence, one time segment;
 // a thread holds a 4-channel x 8-state tile (the forward's tile, scan_fwd_heads.cu).  Per chunk
 // (last to first): level 1 walks the chunk's 16-token tiles forward from the checkpoint and keeps
-// every tile's start state; level 2 walks the tiles in reverse, recomputes the tile's 16 states
-// into a per-block scratch history (a thread's 32 states x 16 tokens do not fit in registers) and
-// runs the adjoint over them:
+// the state at every 8-token half-tile start (global scratch); level 2 walks the tiles in
+// reverse, and per half-tile recomputes its 8 states into tensor memory (a thread's 32 states x
+// 8 tokens: 256 columns of its lane, half the SM's, which register pressure leaves at 2 blocks
+// per SM anyway) and runs the adjoint over them, reading each h_{t-1} back with one 32-column
+// load:
 //   dh = gy C + carry,  carry <- a dh,  w = carry h_prev
 //   dx = gy D + delta sum_n dh B,  ddelta_head = sum_p x sum_n dh B + A sum_{p,n} w,
 //   dA_head += delta sum_{p,n} w,  dB_t = sum_{h,p} dh delta x,  dC_t = sum_{h,p} gy h
@@ -16,6 +18,7 @@
 // 4 tokens, in a fixed order, then over blocks by reduce_bc_kernel.  Segments, their adjoint carry
 // and the d_s0 reduction are the general backward's (scan_bwd.cu).
 #include "scan_bwd.cuh"
+#include "tmem.cuh"
 
 namespace ssm {
 
@@ -28,6 +31,8 @@ constexpr int kBhN = 128;    // d_state
 constexpr int kBhTP = 4;     // channels per thread
 constexpr int kBhTN = 8;     // states per thread
 constexpr int kBhTile = 16;  // tokens per tile
+constexpr int kBhSub = 8;    // tokens per half-tile (the history held in tensor memory)
+constexpr uint32_t kBhTmCols = 256;  // 8 records x 32 states per lane
 constexpr int kBhGrp = 4;    // tokens per shared-memory dB/dC sum
 constexpr int kBhTS = kBhTP * kBhTN;  // states per thread
 
@@ -36,8 +41,7 @@ struct BhArgs {
   int bph;         // blocks per head (P / 32)
   int bpg;         // blocks per group ((H / G) * bph)
   int vec;         // x, dy, z, B, C allow 4-element vector loads
-  float* bnd;      // [blocks][S][tiles per chunk][threads][32]  tile start states
-  float* hist;     // [blocks][S][16][threads][32]               states after each token
+  float* bnd;      // [blocks][S][half-tiles per chunk][threads][32]  half-tile start states
   float* part_dd;  // [ns * L][H][bph]   d delta partial of the block (before softplus')
   float* dA_blk;   // [ns][S][H][bph]
 };
@@ -180,6 +184,50 @@ __device__ __forceinline__ float bh_sum16_transposed(const float (&v)[8], int la
   return y + __shfl_xor_sync(0xffffffffu, y, 1);
 }
 
+// A thread's 32 states to / from 32 columns of its tensor-memory lane (one warp-wide access).
+__device__ __forceinline__ void bh_tm_store(uint32_t taddr, const f2_t (&v)[kBhTP][kBhTN / 2]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int c = 0; c < kBhTP; c++)
+#pragma unroll
+    for (int q = 0; q < kBhTN / 2; q++) {
+      float lo, hi;
+      f2_unpack(v[c][q], lo, hi);
+      r[c * kBhTN + 2 * q] = __float_as_uint(lo);
+      r[c * kBhTN + 2 * q + 1] = __float_as_uint(hi);
+    }
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void bh_tm_load(uint32_t taddr, f2_t (&v)[kBhTP][kBhTN / 2]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int c = 0; c < kBhTP; c++)
+#pragma unroll
+    for (int q = 0; q < kBhTN / 2; q++)
+      v[c][q] = f2_pack(__uint_as_float(r[c * kBhTN + 2 * q]),
+                        __uint_as_float(r[c * kBhTN + 2 * q + 1]));
+}
+
 // A thread's 32 states (4 channels x 8 states as 16 pairs) to / from a scratch slot.
 __device__ __forceinline__ void bh_store(float* slot, const f2_t (&v)[kBhTP][kBhTN / 2]) {
   float4* d = reinterpret_cast<float4*>(slot);
@@ -225,12 +273,19 @@ scan_bwd_heads_kernel(const BhArgs A) {
   const int c_first = s * a.seg_chunks, c_last = min(a.nch_b, c_first + a.seg_chunks) - 1;
   const float Ah = __ldg(p.A + h), A2 = Ah * kLog2e;
   const float bias = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + h) : 0.0f;
-  const int tpc_chunk = a.chunk_b / TT;
+  const int hpc_chunk = a.chunk_b / kBhSub;
   const long blk = ((long)b * a.S + s) * gridDim.x + blockIdx.x;
-  float* bnd = A.bnd + blk * tpc_chunk * kBhThreads * kBhTS;
-  float* hist = A.hist + blk * TT * kBhThreads * kBhTS;
+  float* bnd = A.bnd + blk * hpc_chunk * kBhThreads * kBhTS;
   auto bnd_slot = [&](int j) { return bnd + ((long)j * kBhThreads + tid) * kBhTS; };
-  auto hist_slot = [&](int i) { return hist + ((long)i * kBhThreads + tid) * kBhTS; };
+  // the half-tile history: record k (the state after token k of the half-tile) in columns
+  // 32 k .. 32 k + 31 of this thread's lane
+  __shared__ uint32_t sTmem;
+  __syncwarp();
+  if (warp == 0) tmem_alloc(&sTmem, kBhTmCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tm = sTmem + ((uint32_t)(warp * 32) << 16);
 
   f2_t carry[kBhTP][kBhTN / 2];
 #pragma unroll
@@ -271,8 +326,8 @@ scan_bwd_heads_kernel(const BhArgs A) {
     for (int j = 0; j < nt; j++) {
       const int t0 = t0c + j * TT, cnt = min(TT, t1c - t0);
       bh_load_tile<IO, ACC>(A, S, (long)b * p.L + t0, cnt, ch0, h, g, A2, bias, false);
-      bh_store(bnd_slot(j), hv);
       for (int i = 0; i < cnt; i++) {
+        if (i % kBhSub == 0) bh_store(bnd_slot(2 * j + i / kBhSub), hv);
         const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
         const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
         const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
@@ -288,118 +343,117 @@ scan_bwd_heads_kernel(const BhArgs A) {
         }
       }
     }
-    // ---- level 2: tiles in reverse: recompute into the history, then the adjoint -----------
+    // ---- level 2: tiles in reverse; per half-tile, recompute into tensor memory, then the
+    // adjoint over it ----------------------------------------------------------------------
     for (int j = nt - 1; j >= 0; j--) {
       const int t0 = t0c + j * TT, cnt = min(TT, t1c - t0);
       const long tok0 = (long)b * p.L + t0;
       bh_load_tile<IO, ACC>(A, S, tok0, cnt, ch0, h, g, A2, bias, true);
-      bh_load(bnd_slot(j), hv);
-      for (int i = 0; i < cnt; i++) {
-        const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
-        const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
-                            f2_pack(b1.z, b1.w)};
-        const float4 dx = *reinterpret_cast<const float4*>(&S.dlx[i][pl0]);
-        const float dxs[4] = {dx.x, dx.y, dx.z, dx.w};
+      for (int hf = (cnt - 1) / kBhSub; hf >= 0; hf--) {
+        const int i_lo = hf * kBhSub, i_hi = min(cnt, i_lo + kBhSub);
+        bh_load(bnd_slot(2 * j + hf), hv);
+        for (int i = i_lo; i < i_hi; i++) {
+          const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
+          const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
+          const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
+          const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                              f2_pack(b1.z, b1.w)};
+          const float4 dx = *reinterpret_cast<const float4*>(&S.dlx[i][pl0]);
+          const float dxs[4] = {dx.x, dx.y, dx.z, dx.w};
 #pragma unroll
-        for (int c = 0; c < kBhTP; c++) {
-          const f2_t dx2 = f2_pack(dxs[c], dxs[c]);
+          for (int c = 0; c < kBhTP; c++) {
+            const f2_t dx2 = f2_pack(dxs[c], dxs[c]);
 #pragma unroll
-          for (int q = 0; q < kBhTN / 2; q++) hv[c][q] = step2<ACC>(cf2, hv[c][q], f2_mul(dx2, B2[q]));
-        }
-        bh_store(hist_slot(i), hv);
-      }
-      // hv = state after the tile's last token: h_t of the first adjoint step.  h_{t-1} of
-      // step i is loaded one step ahead (hn), so the scratch latency overlaps a step's work.
-      f2_t hn[kBhTP][kBhTN / 2];
-      bh_load(cnt > 1 ? hist_slot(cnt - 2) : bnd_slot(j), hn);
-      for (int i = cnt - 1; i >= 0; i--) {
-        f2_t hp[kBhTP][kBhTN / 2];
-#pragma unroll
-        for (int c = 0; c < kBhTP; c++)
-#pragma unroll
-          for (int q = 0; q < kBhTN / 2; q++) hp[c][q] = hn[c][q];  // h_{t-1}
-        if (i > 0) bh_load(i > 1 ? hist_slot(i - 2) : bnd_slot(j), hn);
-        const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
-        const float dl = S.tc[i][1];
-        const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
-        const float4 c0 = *reinterpret_cast<const float4*>(&S.C[i][n0]);
-        const float4 c1 = *reinterpret_cast<const float4*>(&S.C[i][n0 + 4]);
-        const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
-                            f2_pack(b1.z, b1.w)};
-        const f2_t C2[4] = {f2_pack(c0.x, c0.y), f2_pack(c0.z, c0.w), f2_pack(c1.x, c1.y),
-                            f2_pack(c1.z, c1.w)};
-        const float4 gyv = *reinterpret_cast<const float4*>(&S.gy[i][pl0]);
-        const float4 dlxv = *reinterpret_cast<const float4*>(&S.dlx[i][pl0]);
-        const float gys[4] = {gyv.x, gyv.y, gyv.z, gyv.w};
-        const float dlxs[4] = {dlxv.x, dlxv.y, dlxv.z, dlxv.w};
-        f2_t dB2[4] = {0ull, 0ull, 0ull, 0ull}, dC2[4] = {0ull, 0ull, 0ull, 0ull}, w2 = 0ull;
-        float v8[8];
-#pragma unroll
-        for (int c = 0; c < kBhTP; c++) {
-          const f2_t gy2 = f2_pack(gys[c], gys[c]), dlx2 = f2_pack(dlxs[c], dlxs[c]);
-          f2_t sb = 0ull, yp = 0ull;
-#pragma unroll
-          for (int q = 0; q < kBhTN / 2; q++) {
-            const f2_t dh = f2_fma(gy2, C2[q], carry[c][q]);
-            sb = f2_fma(dh, B2[q], sb);
-            dB2[q] = f2_fma(dh, dlx2, dB2[q]);
-            dC2[q] = f2_fma(gy2, hv[c][q], dC2[q]);
-            yp = f2_fma(C2[q], hv[c][q], yp);
-            const f2_t cn = apply2<ACC>(cf2, dh);
-            w2 = f2_fma(cn, hp[c][q], w2);
-            carry[c][q] = cn;
+            for (int q = 0; q < kBhTN / 2; q++) hv[c][q] = step2<ACC>(cf2, hv[c][q], f2_mul(dx2, B2[q]));
           }
-          v8[c] = f2_sum(sb);
-          v8[4 + c] = f2_sum(yp);
+          if (i + 1 < i_hi) bh_tm_store(tm + 32u * (uint32_t)(i - i_lo), hv);
         }
-        const float wsum = f2_sum(w2);
-        dA_acc = fmaf(dl, wsum, dA_acc);
-        // per channel: sum over the 128 states (lanes 0..15 of the half-warp)
-        const float tot = bh_sum16_transposed(v8, lane);
-        if ((lane & 1) == 0) {
-          const int k = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-          S.q[i][pl0 + (k & 3)][k >> 2] = tot;
-        }
-        // dB, dC: sum over the warp's two channel groups (lane bit 4), transposed
-        {
-          const bool u4 = lane & 16;
-          float r[8];
+        tmem_wait_st();
+        // hv = the state after the half-tile's last token: h_t of its first adjoint step
+        for (int i = i_hi - 1; i >= i_lo; i--) {
+          f2_t hp[kBhTP][kBhTN / 2];  // h_{t-1}
+          if (i > i_lo) bh_tm_load(tm + 32u * (uint32_t)(i - 1 - i_lo), hp);
+          else bh_load(bnd_slot(2 * j + hf), hp);
+          const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
+          const float dl = S.tc[i][1];
+          const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
+          const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
+          const float4 c0 = *reinterpret_cast<const float4*>(&S.C[i][n0]);
+          const float4 c1 = *reinterpret_cast<const float4*>(&S.C[i][n0 + 4]);
+          const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                              f2_pack(b1.z, b1.w)};
+          const f2_t C2[4] = {f2_pack(c0.x, c0.y), f2_pack(c0.z, c0.w), f2_pack(c1.x, c1.y),
+                              f2_pack(c1.z, c1.w)};
+          const float4 gyv = *reinterpret_cast<const float4*>(&S.gy[i][pl0]);
+          const float4 dlxv = *reinterpret_cast<const float4*>(&S.dlx[i][pl0]);
+          const float gys[4] = {gyv.x, gyv.y, gyv.z, gyv.w};
+          const float dlxs[4] = {dlxv.x, dlxv.y, dlxv.z, dlxv.w};
+          f2_t dB2[4] = {0ull, 0ull, 0ull, 0ull}, dC2[4] = {0ull, 0ull, 0ull, 0ull}, w2 = 0ull;
+          float v8[8];
 #pragma unroll
-          for (int q = 0; q < 4; q++) {
-            float b_lo, b_hi, c_lo, c_hi;
-            f2_unpack(dB2[q], b_lo, b_hi);
-            f2_unpack(dC2[q], c_lo, c_hi);
-            r[2 * q] = (u4 ? c_lo : b_lo) + __shfl_xor_sync(0xffffffffu, u4 ? b_lo : c_lo, 16);
-            r[2 * q + 1] = (u4 ? c_hi : b_hi) + __shfl_xor_sync(0xffffffffu, u4 ? b_hi : c_hi, 16);
-          }
-          float* dst = &S.red[i % kBhGrp][warp][(u4 ? N : 0) + n0];
-          *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(r[4], r[5], r[6], r[7]);
-        }
-        // sum of w over the warp
-        float wv = wsum;
+          for (int c = 0; c < kBhTP; c++) {
+            const f2_t gy2 = f2_pack(gys[c], gys[c]), dlx2 = f2_pack(dlxs[c], dlxs[c]);
+            f2_t sb = 0ull, yp = 0ull;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) wv += __shfl_xor_sync(0xffffffffu, wv, off);
-        if (lane == 0) S.w[i][warp] = wv;
-#pragma unroll
-        for (int c = 0; c < kBhTP; c++)
-#pragma unroll
-          for (int q = 0; q < kBhTN / 2; q++) hv[c][q] = hp[c][q];
-        if (i % kBhGrp == 0) {  // tokens i .. i+3 complete: dB, dC of the block, fixed order
-          __syncthreads();
-          for (int o = tid; o < kBhGrp * 2 * N; o += kBhThreads) {
-            const int k = o / (2 * N), r = o - k * 2 * N;
-            if (i + k < cnt) {
-              float v = 0.0f;
-#pragma unroll
-              for (int w = 0; w < kBhWarps; w++) v += S.red[k][w][r];
-              a.part_bc[(((tok0 + i + k) * p.G + g) * A.bpg + big) * 2 * N + r] = v;
+            for (int q = 0; q < kBhTN / 2; q++) {
+              const f2_t dh = f2_fma(gy2, C2[q], carry[c][q]);
+              sb = f2_fma(dh, B2[q], sb);
+              dB2[q] = f2_fma(dh, dlx2, dB2[q]);
+              dC2[q] = f2_fma(gy2, hv[c][q], dC2[q]);
+              yp = f2_fma(C2[q], hv[c][q], yp);
+              const f2_t cn = apply2<ACC>(cf2, dh);
+              w2 = f2_fma(cn, hp[c][q], w2);
+              carry[c][q] = cn;
             }
+            v8[c] = f2_sum(sb);
+            v8[4 + c] = f2_sum(yp);
           }
-          __syncthreads();
+          const float wsum = f2_sum(w2);
+          dA_acc = fmaf(dl, wsum, dA_acc);
+          // per channel: sum over the 128 states (lanes 0..15 of the half-warp)
+          const float tot = bh_sum16_transposed(v8, lane);
+          if ((lane & 1) == 0) {
+            const int k = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+            S.q[i][pl0 + (k & 3)][k >> 2] = tot;
+          }
+          // dB, dC: sum over the warp's two channel groups (lane bit 4), transposed
+          {
+            const bool u4 = lane & 16;
+            float r[8];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              float b_lo, b_hi, c_lo, c_hi;
+              f2_unpack(dB2[q], b_lo, b_hi);
+              f2_unpack(dC2[q], c_lo, c_hi);
+              r[2 * q] = (u4 ? c_lo : b_lo) + __shfl_xor_sync(0xffffffffu, u4 ? b_lo : c_lo, 16);
+              r[2 * q + 1] = (u4 ? c_hi : b_hi) + __shfl_xor_sync(0xffffffffu, u4 ? b_hi : c_hi, 16);
+            }
+            float* dst = &S.red[i % kBhGrp][warp][(u4 ? N : 0) + n0];
+            *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(r[4], r[5], r[6], r[7]);
+          }
+          // sum of w over the warp
+          float wv = wsum;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) wv += __shfl_xor_sync(0xffffffffu, wv, off);
+          if (lane == 0) S.w[i][warp] = wv;
+#pragma unroll
+          for (int c = 0; c < kBhTP; c++)
+#pragma unroll
+            for (int q = 0; q < kBhTN / 2; q++) hv[c][q] = hp[c][q];
+          if (i % kBhGrp == 0) {  // tokens i .. i+3 complete: dB, dC of the block, fixed order
+            __syncthreads();
+            for (int o = tid; o < kBhGrp * 2 * N; o += kBhThreads) {
+              const int k = o / (2 * N), r = o - k * 2 * N;
+              if (i + k < cnt) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kBhWarps; w++) v += S.red[k][w][r];
+                a.part_bc[(((tok0 + i + k) * p.G + g) * A.bpg + big) * 2 * N + r] = v;
+              }
+            }
+            __syncthreads();
+          }
         }
       }
       // ---- epilogue of the tile: dx, dz per (token, channel); the block's d delta per token --
@@ -431,7 +485,10 @@ scan_bwd_heads_kernel(const BhArgs A) {
   }
 
   // ---- per block: dD per channel, dA of the head, d s0 ---------------------------------------
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 0) tmem_dealloc(sTmem, kBhTmCols);
   S.dd[tid] = dD_acc;
   __syncthreads();
   if (tid < kBhP && a.g.d_D) {
@@ -532,7 +589,7 @@ int bwd_heads_blocks(const ScanProblem& p) { return p.ns * p.H * (p.P / kBhP); }
 
 size_t bwd_heads_scratch_floats(const ScanProblem& p, int S, int chunk_b) {
   const size_t blocks = (size_t)bwd_heads_blocks(p) * S;
-  return blocks * ((size_t)(chunk_b / kBhTile) + kBhTile) * kBhThreads * kBhTS;
+  return blocks * (size_t)(chunk_b / kBhSub) * kBhThreads * kBhTS;
 }
 
 // Main pass and reductions of the Mamba-2-form backward (segments' local adjoint and carry
@@ -545,18 +602,34 @@ cudaError_t launch_bwd_heads(const BwdArgs& a, float* scratch, cudaStream_t st) 
   A.bpg = (p.H / p.G) * A.bph;
   A.a.bpg = A.bpg;  // part_bc is laid out per head-tiled block
   const size_t blocks = (size_t)bwd_heads_blocks(p) * a.S;
+  (void)blocks;
   A.bnd = scratch;
-  A.hist = scratch + blocks * (size_t)(a.chunk_b / kBhTile) * kBhThreads * kBhTS;
   A.part_dd = a.ddt_part;
   const uintptr_t al = p.io == SSM_BF16 ? 8 : 16;
   auto ok = [&](const void* q) { return q == nullptr || ((uintptr_t)q % al) == 0; };
   A.vec = ok(p.x) && ok(a.g.dy) && ok(p.z) && ok(p.B) && ok(p.C);
   A.dA_blk = a.dA_part;
   const dim3 grid(p.H * A.bph, a.S, p.ns);
+  // Each block holds kBhTmCols of the SM's 512 columns of tensor memory; unused dynamic shared
+  // memory keeps a third block off the SM (it would only wait in the allocation).
+  const void* kern = p.io == SSM_BF16 ? reinterpret_cast<const void*>(scan_bwd_heads_kernel<__nv_bfloat16>)
+                                      : reinterpret_cast<const void*>(scan_bwd_heads_kernel<float>);
+  cudaFuncAttributes fa;
+  int dev = 0, smem_sm = 0, reserved = 0;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e != cudaSuccess) return e;
+  const int max_blocks = (int)(512u / kBhTmCols);
+  const long need = (long)smem_sm / (max_blocks + 1) + 1 - (long)fa.sharedSizeBytes - reserved;
+  const size_t dyn = need > 0 ? (size_t)need : 0;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
   if (p.io == SSM_BF16)
-    scan_bwd_heads_kernel<__nv_bfloat16><<<grid, kBhThreads, 0, st>>>(A), count_launches(1);
+    scan_bwd_heads_kernel<__nv_bfloat16><<<grid, kBhThreads, dyn, st>>>(A), count_launches(1);
   else
-    scan_bwd_heads_kernel<float><<<grid, kBhThreads, 0, st>>>(A), count_launches(1);
+    scan_bwd_heads_kernel<float><<<grid, kBhThreads, dyn, st>>>(A), count_launches(1);
   const long nbc = (long)p.ns * p.L * p.G * 2 * p.N;
   const int bbc = (int)((nbc + 255) / 256 < 8192 ? (nbc + 255) / 256 : 8192);
   const long ndt = (long)p.ns * p.L * p.H;
