@@ -691,12 +691,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-targets", action="store_true",
                     help="skip the second target configuration's and the other path's sub-records")
+    ap.add_argument("--backward", action="store_true",
+                    help="run the backward too on a forward-only workload (the Mamba-2 form)")
     ap.add_argument("--path", default="split", choices=["split", "fused"],
                     help="split: conv fwd, scan fwd, scan bwd, conv bwd as four calls; fused: "
                          "the conv1d+scan calls (x not kept between forward and backward)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.config] if args.config is not None else workload(args.workload)
+    if args.backward and w.fwd_only:
+        w = w.with_(fwd_only=False)
     if args.impl == "reference":
         run_reference(args, w)
         return

@@ -21,6 +21,7 @@ SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_WORKSPACE = 0, -1, -2,
 SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NONFINITE = -4, -5, -6
 SSM_CONV_SILU, SSM_DT_SOFTPLUS, SSM_CHECK_FINITE, SSM_A_LOG = 1, 2, 4, 8
 SSM_DEBUG_NO_WAIT = 16  # tests of the timeout path only (include/ssm.h)
+SSM_SCAN_CHUNKED = 32   # the Mamba-2 form's bf16 forward in chunked matrix form (tensor cores)
 
 EXPORTED = ("ssm_conv_fwd", "ssm_conv_workspace_size", "ssm_conv_bwd", "ssm_scan_workspace_size",
             "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv_scan_workspace_size", "ssm_conv_scan_fwd",
@@ -193,13 +194,13 @@ class ScanShape:
 
 
 def scan_shape(x, dt, A, B, s0=None, chunk=256, softplus=False, check_finite=False,
-               state_rows=0, a_log=False, debug_flags=0) -> ScanShape:
+               state_rows=0, a_log=False, debug_flags=0, chunked=False) -> ScanShape:
     n_s, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     a_per_state = 1 if A.dim() == 2 else 0
     rows = state_rows if state_rows else (s0.shape[0] if s0 is not None else 0)
     flags = ((SSM_DT_SOFTPLUS if softplus else 0) | (SSM_CHECK_FINITE if check_finite else 0) |
-             (SSM_A_LOG if a_log else 0) | debug_flags)
+             (SSM_A_LOG if a_log else 0) | (SSM_SCAN_CHUNKED if chunked else 0) | debug_flags)
     return ScanShape(n_s, L, H, P, N, G, a_per_state, rows, chunk, _io_of(x), flags)
 
 
@@ -210,10 +211,11 @@ def ssm_scan_workspace_size(shape: ScanShape, backward: bool) -> int:
 
 def ssm_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, s0=None, ids=None, chunk=256,
                  softplus=False, check_finite=False, want_ckpt=True, state_rows=0, ws=None,
-                 out=None, stream=None, a_log=False):
+                 out=None, stream=None, a_log=False, chunked=False):
     """Returns (y, state_out, ckpt).  ``out`` = (y, state_out, ckpt) preallocated, optional.
-    ``a_log``: A holds A_log (the scan uses -exp(A_log))."""
-    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log)
+    ``a_log``: A holds A_log (the scan uses -exp(A_log)).  ``chunked``: SSM_SCAN_CHUNKED."""
+    sh = scan_shape(x, dt, A, B, s0, chunk, softplus, check_finite, state_rows, a_log,
+                    chunked=chunked)
     io = x.dtype
     dev = x.device
     if out is None:

@@ -57,7 +57,8 @@ int scan_problem(const ssm_scan_desc* d, int backward, ScanProblem* p) {
   if (d->n_head % d->n_group != 0) return SSM_ERR_INVALID_ARG;
   if (d->a_per_state != 0 && d->a_per_state != 1) return SSM_ERR_INVALID_ARG;
   if (!io_size(d->io)) return SSM_ERR_INVALID_ARG;
-  if (d->flags & ~(unsigned)(SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG | SSM_DEBUG_NO_WAIT))
+  if (d->flags & ~(unsigned)(SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG | SSM_DEBUG_NO_WAIT |
+                             SSM_SCAN_CHUNKED))
     return SSM_ERR_INVALID_ARG;
   if (d->d_state > (backward ? SSM_MAX_D_STATE_BWD : SSM_MAX_D_STATE)) return SSM_ERR_UNSUPPORTED;
   const long long HP = (long long)d->n_head * d->head_dim;
@@ -77,6 +78,7 @@ int scan_problem(const ssm_scan_desc* d, int backward, ScanProblem* p) {
   p->softplus = (d->flags & SSM_DT_SOFTPLUS) ? 1 : 0;
   p->check_finite = (d->flags & SSM_CHECK_FINITE) ? 1 : 0;
   p->debug_flags = (d->flags & SSM_DEBUG_NO_WAIT) ? ssm::kDebugNoWait : 0;
+  p->chunked = (d->flags & SSM_SCAN_CHUNKED) ? 1 : 0;
   p->state_rows = d->state_rows > 0 ? d->state_rows : d->n_seqs;
   p->chunk = d->chunk > 0 ? d->chunk : 256;
   p->n_chunks = (p->L + p->chunk - 1) / p->chunk;

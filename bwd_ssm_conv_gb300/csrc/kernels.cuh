@@ -22,6 +22,7 @@ struct ScanProblem {
   int state_rows, chunk, n_chunks;
   int io;
   int debug_flags;  // kDebugNoWait: cross-block waits give up at once (tests of the timeout path)
+  int chunked;      // SSM_SCAN_CHUNKED: the Mamba-2 form's bf16 forward in chunked matrix form
   const float* s0;
   const int* ids;
   const void* x;
@@ -45,8 +46,10 @@ struct ScanProblem {
 constexpr int kDebugNoWait = 1;
 
 // Forward.  y may be NULL (states / checkpoints only), state_out may be NULL, ckpt may be NULL.
-// launch_scan_fwd takes a TMA-staged path when one applies: scan_fwd_tma.cu (head_dim 1) or
-// scan_fwd_heads.cu (one A per head, head_dim a multiple of 64, d_state 128).
+// launch_scan_fwd takes a fast path when one applies: scan_fwd_tma.cu (head_dim 1),
+// scan_fwd_heads.cu (one A per head, head_dim a multiple of 64, d_state 128), or, asked for
+// with SSM_SCAN_CHUNKED, scan_fwd_ssd.cu (the same shapes with bf16 I/O in chunked matrix form
+// on the tensor cores).
 size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms);
 size_t scan_fwd_tma_ws_bytes(const ScanProblem& p, int num_sms);  // 0: path does not apply
 cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out, float* ckpt,
@@ -54,6 +57,12 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
 size_t scan_fwd_heads_ws_bytes(const ScanProblem& p, int num_sms);  // 0: path does not apply
 cudaError_t launch_scan_fwd_heads(const ScanProblem& p, void* y, float* state_out, float* ckpt,
                                   void* ws, int num_sms, cudaStream_t st);
+// scan_fwd_ssd.cu: the Mamba-2 form in chunked matrix form on the tensor cores (SSM_SCAN_CHUNKED;
+// bf16 I/O, one A per head, head_dim a multiple of 64, d_state 128, checkpoint interval a
+// multiple of 64).
+size_t scan_fwd_ssd_ws_bytes(const ScanProblem& p);  // 0: path does not apply
+cudaError_t launch_scan_fwd_ssd(const ScanProblem& p, void* y, float* state_out, float* ckpt,
+                                void* ws, cudaStream_t st);
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st);
 

@@ -184,8 +184,10 @@ static FwdPlan plan_fwd(const ScanProblem& p, int num_sms) {
 
 size_t scan_fwd_ws_bytes(const ScanProblem& p, int num_sms) {
   size_t a = plan_fwd(p, num_sms).bytes;
-  const size_t b = scan_fwd_tma_ws_bytes(p, num_sms), c = scan_fwd_heads_ws_bytes(p, num_sms);
+  const size_t b = scan_fwd_tma_ws_bytes(p, num_sms), c = scan_fwd_heads_ws_bytes(p, num_sms),
+               d = scan_fwd_ssd_ws_bytes(p);
   if (b > a) a = b;
+  if (d > a) a = d;
   return c > a ? c : a;
 }
 
@@ -227,6 +229,8 @@ static void launch_fwd_io(const FwdArgs& a, int ns_state, int blocks_x, bool ful
 cudaError_t launch_scan_fwd(const ScanProblem& p, void* y, float* state_out, float* ckpt, void* ws,
                             int num_sms, cudaStream_t st) {
   cudaError_t e = launch_scan_fwd_tma(p, y, state_out, ckpt, ws, num_sms, st);
+  if (e != cudaErrorNotSupported) return e;
+  e = launch_scan_fwd_ssd(p, y, state_out, ckpt, ws, st);
   if (e != cudaErrorNotSupported) return e;
   e = launch_scan_fwd_heads(p, y, state_out, ckpt, ws, num_sms, st);
   if (e != cudaErrorNotSupported) return e;

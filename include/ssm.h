@@ -94,10 +94,18 @@ enum {
                             dL/dA * A.  The workspace grows by a buffer for A: the
                             *_workspace_size results include it; ssm_decode_step then needs
                             ws_bytes >= 256 + 4 * (elements of A) rounded up to 256. */
-  SSM_DEBUG_NO_WAIT = 16u /* scan, for tests of the error path only: every wait of a block on
-                            another block gives up at once, as if its bound had run out; the
-                            call then records SSM_ERR_TIMEOUT and its outputs are incomplete.
-                            Waits for this block's own copies keep their normal bound. */
+  SSM_DEBUG_NO_WAIT = 16u, /* scan, for tests of the error path only: every wait of a block on
+                             another block gives up at once, as if its bound had run out; the
+                             call then records SSM_ERR_TIMEOUT and its outputs are incomplete.
+                             Waits for this block's own copies keep their normal bound. */
+  SSM_SCAN_CHUNKED = 32u   /* scan forward, Mamba-2 form with bf16 I/O (one A per head, head_dim
+                              a multiple of 64, d_state 128, chunk a multiple of 64): compute it
+                              in chunked matrix form on the tensor cores (64-token chunks, tf32
+                              products with the computed operands split into two terms) instead
+                              of as a recurrence.  Same results to bf16 rounding; the workspace
+                              then holds every 64-token chunk's state in fp32.  Other shapes
+                              ignore the flag.  (ggmlR ssm_scan with a [1, n_head] A; the chunk
+                              composition is that of kizzasi's associative scan.) */
 };
 
 /* Limits (checked on the host; SSM_ERR_UNSUPPORTED beyond them).  Every tensor must also
@@ -117,7 +125,8 @@ typedef struct {
   int state_rows;   /* rows of s0 / d_s0; 0 means n_seqs.  Without ids, must be >= n_seqs */
   int chunk;        /* checkpoint interval in tokens; 0 means 256 */
   int io;           /* ssm_dtype of the activations */
-  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG | SSM_DEBUG_NO_WAIT */
+  unsigned flags;   /* SSM_DT_SOFTPLUS | SSM_CHECK_FINITE | SSM_A_LOG | SSM_DEBUG_NO_WAIT |
+                       SSM_SCAN_CHUNKED */
 } ssm_scan_desc;
 
 /* ---- causal depthwise conv1d (+bias, +SiLU) --------------------------------------------

@@ -45,7 +45,7 @@ def nan_like(t, shape=None, dtype=None):
                       dtype=dtype or t.dtype, device="cuda")
 
 
-def gpu_fwd(inp, chunk, softplus=False, ids=None, state_rows=0, want_ckpt=True):
+def gpu_fwd(inp, chunk, softplus=False, ids=None, state_rows=0, want_ckpt=True, chunked=False):
     d = cuda(inp)
     ns, L, H, P = inp["x"].shape
     N = inp["B"].shape[3]
@@ -56,7 +56,7 @@ def gpu_fwd(inp, chunk, softplus=False, ids=None, state_rows=0, want_ckpt=True):
                                 z=d.get("z"), dt_bias=d.get("dt_bias"), s0=d.get("s0"),
                                 ids=None if ids is None else ids.cuda(), chunk=chunk,
                                 softplus=softplus, want_ckpt=want_ckpt, state_rows=state_rows,
-                                out=out)
+                                out=out, chunked=chunked)
 
 
 def gpu_bwd(inp, chunk, ckpt=None, softplus=False, ids=None, state_rows=0, d_state_out=True,
