@@ -295,3 +295,29 @@ def test_workload_full_size_sampled_channels(name):
     os_ = oracle_bwd(channel_subset(sparse, idx), w.chunk)
     assert_close("d_B", gs["d_B"], os_["d_B"], tol(w.io, True))
     assert_close("d_C", gs["d_C"], os_["d_C"], tol(w.io, True))
+
+
+@pytest.mark.parametrize("shape,io,scalar_a", [
+    ((1, 40, 4, 1, 512, 1), "f32", False),     # the forward's largest d_state, per-state A
+    ((2, 33, 2, 4, 512, 2), "bf16", True),     # ... one A per head, groups, bf16
+])
+def test_scan_forward_largest_d_state(shape, io, scalar_a):
+    """d_state at SSM_MAX_D_STATE (512): the general forward, ragged tokens, against the oracle."""
+    inp = _inputs(shape, io, scalar_a, False, seed=17)
+    y, st, ck = gpu_fwd(inp, 16)
+    yo, so, co = oracle_fwd(inp, 16)
+    t = tol(io, grad=False)
+    assert_close("y", y, yo, t)
+    assert_close("state_out", st, so, t)
+    assert_close("ckpt", ck, co, t)
+
+
+def test_scan_backward_largest_d_state():
+    """d_state at SSM_MAX_D_STATE_BWD (128) with per-state A (the general backward kernels)."""
+    inp = _inputs((2, 45, 3, 2, 128, 1), "f32", False, False, seed=19)
+    _, _, ck = gpu_fwd(inp, 16)
+    g = gpu_bwd(inp, 16, ckpt=ck)
+    o = oracle_bwd(inp, 16)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], tol("f32", grad=True))
