@@ -45,10 +45,15 @@ struct BwdTma {
   uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
   uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
-  // persistent mode: unit queue counter, per-unit ready flags, units, chains, chain stride
+  // persistent mode: unit queue counter, per-unit ready flags, units, chains, chain stride;
+  // then the tail's dB/dC reduction: its item counter, per-(sequence, group, chunk) counts of
+  // finished units, the item count and 32-token slices per chunk
   int* counter;
   int* flags;
   int units, chains, gx;
+  int* red_counter;
+  int* done;
+  int red_items, red_slices;
   uint32_t flag_spin;  // polls of a unit flag before the wait gives up
 };
 
@@ -61,6 +66,18 @@ __device__ __forceinline__ bool wait_unit_flag(const int* flag, const int* statu
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
     if (v) return true;
+    if (status && *reinterpret_cast<const volatile int*>(status)) return false;
+    __nanosleep(64);
+  }
+  return false;
+}
+// Waits (bounded, as wait_unit_flag) until *count reaches `target`.
+__device__ __forceinline__ bool wait_count(const int* count, int target, const int* status,
+                                           uint32_t spin) {
+  for (uint32_t i = 0; i < spin; i++) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    if (v >= target) return true;
     if (status && *reinterpret_cast<const volatile int*>(status)) return false;
     __nanosleep(64);
   }
@@ -79,6 +96,10 @@ int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc) {
   return 0;
 }
 int bwd_tma_channels_per_block() { return kCB; }
+int bwd_tma_queue_ints(const ScanProblem& p, int nch, long chains) {
+  // unit counter, unit flags, the tail's item counter, per-(sequence, group, chunk) counts
+  return (int)(1 + chains * nch + 1 + (long)p.ns * p.G * nch);
+}
 
 template <typename IO>
 __device__ __forceinline__ float lds_f(const IO* p) {
@@ -582,7 +603,9 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
 #pragma unroll
       for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
       const long tok = (long)b * p.L + t0 + i;
-      st_global_hint(a.part_bc + ((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r, v, pol_first);
+      float* dst = a.part_bc + ((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r;
+      if constexpr (PERSIST) *dst = v;  // read back from L2 by the tail's reduction
+      else st_global_hint(dst, v, pol_first);
     };
     if (cnt == TT) {  // full tile: a compile-time item count, so the items interleave
 #pragma unroll
@@ -637,7 +660,51 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     __syncthreads();
     if (tid == 0) publish_unit_flag(m.flags + (long)(b * m.gx + ux) * a.nch_b + s - 1);
   }
+  if constexpr (PERSIST) {  // the unit's dB/dC partials are all stored: count it
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(m.done + ((long)b * p.G + l.g) * a.nch_b + s, 1);
+    }
+  }
   }  // units
+  if constexpr (PERSIST) {
+    // ---- the tail: dB, dC of (sequence, group, chunk, 32-token slice) items, each once its
+    // chunk's a.bpg channel-block units are counted; items run in the chunks' finishing order.
+    // The sum over blocks has reduce_bc_kernel's fixed order, so results are the same bits.
+    __shared__ int sItem;
+    for (;;) {
+      if (tid == 0) {
+        const bool failed = p.status && *reinterpret_cast<const volatile int*>(p.status) != 0;
+        sItem = failed ? m.red_items : atomicAdd(m.red_counter, 1);
+      }
+      __syncthreads();
+      const int it = sItem;
+      __syncthreads();
+      if (it >= m.red_items) break;
+      const int slice = it % m.red_slices;
+      const int bgc = it / m.red_slices;  // (chunk-major, last chunk first) x (sequence, group)
+      const int ngroups = p.ns * p.G;
+      const int cc = a.nch_b - 1 - bgc / ngroups, bg = bgc % ngroups;
+      const int rb = bg / p.G, rg = bg - rb * p.G;
+      bool ok = true;
+      if (tid == 0) {
+        ok = wait_count(m.done + (long)bg * a.nch_b + cc, a.bpg, p.status, m.flag_spin);
+        if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
+      }
+      if (__syncthreads_or(!ok)) continue;
+      const int t0 = cc * a.chunk_b + slice * 32;
+      const int tn = min(32, min(p.L, (cc + 1) * a.chunk_b) - t0);
+      for (int o = tid; o < tn * 2 * N; o += kScanThreads) {
+        const int i = o / (2 * N), r = o - i * 2 * N;
+        const long tg = ((long)rb * p.L + t0 + i) * p.G + rg;
+        const float* src = a.part_bc + tg * a.bpg * 2 * N + r;
+        float v = 0.0f;
+        for (int k = 0; k < a.bpg; k++) v += __ldcg(src + (long)k * 2 * N);
+        sts_f((IO*)(r < N ? a.g.d_B : a.g.d_C) + tg * N + (r < N ? r : r - N), v);
+      }
+    }
+  }
   }();
   tmem_fence_before_sync();
   __syncthreads();
@@ -844,10 +911,14 @@ static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, 
   m.gx = p.G * a.bpg;
   m.chains = m.gx * p.ns;
   m.units = m.chains * a.nch_b;
+  m.red_counter = m.flags + m.units;
+  m.done = m.red_counter + 1;
+  m.red_slices = (a.chunk_b + 31) / 32;
+  m.red_items = p.ns * p.G * a.nch_b * m.red_slices;
+  const int nq = bwd_tma_queue_ints(p, a.nch_b, m.chains);
   const long slots = (long)per_sm * num_sms;
   const int grid = (int)(slots < m.units ? slots : m.units);
-  bwd_queue_reset_kernel<<<(1 + m.units + 255) / 256, 256, 0, st>>>(m.counter, 1 + m.units),
-      count_launches(1);
+  bwd_queue_reset_kernel<<<(nq + 255) / 256, 256, 0, st>>>(m.counter, nq), count_launches(1);
   k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
   return cudaGetLastError();
 }
