@@ -80,18 +80,18 @@ TARGET_WORKLOADS = ("mamba1_long_bf16_b1_l16384_d2048_n16", DEFAULT_WORKLOAD)
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 422653696 + 472961280,
+        "bytes": 460764416 + 361437952,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "002fc5a97d7695593c0b457849190d343e69fef2776ce838d83ee07a9862fda8",
+                "3cf909cbe1c56a4e5bfa3bd1987296ec0ec513ac799fcd7a962aa3fc9339b6a0",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
-                "42d6cfde6338fb1d9fa0db2c74aae2f3108949b3c94f1e463dc38801cd9c8584",
+                "1ba6a1c2e1acc8aa74133a18acf8163297c25c51b3485aade9655a20773ec648",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
                 "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
             "bwd_ssm_conv_gb300/csrc/tmem.cuh":
-                "7460dfcf5836cbb974ca8c84ec19c0858a2376bf6f308206f2db15ba286874db",
+                "a55a9f2b432aed93c2a879bdb73a942f1e4300594365b99509ffbe376fc332f5",
             "bwd_ssm_conv_gb300/csrc/tma.cuh":
-                "b34d036a83829241c4d9054142a9f1af16468fc28db91019d9abeea76186950b",
+                "0f9b45ac1fa9626f7e6e586d6d333bc14d1682fe84c565886c7e5e328abc1f5a",
         },
     },
 }

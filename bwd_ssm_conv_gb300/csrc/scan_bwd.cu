@@ -482,7 +482,7 @@ static BwdPlan plan_bwd(const ScanProblem& p, int num_sms) {
   q.off_dtb = take(segch);
   q.off_ddt = take(p.P > 1 ? F * (size_t)p.ns * p.L * p.HP : 0);
   q.off_dh0 = take(F * (size_t)p.ns * p.HP * p.N);
-  if (q.tma_tt && q.persist)  // queue counter, unit flags, the tail's counters
+  if (q.tma_tt && q.persist)  // queue counter, unit flags, finished-unit counts
     q.off_queue = take(sizeof(int) * (size_t)bwd_tma_queue_ints(p, q.nch_b, chains));
   if (q.heads) q.off_mh = take(F * bwd_heads_scratch_floats(p, q.S, q.chunk_b));
   q.bytes = off;
@@ -543,7 +543,7 @@ static cudaError_t launch_bwd_t(BwdArgs a, const BwdPlan& q, char* w, cudaStream
   } else if (e != cudaSuccess) {
     return e;
   }
-  if (!(persist && e == cudaSuccess))  // (the persistent TMA kernel sums dB, dC in its tail)
+  if (!(persist && e == cudaSuccess))  // (the persistent TMA kernel sums dB, dC in its queue)
     reduce_bc_kernel<IO><<<blocks_for((long)p.ns * p.L * p.G * 2 * p.N), 256, 0, st>>>(a), count_launches(1);
   const long nparams = (long)(p.a_per_state ? p.H * p.N : p.H) + p.HP + p.H;
   reduce_params_kernel<<<blocks_for(nparams), 256, 0, st>>>(a), count_launches(1);

@@ -111,7 +111,7 @@ int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc);
 int bwd_tma_channels_per_block();
 // Ints of the persistent path's queue area in the workspace (counters, flags, unit counts).
 int bwd_tma_queue_ints(const ScanProblem& p, int nch, long chains);
-// The persistent TMA path sums the dB/dC partials itself, in its tail.
+// The persistent TMA path sums the dB/dC partials itself, in reduction items of its queue.
 // Both return cudaErrorNotSupported, launching nothing, when the pointers do not allow the
 // path; the caller then runs the general kernels.
 cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, cudaStream_t st);

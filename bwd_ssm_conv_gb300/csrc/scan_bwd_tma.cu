@@ -45,19 +45,22 @@ struct BwdTma {
   uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
   uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
-  // persistent mode: unit queue counter, per-unit ready flags, units, chains, chain stride;
-  // then the tail's dB/dC reduction: its item counter, per-(sequence, group, chunk) counts of
-  // finished units, the item count and 32-token slices per chunk
+  // persistent mode: queue counter, per-unit ready flags, units, chains, chain stride; the
+  // dB/dC reduction items that share the queue: per-(sequence, group, chunk) counts of finished
+  // units, items per chunk, 32-token slices per chunk, and the queue's length (units + items)
   int* counter;
   int* flags;
   int units, chains, gx;
-  int* red_counter;
   int* done;
-  int red_items, red_slices;
+  int red_per_chunk, red_slices, queue_len;
   uint32_t flag_spin;  // polls of a unit flag before the wait gives up
 };
 
 constexpr uint32_t kFlagSpin = 1u << 22;
+// Chunks (the last to finish) whose dB/dC reduction items wait for the end of the persistent
+// queue.  On 16 x 2048 tokens x 1536 channels in chunks of 256: 1 -> 780 MB of DRAM traffic per
+// call and 1.231 ms, 3 -> 822 MB and 1.227 ms, all 8 -> 1094 MB and 1.224 ms.
+constexpr int kRedTail = 3;
 
 // Waits (bounded) until another block has published *flag; gives up at once when any block has
 // recorded an error in the status word, so that one failure cannot chain into long waits.
@@ -97,8 +100,8 @@ int bwd_tma_tile(const ScanProblem& p, int chunk_b, int gc) {
 }
 int bwd_tma_channels_per_block() { return kCB; }
 int bwd_tma_queue_ints(const ScanProblem& p, int nch, long chains) {
-  // unit counter, unit flags, the tail's item counter, per-(sequence, group, chunk) counts
-  return (int)(1 + chains * nch + 1 + (long)p.ns * p.G * nch);
+  // queue counter, unit flags, per-(sequence, group, chunk) counts of finished units
+  return (int)(1 + chains * nch + (long)p.ns * p.G * nch);
 }
 
 template <typename IO>
@@ -194,11 +197,101 @@ __device__ __forceinline__ f2_t reduce_bc_warp(f2_t dB01, f2_t dB23, f2_t dC01, 
   return f2_add(x, f2_pack(__shfl_xor_sync(0xffffffffu, xb, 4), __shfl_xor_sync(0xffffffffu, xc, 4)));
 }
 
-// PERSIST: the grid is a set of resident blocks that take (chain, chunk) units from a queue in
-// the order chunk-major, last chunk first (unit u: chain u % chains, chunk nch - 1 - u / chains),
-// so the unit that produces a chunk's end adjoint (the start adjoint of the chunk after it) was
-// taken from the queue `chains` units earlier by a running block.  Otherwise one block = one
-// (sequence, channel block, segment) of whole chunks, as given by the grid.
+// One dB/dC reduction item of the persistent path: for (sequence, group) bg = j / slices and the
+// 32-token slice j % slices of chunk cc, the sums over the a.bpg channel blocks' partials, taken
+// in block order 0..bpg-1 (the separate reduction kernel's order, so the results are the same
+// bits), once that chunk's units of bg are all counted.  A wait that gives up records a time-out
+// and returns.  Entered and left by the whole block.
+template <typename IO>
+__device__ __forceinline__ void reduce_item(const BwdTma& m, const BwdArgs& a, int cc, int j) {
+  constexpr int N = 16, R2 = 2 * N;
+  const ScanProblem& p = a.p;
+  const int tid = threadIdx.x;
+  const int bg = j / m.red_slices, slice = j - bg * m.red_slices;
+  const int rb = bg / p.G, rg = bg - rb * p.G;
+  bool ok = true;
+  if (tid == 0) {
+    ok = wait_count(m.done + (long)bg * a.nch_b + cc, a.bpg, p.status, m.flag_spin);
+    if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
+  }
+  if (__syncthreads_or(!ok)) return;
+  const int t0 = cc * a.chunk_b + slice * 32;
+  const int tn = min(32, min(p.L, (cc + 1) * a.chunk_b) - t0);
+  // 8 threads share a token's partial line (one per block index k: 2N floats, 128 bytes), each
+  // holding 4 entries (one 16-byte load per line); thread tid sums the quad q of tokens
+  // i0 + kRowsQ u.  kK block indices x kOutQ tokens of loads are in flight together, and each sum
+  // still adds its partials in the order k = 0, 1, ... (paired adds round as scalar ones).
+  constexpr int kQ = R2 / 4, kRowsQ = kScanThreads / kQ, kOutQ = 32 / kRowsQ, kK = 4;
+  static_assert(kScanThreads % kQ == 0 && 32 % kRowsQ == 0 && 32 % kQ == 0, "item layout");
+  const int q = tid % kQ, i0 = tid / kQ;
+  const long tg0 = ((long)rb * p.L + t0 + i0) * p.G + rg;
+  const long tstep = (long)kRowsQ * p.G;                 // token rows between passes
+  const float* line0 = a.part_bc + tg0 * a.bpg * R2;     // token i0's line of block 0
+  const long sstep = tstep * a.bpg * R2;
+  f2_t v[kOutQ][2];
+#pragma unroll
+  for (int u = 0; u < kOutQ; u++) v[u][0] = v[u][1] = 0ull;
+  auto acc = [&](int u, float4 t) {
+    v[u][0] = f2_add(v[u][0], f2_pack(t.x, t.y));
+    v[u][1] = f2_add(v[u][1], f2_pack(t.z, t.w));
+  };
+  auto ld4 = [&](int u, int k) {
+    return __ldcg(reinterpret_cast<const float4*>(line0 + u * sstep + (long)k * R2) + q);
+  };
+  int k = 0;
+  for (; k + kK <= a.bpg; k += kK) {
+    float4 t[kK][kOutQ];
+#pragma unroll
+    for (int d = 0; d < kK; d++)
+#pragma unroll
+      for (int u = 0; u < kOutQ; u++)
+        t[d][u] = i0 + u * kRowsQ < tn ? ld4(u, k + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int d = 0; d < kK; d++)
+#pragma unroll
+      for (int u = 0; u < kOutQ; u++) acc(u, t[d][u]);
+  }
+  for (; k < a.bpg; k++) {
+#pragma unroll
+    for (int u = 0; u < kOutQ; u++)
+      if (i0 + u * kRowsQ < tn) acc(u, ld4(u, k));
+  }
+  const int r = 4 * q;  // entries r .. r+3: dB (r < N) or dC, never both
+  IO* dst = (IO*)(r < N ? a.g.d_B : a.g.d_C) + (r < N ? r : r - N);
+#pragma unroll
+  for (int u = 0; u < kOutQ; u++) {
+    if (i0 + u * kRowsQ >= tn) continue;
+    float e[4];
+    f2_unpack(v[u][0], e[0], e[1]);
+    f2_unpack(v[u][1], e[2], e[3]);
+    IO* o = dst + (tg0 + u * tstep) * N;
+#pragma unroll
+    for (int c = 0; c < 4; c++) sts_f(o + c, e[c]);
+  }
+  // the lines are read (their values are in the sums; a line's 8 readers share a warp): drop
+  // them from L2 unwritten
+  __syncwarp();
+  for (int kk = q; kk < a.bpg; kk += kQ) {
+#pragma unroll
+    for (int u = 0; u < kOutQ; u++)
+      if (i0 + u * kRowsQ < tn) discard_l2_line(line0 + u * sstep + (long)kk * R2);
+  }
+  __syncthreads();
+}
+
+// PERSIST: the grid is a set of resident blocks that take work from one queue.  The queue holds
+// the (chain, chunk) units chunk-major, last chunk first (unit u: chain u % chains, chunk
+// nch - 1 - u / chains), so the unit that produces a chunk's end adjoint (the start adjoint of
+// the chunk after it) was taken `chains` positions earlier by a running block.  The dB/dC
+// reduction items of chunk c follow the units of chunk c - 1, whose units were all taken before
+// them, except for the last kRedTail chunks to finish (c < kRedTail), whose items close the
+// queue (nch = 8, kRedTail = 3):
+//   [units 7] [units 6][items 7] [units 5][items 6] ... [units 2][items 3] [units 1] [units 0]
+//   [items 2] [items 1] [items 0]
+// Every wait is on work taken earlier.  A chunk's partials are summed about one chunk of units
+// after they are stored, while they are still in L2; the items at the end run in the slots
+// that the last units leave idle, on partials recent enough to be in L2 too.  Otherwise one
+// block = one (sequence, channel block, segment) of whole chunks, as given by the grid.
 template <typename IO, bool PERSIST>
 __global__ void __launch_bounds__(kScanThreads, kBwdTmaBlocksPerSM)
 scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
@@ -233,11 +326,36 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   if constexpr (PERSIST) {
     if (tid == 0) {
       const bool failed = p.status && *reinterpret_cast<const volatile int*>(p.status) != 0;
-      sUnit = failed ? m.units : atomicAdd(m.counter, 1);
+      sUnit = failed ? m.queue_len : atomicAdd(m.counter, 1);
     }
     __syncthreads();
-    const int u = sUnit;
-    if (u >= m.units) break;
+    const int q = sUnit;
+    if (q >= m.queue_len) break;
+    // position -> unit u, or reduction item j of chunk cc
+    int u = q, cc = -1, j = 0;
+    if (q >= m.chains) {
+      const int C = m.chains, R = m.red_per_chunk, per = C + R;
+      const int k1 = max(0, a.nch_b - kRedTail);  // unit blocks 1..k1 carry items
+      const int q2 = q - C;
+      if (q2 < k1 * per) {
+        const int k = 1 + q2 / per, r = q2 - (k - 1) * per;
+        if (r < C) u = k * C + r;
+        else { cc = a.nch_b - k; j = r - C; }
+      } else {
+        const int q3 = q2 - k1 * per, nb = a.nch_b - 1 - k1;
+        if (q3 < nb * C) {
+          u = (1 + k1) * C + q3;
+        } else {
+          const int q4 = q3 - nb * C, t = min(kRedTail, a.nch_b);
+          cc = t - 1 - q4 / R;
+          j = q4 - (t - 1 - cc) * R;
+        }
+      }
+    }
+    if (cc >= 0) {
+      reduce_item<IO>(m, a, cc, j);
+      continue;
+    }
     const int chain = u % m.chains;
     s = a.nch_b - 1 - u / m.chains;
     ux = chain % m.gx;
@@ -604,7 +722,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       for (int w = 0; w < kWarps; w++) v += red[(i * kWarps + w) * 2 * N + r];
       const long tok = (long)b * p.L + t0 + i;
       float* dst = a.part_bc + ((tok * p.G + l.g) * a.bpg + l.blk) * 2 * N + r;
-      if constexpr (PERSIST) *dst = v;  // read back from L2 by the tail's reduction
+      if constexpr (PERSIST) *dst = v;  // summed from L2 by a reduction item a chunk later
       else st_global_hint(dst, v, pol_first);
     };
     if (cnt == TT) {  // full tile: a compile-time item count, so the items interleave
@@ -668,43 +786,6 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
     }
   }
   }  // units
-  if constexpr (PERSIST) {
-    // ---- the tail: dB, dC of (sequence, group, chunk, 32-token slice) items, each once its
-    // chunk's a.bpg channel-block units are counted; items run in the chunks' finishing order.
-    // The sum over blocks has reduce_bc_kernel's fixed order, so results are the same bits.
-    __shared__ int sItem;
-    for (;;) {
-      if (tid == 0) {
-        const bool failed = p.status && *reinterpret_cast<const volatile int*>(p.status) != 0;
-        sItem = failed ? m.red_items : atomicAdd(m.red_counter, 1);
-      }
-      __syncthreads();
-      const int it = sItem;
-      __syncthreads();
-      if (it >= m.red_items) break;
-      const int slice = it % m.red_slices;
-      const int bgc = it / m.red_slices;  // (chunk-major, last chunk first) x (sequence, group)
-      const int ngroups = p.ns * p.G;
-      const int cc = a.nch_b - 1 - bgc / ngroups, bg = bgc % ngroups;
-      const int rb = bg / p.G, rg = bg - rb * p.G;
-      bool ok = true;
-      if (tid == 0) {
-        ok = wait_count(m.done + (long)bg * a.nch_b + cc, a.bpg, p.status, m.flag_spin);
-        if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
-      }
-      if (__syncthreads_or(!ok)) continue;
-      const int t0 = cc * a.chunk_b + slice * 32;
-      const int tn = min(32, min(p.L, (cc + 1) * a.chunk_b) - t0);
-      for (int o = tid; o < tn * 2 * N; o += kScanThreads) {
-        const int i = o / (2 * N), r = o - i * 2 * N;
-        const long tg = ((long)rb * p.L + t0 + i) * p.G + rg;
-        const float* src = a.part_bc + tg * a.bpg * 2 * N + r;
-        float v = 0.0f;
-        for (int k = 0; k < a.bpg; k++) v += __ldcg(src + (long)k * 2 * N);
-        sts_f((IO*)(r < N ? a.g.d_B : a.g.d_C) + tg * N + (r < N ? r : r - N), v);
-      }
-    }
-  }
   }();
   tmem_fence_before_sync();
   __syncthreads();
@@ -911,10 +992,10 @@ static cudaError_t launch_main_t(BwdTma& m, const BwdArgs& a, const BwdPlan& q, 
   m.gx = p.G * a.bpg;
   m.chains = m.gx * p.ns;
   m.units = m.chains * a.nch_b;
-  m.red_counter = m.flags + m.units;
-  m.done = m.red_counter + 1;
+  m.done = m.flags + m.units;
   m.red_slices = (a.chunk_b + 31) / 32;
-  m.red_items = p.ns * p.G * a.nch_b * m.red_slices;
+  m.red_per_chunk = p.ns * p.G * m.red_slices;
+  m.queue_len = m.units + a.nch_b * m.red_per_chunk;
   const int nq = bwd_tma_queue_ints(p, a.nch_b, m.chains);
   const long slots = (long)per_sm * num_sms;
   const int grid = (int)(slots < m.units ? slots : m.units);

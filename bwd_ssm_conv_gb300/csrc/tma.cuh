@@ -115,6 +115,13 @@ __device__ __forceinline__ void st_global_hint(float* p, float v, uint64_t pol) 
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
 
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back: for scratch that is
+// never read again, so that a dirty line costs no DRAM write.  The line's contents are undefined
+// until it is written again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
