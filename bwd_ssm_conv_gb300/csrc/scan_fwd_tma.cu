@@ -106,21 +106,27 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   }
   const uint64_t C = p.HP, L = p.L, NSq = p.ns, GN = (uint64_t)p.G * p.N;
   const int ck = p.sx ? p.d_conv : 0;  // the fused conv computes x: no tensor map for it
-  bool ok = (ck > 0 || encode_tmap_3d(&a.mx, p.x, io, C, L, NSq, C, C * L, q.cb, q.tt, 1)) &&
+  // the x, z and y tiles are swizzled whenever a tile row (cb channels) is 32, 64 or 128 bytes,
+  // the rule the kernel's fwd_tile_swizzle applies to the same cb
+  const int rowb = q.cb * io, swz = (rowb == 32 || rowb == 64 || rowb == 128) ? rowb : 0;
+  bool ok = (ck > 0 || encode_tmap_3d(&a.mx, p.x, io, C, L, NSq, C, C * L, q.cb, q.tt, 1, swz)) &&
             encode_tmap_3d(&a.mdt, p.dt, io, C, L, NSq, C, C * L, q.cb, q.tt, 1) &&
             encode_tmap_3d(&a.mb, p.B, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1) &&
             encode_tmap_3d(&a.mc, p.C, io, GN, L, NSq, GN, GN * L, p.N, q.tt, 1);
-  if (ok && p.z) ok = encode_tmap_3d(&a.mz, p.z, io, C, L, NSq, C, C * L, q.cb, q.tt, 1);
-  if (ok && y) ok = encode_tmap_3d(&a.my, y, io, C, L, NSq, C, C * L, q.cb, q.tt, 1);
+  if (ok && p.z) ok = encode_tmap_3d(&a.mz, p.z, io, C, L, NSq, C, C * L, q.cb, q.tt, 1, swz);
+  if (ok && y) ok = encode_tmap_3d(&a.my, y, io, C, L, NSq, C, C * L, q.cb, q.tt, 1, swz);
   if (!ok) return cudaErrorNotSupported;
   const uint32_t tile = (uint32_t)(q.tt * q.cb * io), row = (uint32_t)(q.tt * p.N * io);
+  // every buffer 128-byte aligned; the swizzled x, z, y tiles (and so the stages) 1024-byte
+  // aligned, from a base the kernel aligns to 1024 bytes
   auto al = [](uint32_t v) { return (v + 127u) & ~127u; };
+  auto alk = [](uint32_t v) { return (v + 1023u) & ~1023u; };
   a.off_x = 0;
   a.off_dt = al(tile);
-  a.off_z = a.off_dt + al(tile);
+  a.off_z = alk(a.off_dt + al(tile));
   a.off_b = a.off_z + (p.z ? al(tile) : 0);
   a.off_c = a.off_b + al(row);
-  a.stage_stride = a.off_c + al(row);
+  a.stage_stride = alk(a.off_c + al(row));
   a.off_dd = kFwdStages * a.stage_stride;                       // float2 (delta, delta x)
   // B and C of a tile as fp32 rows (bf16 I/O only; fp32 I/O reads the staged rows)
   const uint32_t frow = io == 2 ? al((uint32_t)(q.tt * p.N * 4)) : 0u;
@@ -128,12 +134,12 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   a.off_cf = a.off_bf + frow;
   a.off_par = a.off_cf + frow;
   // D, dt_bias; with the fused conv also the conv bias and weights
-  a.off_y = a.off_par + al((uint32_t)((2 + (ck ? 1 + ck : 0)) * q.cb * 4));
-  a.y_stride = al(tile);
+  a.off_y = alk(a.off_par + al((uint32_t)((2 + (ck ? 1 + ck : 0)) * q.cb * 4)));
+  a.y_stride = alk(tile);
   a.off_sxs = a.off_y + 2 * a.y_stride;
   const uint32_t pitch = (uint32_t)((q.tt + ck - 1) | 1);
   a.off_bar = a.off_sxs + (ck > 0 ? al((uint32_t)(q.cb * pitch * 4)) : 0u);
-  const size_t smem = a.off_bar + 64;
+  const size_t smem = a.off_bar + 64 + 1024;  // + the kernel's alignment of its base
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
   // the fused conv's x slot in a stage is written by the prepass, not copied
   a.bytes_local = (ck > 0 ? 1 : 2) * tile + row;

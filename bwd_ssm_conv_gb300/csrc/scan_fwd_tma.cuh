@@ -63,6 +63,16 @@ __host__ __device__ constexpr int conv_cols() { return 16 + CK - 1; }
 template <int CK>
 __host__ __device__ constexpr int conv_pitch() { return conv_cols<CK>() | 1; }
 
+// The TMA swizzle of the x, z and y tiles ([TT][cb], one tile row per token): the span of a
+// tile row when that is 32, 64 or 128 bytes (as a log2 of 16-byte chunks), else none.  The
+// epilogue's warp reads 4 token rows of 8 channels; unswizzled, rows 128 bytes apart share
+// banks (2-way for bf16 rows of 32 channels, 4-way for fp32).
+template <typename IO, int CB>
+__host__ __device__ constexpr int fwd_tile_swizzle() {
+  return CB * (int)sizeof(IO) == 32 ? 1 : CB * (int)sizeof(IO) == 64 ? 2
+                                        : CB * (int)sizeof(IO) == 128 ? 3 : 0;
+}
+
 template <typename IO>
 __device__ __forceinline__ float lds1(const IO* p) {
   if constexpr (sizeof(IO) == 4) return *reinterpret_cast<const float*>(p);
@@ -116,7 +126,11 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr int cb = THR / TPC;  // compile-time: index math is shifts
   static_assert(NS % 4 == 0, "states per thread come in groups of 4");
   static_assert(TT % TPC == 0, "token groups tile the staged tile");
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // the swizzled tiles want 1024-byte alignment: the host adds 1024 bytes for this shift
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr int SWZ = fwd_tile_swizzle<IO, cb>();
+  auto xi = [](int idx) { return swizzled_index<SWZ, (int)sizeof(IO)>(idx); };  // x, z, y tiles
   const ScanProblem& p = a.p;
   const int tid = threadIdx.x;
   const int cl = tid / TPC, sg = tid - cl * TPC;
@@ -245,7 +259,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         const int c = idx % cb;
         float dl = lds1(sdt + idx);
         if (p.softplus) dl = softplusf_(dl + sPar[cb + c]);
-        sDD[idx] = make_float2(dl, dl * lds1(sx + idx));
+        sDD[idx] = make_float2(dl, dl * lds1(sx + xi(idx)));
       }
     } else {
       // the conv: warp w takes tokens 4w .. 4w+3 of channel `lane`, a sliding window over
@@ -268,7 +282,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
         for (int kk = 0; kk < CK; kk++) acc = fmaf(win[u + kk], wk[kk], acc);
         if (p.conv_silu) acc = siluf_(acc);
         const IO xr = static_cast<IO>(acc);
-        const_cast<IO*>(sx)[idx] = xr;
+        const_cast<IO*>(sx)[xi(idx)] = xr;
         sDD[idx] = make_float2(dl, dl * static_cast<float>(xr));
       }
     }
@@ -387,7 +401,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       if (LOCAL) return;
       const float tot = group_reduce_scatter<TPC>(acc, sg);
       if (want_y) {  // token i0 + sg of channel cl (rows past the sequence end are not stored)
-        const int idx = (i0 + sg) * cb + cl;
+        const int idx = xi((i0 + sg) * cb + cl);
         float yv = fmaf(Dc, lds1(sx + idx), tot);
         if (p.z) yv *= siluf_(lds1(sz + idx));
         if (p.check_finite && (FULL || i0 + sg < cnt) && !isfinite(yv))

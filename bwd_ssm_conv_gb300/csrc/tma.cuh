@@ -122,6 +122,19 @@ __device__ __forceinline__ void discard_l2_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
+// Element index -> its place in a shared-memory box that a tensor map with a swizzle span of
+// 16 << SWZ_B bytes (SWZ_B = 1, 2, 3: 32, 64, 128 bytes) fills or stores, for a buffer aligned
+// to 1024 bytes: the 16-byte chunk index takes the XOR of address bits 7 .. 7 + SWZ_B - 1.
+template <int SWZ_B, int ESIZE>
+__device__ __forceinline__ int swizzled_index(int idx) {
+  if constexpr (SWZ_B == 0) {
+    return idx;
+  } else {
+    const int off = idx * ESIZE;
+    return (off ^ (((off >> 7) & ((1 << SWZ_B) - 1)) << 4)) / ESIZE;
+  }
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -142,9 +155,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // ---- host --------------------------------------------------------------------------------
 // Encodes a 3-D tensor map over a row-major [d2][d1][d0] tensor (d0 fastest, element size
 // `esize`, row stride `stride1` elements, plane stride `stride2` elements) with box
-// {b0, b1, b2}.  Returns false if the driver rejects it (alignment, box size).
+// {b0, b1, b2}.  `swizzle` = 32, 64 or 128 lays the box out in shared memory with that
+// swizzle span (the 16-byte chunk index XOR address bits 7.. : see swizzled_index), 0 plainly.
+// Returns false if the driver rejects it (alignment, box size).
 bool encode_tmap_3d(CUtensorMap* map, const void* base, int esize, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1,
-                    uint32_t b2);
+                    uint32_t b2, int swizzle = 0);
 
 }  // namespace ssm
