@@ -41,14 +41,20 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   // largest states-per-thread that still gives four blocks per SM without time segments
   // (the recurrence is latency-bound: more warps per SM beat fewer instructions per state;
   // two states per thread, eight threads per channel, measured slower on both of d_inner 1536
-  // x 16 sequences and d_inner 2048 x 1 sequence)
+  // x 16 sequences and d_inner 2048 x 1 sequence).  When none does, time segments make up the
+  // blocks, and for bf16 I/O 8 states per thread (fewer shuffles per token, twice the
+  // segments) beat 4: d_inner 2048 x one 16384-token sequence 0.321 -> 0.310 ms.  Not for
+  // fp32, whose batched accurate decays then cost more (d_inner 512 x 8 x 1024: 0.093 ->
+  // 0.103 ms); with 16 states per thread both lose (0.376 ms on the former).
   int ns = 0;
+  bool fills = false;
   for (int cand = 16; cand >= 4; cand >>= 1) {
     if (p.N % cand != 0 || !instantiated(cand, p.N / cand, sa, ck)) continue;
     ns = cand;
     const int cb = kScanThreads / (p.N / cand);
-    if ((long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) break;
+    if ((long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) { fills = true; break; }
   }
+  if (!fills && io == 2 && ns < 8 && p.N % 8 == 0 && instantiated(8, p.N / 8, sa, ck)) ns = 8;
   if (ns == 0) return q;
   q.ns_state = ns;
   q.tpc = p.N / ns;
