@@ -105,12 +105,16 @@ def test_scan_backward_parity(case):
 # chunk) units, last chunk first, each handing its chunk's start adjoint to the unit of the
 # chunk before it.  Ragged last chunk.  22 x 32 = 704 chains fill 3/4 of the 608 resident
 # blocks but not all: also persistent, with some blocks waiting on the flag of a chunk still in
-# progress.
+# progress.  The dB/dC reduction items share the unit queue: chunk counts 2 and 3 put all of
+# them at its end, 4, 5 and 10 interleave them with the units of earlier chunks (10: a ragged
+# last chunk and two 32-token items per chunk).
 PERSIST_CASES = [
     ("persist_bf16", (40, 100, 1024, 1, 16, 1), "bf16", 32, False),
     ("persist_f32_softplus", (24, 72, 1024, 1, 16, 1), "f32", 16, True),
     ("persist_partial_bf16", (22, 100, 1024, 1, 16, 1), "bf16", 32, False),
     ("persist_pieces_bf16", (24, 300, 1024, 1, 16, 1), "bf16", 144, False),
+    ("persist_two_chunks_bf16", (40, 64, 1024, 1, 16, 1), "bf16", 32, False),
+    ("persist_ten_chunks_bf16", (24, 600, 1024, 1, 16, 1), "bf16", 64, False),
 ]
 
 
