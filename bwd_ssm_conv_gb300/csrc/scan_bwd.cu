@@ -310,53 +310,51 @@ __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
 }
 
 // ---- fixed-order reductions --------------------------------------------------------------
-// sum_{j < count} base[j * stride], added in the order of j; the loads go out eight at a time
-// so that a long sum is not one load latency per term.
-__device__ __forceinline__ float sum_strided(const float* base, long stride, int count) {
-  float v = 0.0f;
-  int j = 0;
-  for (; j + 8 <= count; j += 8) {
-    float t[8];
-#pragma unroll
-    for (int u = 0; u < 8; u++) t[u] = base[(long)(j + u) * stride];
-#pragma unroll
-    for (int u = 0; u < 8; u++) v += t[u];
-  }
-  for (; j < count; j++) v += base[(long)j * stride];
-  return v;
-}
-
-__global__ void reduce_params_kernel(const BwdArgs a) {
+// dA, dD and d dt_bias: the sums of the per-(sequence, segment) partials.  A block = kParOut
+// outputs x kParSlices slices of each output's terms; slice sl adds terms sl, sl + kParSlices,
+// ... in order and the slices combine in shared memory in a fixed order, so the result is the
+// same bits on every run.  (One thread per output left most SMs idle and each thread on a long
+// chain of strided loads.)
+constexpr int kParOut = 32, kParSlices = 8;
+__global__ void __launch_bounds__(kParOut * kParSlices) reduce_params_kernel(const BwdArgs a) {
+  __shared__ float sred[kParSlices][kParOut];
   const ScanProblem& p = a.p;
   const int nA = p.a_per_state ? p.H * p.N : p.H;
   const long total = (long)nA + p.HP + p.H;
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
-       i += (long)gridDim.x * blockDim.x) {
-    if (i < nA) {  // dA: over sequences, segments, head_dim (and states in the scalar form)
-      const int h = p.a_per_state ? (int)(i / p.N) : (int)i;
-      const int n_lo = p.a_per_state ? (int)(i % p.N) : 0;
-      const int n_hi = p.a_per_state ? n_lo + 1 : p.N;
-      float v = 0.0f;
-      if (p.P == 1 && n_hi == n_lo + 1) {  // one term per (sequence, segment), in that order
-        v = sum_strided(a.dA_part + (long)h * p.N + n_lo, (long)p.HP * p.N, p.ns * a.S);
-      } else {
-        for (int b = 0; b < p.ns; b++)
-          for (int s = 0; s < a.S; s++)
-            for (int pp = 0; pp < p.P; pp++)
-              for (int n = n_lo; n < n_hi; n++)
-                v += a.dA_part[(((long)b * a.S + s) * p.HP + h * p.P + pp) * p.N + n];
-      }
-      a.g.d_A[i] = v;
-    } else if (i < nA + p.HP) {  // dD
-      const int ch = (int)(i - nA);
-      if (!a.g.d_D) continue;
-      a.g.d_D[ch] = sum_strided(a.dD_part + ch, p.HP, p.ns * a.S);
-    } else {  // d dt_bias (head_dim == 1; the head_dim > 1 case is reduce_ddt_kernel's)
-      const int h = (int)(i - nA - p.HP);
-      if (!a.g.d_dt_bias || p.P != 1) continue;
-      a.g.d_dt_bias[h] = sum_strided(a.dtb_part + h, p.HP, p.ns * a.S);
+  const int lo = threadIdx.x % kParOut, sl = threadIdx.x / kParOut;
+  const long i = (long)blockIdx.x * kParOut + lo;
+  const int bs = p.ns * a.S;  // (sequence, segment) partials
+  float v = 0.0f;
+  bool want = i < total;
+  if (want && i < nA) {  // dA: over sequences, segments, head_dim (and states in the scalar form)
+    const int h = p.a_per_state ? (int)(i / p.N) : (int)i;
+    const int n_lo = p.a_per_state ? (int)(i % p.N) : 0;
+    const int nn = p.a_per_state ? 1 : p.N;
+    const int terms = bs * p.P * nn;  // term (b s, pp, n), n fastest
+    for (int j = sl; j < terms; j += kParSlices) {
+      const int n = n_lo + j % nn, pp = (j / nn) % p.P, q = j / (nn * p.P);
+      v += a.dA_part[((long)q * p.HP + h * p.P + pp) * p.N + n];
     }
+  } else if (want && i < nA + p.HP) {  // dD
+    const int ch = (int)(i - nA);
+    want = a.g.d_D != nullptr;
+    if (want)
+      for (int j = sl; j < bs; j += kParSlices) v += a.dD_part[(long)j * p.HP + ch];
+  } else if (want) {  // d dt_bias (head_dim == 1; the head_dim > 1 case is reduce_ddt_kernel's)
+    const int h = (int)(i - nA - p.HP);
+    want = a.g.d_dt_bias != nullptr && p.P == 1;
+    if (want)
+      for (int j = sl; j < bs; j += kParSlices) v += a.dtb_part[(long)j * p.HP + h];
   }
+  sred[sl][lo] = v;
+  __syncthreads();
+  if (sl != 0 || !want) return;
+  float t = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kParSlices; q++) t += sred[q][lo];
+  if (i < nA) a.g.d_A[i] = t;
+  else if (i < nA + p.HP) a.g.d_D[i - nA] = t;
+  else a.g.d_dt_bias[i - nA - p.HP] = t;
 }
 
 // head_dim > 1: d_dt[b][t][h] = softplus'(pre) * sum_p ddelta_p
@@ -521,7 +519,7 @@ static cudaError_t launch_bwd_t(BwdArgs a, const BwdPlan& q, char* w, cudaStream
   if (q.heads) {
     cudaError_t e = launch_bwd_heads(a, (float*)(w + q.off_mh), st);
     if (e != cudaSuccess) return e;
-    if (a.g.d_s0)
+    if (a.g.d_s0 && a.dh0 != a.g.d_s0)
       reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
     return cudaGetLastError();
   }
@@ -546,12 +544,13 @@ static cudaError_t launch_bwd_t(BwdArgs a, const BwdPlan& q, char* w, cudaStream
   if (!(persist && e == cudaSuccess))  // (the persistent TMA kernel sums dB, dC in its queue)
     reduce_bc_kernel<IO><<<blocks_for((long)p.ns * p.L * p.G * 2 * p.N), 256, 0, st>>>(a), count_launches(1);
   const long nparams = (long)(p.a_per_state ? p.H * p.N : p.H) + p.HP + p.H;
-  reduce_params_kernel<<<blocks_for(nparams), 256, 0, st>>>(a), count_launches(1);
+  reduce_params_kernel<<<(int)((nparams + kParOut - 1) / kParOut), kParOut * kParSlices, 0, st>>>(a),
+      count_launches(1);
   if (p.P > 1) {
     reduce_ddt_kernel<IO><<<blocks_for((long)p.ns * p.L * p.H), 256, 0, st>>>(a), count_launches(1);
     if (p.softplus && a.g.d_dt_bias) reduce_dtb_kernel<IO><<<blocks_for(p.H), 256, 0, st>>>(a), count_launches(1);
   }
-  if (a.g.d_s0)
+  if (a.g.d_s0 && a.dh0 != a.g.d_s0)
     reduce_ds0_kernel<<<blocks_for((long)p.state_rows * p.HP * p.N), 256, 0, st>>>(a), count_launches(1);
   return cudaGetLastError();
 }
@@ -596,7 +595,10 @@ cudaError_t launch_scan_bwd(const ScanProblem& p, const float* ckpt, const ScanG
   a.dD_part = (float*)(w + q.off_dD);
   a.dtb_part = (float*)(w + q.off_dtb);
   a.ddt_part = (float*)(w + q.off_ddt);
-  a.dh0 = (float*)(w + q.off_dh0);
+  // the start-state adjoints, one row per sequence; when sequence b's initial state is row b
+  // (no ids, one row per sequence) they are d_s0 itself and no sum runs.  Every path writes
+  // each element once, from the unit or segment that ends at the sequence start.
+  a.dh0 = (!p.ids && p.state_rows == p.ns && g.d_s0) ? g.d_s0 : (float*)(w + q.off_dh0);
   const bool full = rows_vectorizable(p, kBwdNS, q.tpc);
   return p.io == SSM_BF16 ? launch_bwd_io<__nv_bfloat16>(a, q, full, w, st)
                           : launch_bwd_io<float>(a, q, full, w, st);
