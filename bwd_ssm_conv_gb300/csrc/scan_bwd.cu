@@ -330,10 +330,22 @@ __global__ void __launch_bounds__(kParOut * kParSlices) reduce_params_kernel(con
     const int h = p.a_per_state ? (int)(i / p.N) : (int)i;
     const int n_lo = p.a_per_state ? (int)(i % p.N) : 0;
     const int nn = p.a_per_state ? 1 : p.N;
-    const int terms = bs * p.P * nn;  // term (b s, pp, n), n fastest
-    for (int j = sl; j < terms; j += kParSlices) {
-      const int n = n_lo + j % nn, pp = (j / nn) % p.P, q = j / (nn * p.P);
-      v += a.dA_part[((long)q * p.HP + h * p.P + pp) * p.N + n];
+    if (p.P == 1 && nn == 1) {  // one term per (sequence, segment): a plain strided sum
+      const float* src = a.dA_part + i;
+      const long stride = (long)kParSlices * p.HP * p.N;
+      int j = sl;
+      for (; j + 3 * kParSlices < bs; j += 4 * kParSlices) {  // 4 loads in flight, same order
+        const float* q0 = src + (long)j * p.HP * p.N;
+        const float t0 = q0[0], t1 = q0[stride], t2 = q0[2 * stride], t3 = q0[3 * stride];
+        v += t0; v += t1; v += t2; v += t3;
+      }
+      for (; j < bs; j += kParSlices) v += src[(long)j * p.HP * p.N];
+    } else {
+      const int terms = bs * p.P * nn;  // term (b s, pp, n), n fastest
+      for (int j = sl; j < terms; j += kParSlices) {
+        const int n = n_lo + j % nn, pp = (j / nn) % p.P, q = j / (nn * p.P);
+        v += a.dA_part[((long)q * p.HP + h * p.P + pp) * p.N + n];
+      }
     }
   } else if (want && i < nA + p.HP) {  // dD
     const int ch = (int)(i - nA);
