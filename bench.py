@@ -80,7 +80,7 @@ TARGET_WORKLOADS = ("mamba1_long_bf16_b1_l16384_d2048_n16", DEFAULT_WORKLOAD)
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 460764416 + 361437952,
+        "bytes": 461096448 + 360978176,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
                 "3cf909cbe1c56a4e5bfa3bd1987296ec0ec513ac799fcd7a962aa3fc9339b6a0",
@@ -91,7 +91,7 @@ TRAFFIC_CAPTURES = {
             "bwd_ssm_conv_gb300/csrc/tmem.cuh":
                 "a55a9f2b432aed93c2a879bdb73a942f1e4300594365b99509ffbe376fc332f5",
             "bwd_ssm_conv_gb300/csrc/tma.cuh":
-                "0f9b45ac1fa9626f7e6e586d6d333bc14d1682fe84c565886c7e5e328abc1f5a",
+                "7faa420ff2e14fc905e7e16a643798cbd631d272b9772c9e1d3e1d9fbd4b4f6c",
         },
     },
 }
