@@ -290,6 +290,7 @@ scan_bwd_local_kernel(const BwdArgs a) {
 
 // Adjoint at every segment end, composing segments from the last: end[s-1] =
 // exp(A sum_delta[s]) end[s] + local[s]; the last segment ends at d_state_out.
+constexpr int kCarryBatch = 8;
 __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
   const ScanProblem& p = a.p;
   const long total = (long)p.ns * p.HP * p.N;
@@ -301,10 +302,24 @@ __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
     const int h = ch / p.P;
     const float A2 = (p.a_per_state ? __ldg(p.A + (long)h * p.N + n) : __ldg(p.A + h)) * kLog2e;
     float c = a.g.d_state_out ? __ldg(a.g.d_state_out + i) : 0.0f;
-    for (int s = a.S - 1; s >= 0; s--) {
-      const long si = ((long)b * a.S + s) * p.HP + ch;
-      a.segend[si * p.N + n] = c;
-      if (s > 0) c = fmaf(ex2(A2 * a.sumd[si]), c, a.dhloc[si * p.N + n]);
+    // segments S-1 .. 0, kCarryBatch at a time: their decays and local adjoints do not depend
+    // on c, so their loads go out together ahead of the composition
+    for (int s0 = a.S - 1; s0 >= 0; s0 -= kCarryBatch) {
+      float dk[kCarryBatch], lv[kCarryBatch];
+#pragma unroll
+      for (int j = 0; j < kCarryBatch; j++) {
+        const int s = s0 - j;
+        const long si = ((long)b * a.S + s) * p.HP + ch;
+        dk[j] = s > 0 ? ex2(A2 * a.sumd[si]) : 0.0f;
+        lv[j] = s > 0 ? a.dhloc[si * p.N + n] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kCarryBatch; j++) {
+        const int s = s0 - j;
+        if (s < 0) break;
+        a.segend[(((long)b * a.S + s) * p.HP + ch) * p.N + n] = c;
+        if (s > 0) c = fmaf(dk[j], c, lv[j]);
+      }
     }
   }
 }

@@ -458,10 +458,25 @@ __global__ void scan_fwd_tma_carry_kernel(const __grid_constant__ FwdTmaArgs a) 
     const float A2 = (p.a_per_state ? __ldg(p.A + (long)h * p.N + n) : __ldg(p.A + h)) * kLog2e;
     const float* row = start_row(p, b);
     float hv = row ? __ldg(row + (long)ch * p.N + n) : 0.0f;
-    for (int s = 0; s < a.S; s++) {
-      const long si = ((long)b * a.S + s) * p.HP + ch;
-      a.segstart[si * p.N + n] = hv;
-      if (s + 1 < a.S) hv = fmaf(ex2(A2 * a.sumdelta[si]), hv, a.hloc[si * p.N + n]);
+    // segments 0 .. S-1, 8 at a time: their decays and local aggregates do not depend on hv,
+    // so their loads go out together ahead of the composition
+    constexpr int kBatch = 8;
+    for (int s0 = 0; s0 < a.S; s0 += kBatch) {
+      float dk[kBatch], lv[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; j++) {
+        const int s = s0 + j;
+        const long si = ((long)b * a.S + s) * p.HP + ch;
+        dk[j] = s + 1 < a.S ? ex2(A2 * a.sumdelta[si]) : 0.0f;
+        lv[j] = s + 1 < a.S ? a.hloc[si * p.N + n] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; j++) {
+        const int s = s0 + j;
+        if (s >= a.S) break;
+        a.segstart[(((long)b * a.S + s) * p.HP + ch) * p.N + n] = hv;
+        if (s + 1 < a.S) hv = fmaf(dk[j], hv, lv[j]);
+      }
     }
   }
 }
