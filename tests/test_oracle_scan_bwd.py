@@ -151,6 +151,33 @@ def test_backward_matches_torch_autograd(case):
         np.testing.assert_allclose(o["d_dt_bias"], dt_bias.grad.numpy(), rtol=1e-10, atol=1e-11)
 
 
+def test_softplus_threshold_matches_torch_autograd():
+    """softplus is the identity above 20 (and its derivative 1 there), sigmoid-sloped below: dt
+    biases near 20 put the pre-activations of two heads on both sides of the threshold, and the
+    oracle's gradients equal torch's autograd of its own thresholded softplus (same convention)."""
+    ns, L, H, P, N = 2, 9, 3, 1, 3
+    d = random_scan_inputs(ns, L, H, P, N, seed=47, dt_raw=True)
+    bias = torch.tensor([20.2, -0.3, 19.6], dtype=torch.float64)
+    pre = d["dt"].double() + bias
+    assert bool((pre > 20).any()) and bool((pre[..., [0, 2]] <= 20).any())
+    t = {k: (v.double().clone().requires_grad_(True) if torch.is_tensor(v) else v)
+         for k, v in d.items()}
+    dt_bias = bias.clone().requires_grad_(True)
+    y, st = _torch_scan(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["z"], t["s0"],
+                        dt_bias, True, True, 1)
+    ((y * t["dy"]).sum() + (st * t["d_state_out"]).sum()).backward()
+    dims = ScanDims(ns, L, H, P, N, chunk=4, dt_softplus=1)
+    yo, so, _ = oracle.scan_fwd(dims, x=d["x"], dt=d["dt"], A=d["A"], B=d["B"], C=d["C"],
+                                D=d["D"], z=d["z"], s0=d["s0"], dt_bias=bias.numpy())
+    np.testing.assert_allclose(yo, y.detach().numpy(), rtol=1e-12, atol=1e-13)
+    o = oracle.scan_bwd(dims, x=d["x"], dt=d["dt"], A=d["A"], B=d["B"], C=d["C"], D=d["D"],
+                        z=d["z"], s0=d["s0"], dy=d["dy"], d_state_out=d["d_state_out"],
+                        dt_bias=bias.numpy())
+    np.testing.assert_allclose(o["d_dt"], t["dt"].grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(o["d_dt_bias"], dt_bias.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(o["d_x"], t["x"].grad.numpy(), rtol=1e-10, atol=1e-11)
+
+
 def test_zero_upstream_gives_zero_gradients():
     d = random_scan_inputs(2, 10, 3, 2, 4, seed=5)
     dims = ScanDims(2, 10, 3, 2, 4, chunk=3)
