@@ -76,12 +76,12 @@ decode_step_kernel(const ScanProblem p, int K, int silu, int tpc, const IO* __re
     const IO* Br = reinterpret_cast<const IO*>(p.B) + ((long)b * p.G + g) * N;
     const IO* Cr = reinterpret_cast<const IO*>(p.C) + ((long)b * p.G + g) * N;
     float* sp = state + ((long)row * p.HP + ch) * N;
-    const float as = SCALAR_A ? decay_coef<ACC>(dl, __ldg(p.A + h) * kLog2e) : 0.0f;
+    const DecayCoef as = SCALAR_A ? decay_coef<ACC>(dl, __ldg(p.A + h) * kLog2e) : DecayCoef{0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < NS; j++) {
       const int n = sg * NS + j;
       if (n < N) {
-        const float a = SCALAR_A ? as : decay_coef<ACC>(dl, __ldg(p.A + (long)h * N + n) * kLog2e);
+        const DecayCoef a = SCALAR_A ? as : decay_coef<ACC>(dl, __ldg(p.A + (long)h * N + n) * kLog2e);
         const float hv = decay_step<ACC>(a, sp[n], dx * ld(Br + n));
         sp[n] = hv;
         acc = fmaf(ld(Cr + n), hv, acc);

@@ -102,17 +102,18 @@ scan_bwd_kernel(const BwdArgs a) {
         float Bv[kBwdNS];
         load_row<IO, kBwdNS, FULL>(Bm + tok * p.G * N + gbase, N - l.n0, Bv);
         const float dx = dl * xv;
-        const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
+        const DecayCoef as = SCALAR_A ? decay_coef<ACC, true>(dl, A2[0]) : DecayCoef{0.0f, 0.0f};
 #pragma unroll
         for (int j = 0; j < kBwdNS; j++)
-          hs[j] = decay_step<ACC>(SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]), hs[j], dx * Bv[j]);
+          hs[j] = decay_step<ACC>(SCALAR_A ? as : decay_coef<ACC, true>(dl, A2[j]), hs[j], dx * Bv[j]);
       }
     }
     // ---- level 2: per sub-chunk, last to first --------------------------------------------
     for (int k = nsub - 1; k >= 0; k--) {
       const int ts = t0 + k * kTsub;
       const int cnt = min(kTsub, t1 - ts);
-      float hh[kTsub + 1][kBwdNS], aa[kTsub][kBwdNS], dls[kTsub], xs[kTsub], pres[kTsub];
+      float hh[kTsub + 1][kBwdNS], dls[kTsub], xs[kTsub], pres[kTsub];
+      DecayCoef aa[kTsub][kBwdNS];
       {
         const float4 v = bnd[k * kScanThreads + threadIdx.x];
         hh[0][0] = v.x; hh[0][1] = v.y; hh[0][2] = v.z; hh[0][3] = v.w;
@@ -127,16 +128,19 @@ scan_bwd_kernel(const BwdArgs a) {
           float Bv[kBwdNS];
           load_row<IO, kBwdNS, FULL>(Bm + tok * p.G * N + gbase, N - l.n0, Bv);
           const float dx = dl * xv;
-          const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
+          const DecayCoef as = SCALAR_A ? decay_coef<ACC, true>(dl, A2[0]) : DecayCoef{0.0f, 0.0f};
 #pragma unroll
           for (int j = 0; j < kBwdNS; j++) {
-            aa[i][j] = SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]);
+            aa[i][j] = SCALAR_A ? as : decay_coef<ACC, true>(dl, A2[j]);
             hh[i + 1][j] = decay_step<ACC>(aa[i][j], hh[i][j], dx * Bv[j]);
           }
           dls[i] = dl; xs[i] = xv; pres[i] = pre;
         } else {
 #pragma unroll
-          for (int j = 0; j < kBwdNS; j++) { aa[i][j] = ACC ? 0.0f : 1.0f; hh[i + 1][j] = hh[i][j]; }
+          for (int j = 0; j < kBwdNS; j++) {  // the identity step, a = 1
+            aa[i][j] = ACC ? DecayCoef{0.0f, 1.0f} : DecayCoef{1.0f, 0.0f};
+            hh[i + 1][j] = hh[i][j];
+          }
           dls[i] = 0.0f; xs[i] = 0.0f; pres[i] = 0.0f;
         }
       }
@@ -273,10 +277,10 @@ scan_bwd_local_kernel(const BwdArgs a) {
     load_row<IO, kBwdNS, FULL>(Cm + tok * p.G * N + gbase, N - l.n0, Cv);
     float gy = l.valid ? ld(dy + tok * p.HP + l.ch) : 0.0f;
     if (z) gy *= siluf_(l.valid ? ld(z + tok * p.HP + l.ch) : 0.0f);
-    const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
+    const DecayCoef as = SCALAR_A ? decay_coef<ACC, true>(dl, A2[0]) : DecayCoef{0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < kBwdNS; j++)
-      c[j] = decay_apply<ACC>(SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]), fmaf(gy, Cv[j], c[j]));
+      c[j] = decay_apply<ACC>(SCALAR_A ? as : decay_coef<ACC, true>(dl, A2[j]), fmaf(gy, Cv[j], c[j]));
     sumd += dl;
   }
   if (l.valid) {

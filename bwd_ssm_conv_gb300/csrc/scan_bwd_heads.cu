@@ -50,7 +50,7 @@ struct BhArgs {
 struct BhSmem {
   float x[kBhTile][kBhP], gy[kBhTile][kBhP], dlx[kBhTile][kBhP], dyg[kBhTile][kBhP];
   float B[kBhTile][kBhN], C[kBhTile][kBhN];
-  float tc[kBhTile][4];                   // (decay coefficient, delta, softplus', -)
+  float tc[kBhTile][4];                   // (decay c, delta, softplus', decay s)
   float q[kBhTile][kBhP][2];              // per channel: sum_n dh B, sum_n C h
   float w[kBhTile][kBhWarps];             // per warp: sum of w over its states
   float red[kBhGrp][kBhWarps][2 * kBhN];  // per warp: dB (0..127), dC (128..255)
@@ -94,7 +94,9 @@ __device__ void bh_load_tile(const BhArgs& A, BhSmem& S, long tok0, int cnt, int
         dl = raw;
       }
     }
-    S.tc[tid][0] = decay_coef<ACC>(dl, A2);
+    const DecayCoef k = decay_coef<ACC, true>(dl, A2);
+    S.tc[tid][0] = k.c;
+    S.tc[tid][3] = k.s;
     S.tc[tid][1] = dl;
     S.tc[tid][2] = spg;
   }
@@ -328,7 +330,7 @@ scan_bwd_heads_kernel(const BhArgs A) {
       bh_load_tile<IO, ACC>(A, S, (long)b * p.L + t0, cnt, ch0, h, g, A2, bias, false);
       for (int i = 0; i < cnt; i++) {
         if (i % kBhSub == 0) bh_store(bnd_slot(2 * j + i / kBhSub), hv);
-        const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
+        const DecayCoef2 cf2 = decay_pair(DecayCoef{S.tc[i][0], S.tc[i][3]});
         const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
         const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
         const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
@@ -353,7 +355,7 @@ scan_bwd_heads_kernel(const BhArgs A) {
         const int i_lo = hf * kBhSub, i_hi = min(cnt, i_lo + kBhSub);
         bh_load(bnd_slot(2 * j + hf), hv);
         for (int i = i_lo; i < i_hi; i++) {
-          const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
+          const DecayCoef2 cf2 = decay_pair(DecayCoef{S.tc[i][0], S.tc[i][3]});
           const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
           const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);
           const f2_t B2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
@@ -374,7 +376,7 @@ scan_bwd_heads_kernel(const BhArgs A) {
           f2_t hp[kBhTP][kBhTN / 2];  // h_{t-1}
           if (i > i_lo) bh_tm_load(tm + 32u * (uint32_t)(i - 1 - i_lo), hp);
           else bh_load(bnd_slot(2 * j + hf), hp);
-          const f2_t cf2 = f2_pack(S.tc[i][0], S.tc[i][0]);
+          const DecayCoef2 cf2 = decay_pair(DecayCoef{S.tc[i][0], S.tc[i][3]});
           const float dl = S.tc[i][1];
           const float4 b0 = *reinterpret_cast<const float4*>(&S.B[i][n0]);
           const float4 b1 = *reinterpret_cast<const float4*>(&S.B[i][n0 + 4]);

@@ -570,8 +570,8 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
         f2_t B2[2];
         ld_b(i, B2);
-        hp[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hp[0], f2_mul(dx2, B2[0]));
-        hp[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hp[1], f2_mul(dx2, B2[1]));
+        hp[0] = step2<ACC>(decay2<ACC, true>(dl2, A2p[0]), hp[0], f2_mul(dx2, B2[0]));
+        hp[1] = step2<ACC>(decay2<ACC, true>(dl2, A2p[1]), hp[1], f2_mul(dx2, B2[1]));
       };
       if (cnt == TT) {  // full tile: no per-token branch, so tokens can interleave
 #pragma unroll
@@ -611,7 +611,7 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
           dC2[q] = f2_mul(gy2, hcur[q]);
           sB2 = f2_fma(dh2, B2[q], sB2);
           dB2[q] = f2_mul(dh2, dlx2);
-          const f2_t cn2 = apply2<ACC>(decay2<ACC>(dl2, A2p[q]), dh2);
+          const f2_t cn2 = apply2<ACC>(decay2<ACC, true>(dl2, A2p[q]), dh2);
           const f2_t w2 = f2_mul(cn2, hprev[q]);
           sAw2 = f2_fma(Anp[q], w2, sAw2);
           dA2[q] = f2_fma(dl2, w2, dA2[q]);
@@ -655,8 +655,8 @@ scan_bwd_tma_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
             const f2_t dl2 = f2_pack(d2.x, d2.x), dx2 = f2_pack(d2.y, d2.y);
             f2_t B2[2];
             ld_b(i, B2);
-            hcur[0] = step2<ACC>(decay2<ACC>(dl2, A2p[0]), hcur[0], f2_mul(dx2, B2[0]));
-            hcur[1] = step2<ACC>(decay2<ACC>(dl2, A2p[1]), hcur[1], f2_mul(dx2, B2[1]));
+            hcur[0] = step2<ACC>(decay2<ACC, true>(dl2, A2p[0]), hcur[0], f2_mul(dx2, B2[0]));
+            hcur[1] = step2<ACC>(decay2<ACC, true>(dl2, A2p[1]), hcur[1], f2_mul(dx2, B2[1]));
           }
         }
         tmem_st16(tm + kTmHist + 16 * g, rec);
@@ -871,8 +871,8 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
         const float2 p4 = sP[r * CB + cl];
         const f2_t dl2 = f2_pack(p4.x, p4.x), gy2 = f2_pack(p4.y, p4.y);
         const float4 cv = *reinterpret_cast<const float4*>(sCf + r * N + n0);
-        c2[0] = apply2<ACC>(decay2<ACC>(dl2, A2p[0]), f2_fma(gy2, f2_pack(cv.x, cv.y), c2[0]));
-        c2[1] = apply2<ACC>(decay2<ACC>(dl2, A2p[1]), f2_fma(gy2, f2_pack(cv.z, cv.w), c2[1]));
+        c2[0] = apply2<ACC>(decay2<ACC, true>(dl2, A2p[0]), f2_fma(gy2, f2_pack(cv.x, cv.y), c2[0]));
+        c2[1] = apply2<ACC>(decay2<ACC, true>(dl2, A2p[1]), f2_fma(gy2, f2_pack(cv.z, cv.w), c2[1]));
         sumd += p4.x;
       }
     }

@@ -32,48 +32,64 @@ __host__ inline void state_split(int N, int pref_ns, int* ns, int* tpc) {
 
 // ---- the per-step decay ---------------------------------------------------------------
 // Fast form (bf16 I/O): a = 2^(delta A log2 e) by the SFU, h <- a h + u.
-// Accurate form (fp32 I/O): e = exp(delta A) - 1 and h <- h + (e h + u).  When delta |A| is
-// small, a sits just below 1 and fp32 cannot hold 1 - a to better than ~6e-8 / (delta |A|);
-// the SFU result is also biased there (about -0.3 ulp), and both errors compound over the
-// ~1 / (delta |A|) tokens a state remembers.  Carrying e instead keeps each step's error at
-// one fp32 rounding of h.  e comes from the Taylor series x + x^2/2 + x^3/6 + x^4/24
-// (remainder below 1.3e-7 relative for |x| < 1/16) and from 2^(x log2 e) - 1 above that.
-template <bool ACC>
-__device__ __forceinline__ float decay_coef(float dl, float A2) {
+// Accurate form (fp32 I/O): when delta |A| is small, a sits just below 1 and fp32 cannot hold
+// 1 - a to better than ~6e-8 / (delta |A|); the SFU result is also biased there (about -0.3
+// ulp), and both errors compound over the ~1 / (delta |A|) tokens a state remembers.  The step
+// therefore carries e = exp(delta A) - 1 and updates h <- h + (e h + u), which keeps each
+// step's error at one fp32 rounding of h.  e comes from the Taylor series x + x^2/2 + x^3/6 +
+// x^4/24 (remainder below 1.3e-7 relative for |x| < 1/16) and from 2^(x log2 e) - 1 above that.
+// SMALL (the backward kernels): for a small decay 1 + e keeps only ~6e-8 / a of it (a gradient
+// through a decay of 1e-5 would be 1 % off), so above |delta A| = 1/16, where 1 - a > 0.06 and
+// a itself is as good, the step carries a from the SFU and updates h <- a h + u.  (The forward
+// keeps e up to the SFU range: its outputs need no relative precision of small decays, and its
+// 1e-4 fp32 gate has little room for a change of rounding.)
+// Either way the coefficient is (c, s) with a = c + s: (a, 0) for the fast form and for the
+// larger SMALL steps, (e, 1) otherwise.  s is 0 or 1, so s h and s v are exact; without SMALL
+// it is the constant 1 of the accurate form.
+struct DecayCoef { float c, s; };
+template <bool ACC, bool SMALL = false>
+__device__ __forceinline__ DecayCoef decay_coef(float dl, float A2) {
   const float x2 = dl * A2;  // delta A log2(e)
-  if (!ACC) return ex2(x2);
+  const float a = ex2(x2);
+  if (!ACC) return DecayCoef{a, 0.0f};
   const float x = x2 * 0.6931471805599453f;  // delta A
   const float p = x * fmaf(x, fmaf(x, fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-  const float q = ex2(x2) - 1.0f;
-  return fabsf(x) < 0.0625f ? p : q;
+  const bool near1 = fabsf(x) < 0.0625f;
+  if (!SMALL) return DecayCoef{near1 ? p : a - 1.0f, 1.0f};
+  return DecayCoef{near1 ? p : a, near1 ? 1.0f : 0.0f};  // selects: neighbouring states differ
 }
-// h <- a h + u   (fast)   or   h <- h + (e h + u)   (accurate)
+// h <- a h + u   (fast)   or   h <- (c h + u) + s h   (accurate; (e h + u) + h near a = 1)
 template <bool ACC>
-__device__ __forceinline__ float decay_step(float coef, float h, float u) {
-  return ACC ? h + fmaf(coef, h, u) : fmaf(coef, h, u);
+__device__ __forceinline__ float decay_step(DecayCoef k, float h, float u) {
+  return ACC ? fmaf(k.s, h, fmaf(k.c, h, u)) : fmaf(k.c, h, u);
 }
-// a * v   (fast)   or   v + e v   (accurate)
+// a * v   (fast)   or   c v + s v   (accurate; v + e v near a = 1)
 template <bool ACC>
-__device__ __forceinline__ float decay_apply(float coef, float v) {
-  return ACC ? fmaf(coef, v, v) : coef * v;
+__device__ __forceinline__ float decay_apply(DecayCoef k, float v) {
+  return ACC ? fmaf(k.c, v, k.s * v) : k.c * v;
 }
 
-// Packed versions for a pair of states (f32x2): the coefficient and its two uses.
-template <bool ACC>
-__device__ __forceinline__ f2_t decay2(f2_t dl2, f2_t A2p) {
-  if constexpr (!ACC) return f2_ex2(f2_mul(dl2, A2p));
+// Packed versions for a pair of states (f32x2): the coefficients and their two uses.
+struct DecayCoef2 { f2_t c, s; };
+__device__ __forceinline__ DecayCoef2 decay_pair(DecayCoef k) {
+  return DecayCoef2{f2_pack(k.c, k.c), f2_pack(k.s, k.s)};
+}
+template <bool ACC, bool SMALL = false>
+__device__ __forceinline__ DecayCoef2 decay2(f2_t dl2, f2_t A2p) {
+  if constexpr (!ACC) return DecayCoef2{f2_ex2(f2_mul(dl2, A2p)), 0ull};
   float dl, d2, a0, a1;
   f2_unpack(dl2, dl, d2);
   f2_unpack(A2p, a0, a1);
-  return f2_pack(decay_coef<true>(dl, a0), decay_coef<true>(dl, a1));
+  const DecayCoef k0 = decay_coef<true, SMALL>(dl, a0), k1 = decay_coef<true, SMALL>(dl, a1);
+  return DecayCoef2{f2_pack(k0.c, k1.c), f2_pack(k0.s, k1.s)};
 }
 template <bool ACC>
-__device__ __forceinline__ f2_t step2(f2_t coef, f2_t h, f2_t u) {
-  return ACC ? f2_add(h, f2_fma(coef, h, u)) : f2_fma(coef, h, u);
+__device__ __forceinline__ f2_t step2(const DecayCoef2& k, f2_t h, f2_t u) {
+  return ACC ? f2_fma(k.s, h, f2_fma(k.c, h, u)) : f2_fma(k.c, h, u);
 }
 template <bool ACC>
-__device__ __forceinline__ f2_t apply2(f2_t coef, f2_t v) {
-  return ACC ? f2_fma(coef, v, v) : f2_mul(coef, v);
+__device__ __forceinline__ f2_t apply2(const DecayCoef2& k, f2_t v) {
+  return ACC ? f2_fma(k.c, v, f2_mul(k.s, v)) : f2_mul(k.c, v);
 }
 __device__ __forceinline__ float f2_sum(f2_t v) {
   float lo, hi;

@@ -99,10 +99,10 @@ scan_fwd_kernel(const FwdArgs a) {
     load_row<IO, NS, FULL>(Bm + (tok * p.G + g) * N + n0, N - n0, Bv);
     if (!LOCAL) load_row<IO, NS, FULL>(Cm + (tok * p.G + g) * N + n0, N - n0, Cv);
     float acc = 0.0f;
-    const float as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : 0.0f;
+    const DecayCoef as = SCALAR_A ? decay_coef<ACC>(dl, A2[0]) : DecayCoef{0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < NS; j++) {
-      const float av = SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]);
+      const DecayCoef av = SCALAR_A ? as : decay_coef<ACC>(dl, A2[j]);
       hs[j] = decay_step<ACC>(av, hs[j], dx * Bv[j]);
       if (!LOCAL) acc = fmaf(Cv[j], hs[j], acc);
     }

@@ -134,7 +134,7 @@ scan_fwd_heads_kernel(const __grid_constant__ MhArgs a) {
     if (tid < TT) {
       float dl = mh_lds(sdt + tid * a.dt_box + (h - h_lo));
       if (p.softplus) dl = softplusf_(dl + bias);
-      sT[tid] = make_float2(decay_coef<ACC>(dl, A2), dl);
+      sT[tid] = make_float2(decay_coef<ACC>(dl, A2).c, dl);  // s is the form's constant
     }
     __syncthreads();
     for (int idx = tid; idx < TT * kMhP; idx += kMhThreads)
@@ -175,7 +175,7 @@ scan_fwd_heads_kernel(const __grid_constant__ MhArgs a) {
     // ---- the recurrence: rank-1 update of the thread's 4 x 8 tile, then C . h ---------------
     auto token = [&](int i) {
       const float2 tc = sT[i];
-      const f2_t cf2 = f2_pack(tc.x, tc.x);
+      const DecayCoef2 cf2 = decay_pair(DecayCoef{tc.x, ACC ? 1.0f : 0.0f});
       const float4 dxv = *reinterpret_cast<const float4*>(sDX + i * kMhP + pl0);
       const float dxs[kMhTP] = {dxv.x, dxv.y, dxv.z, dxv.w};
       f2_t B2[kMhTN / 2], C2[kMhTN / 2];

@@ -330,11 +330,11 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
     }
     // the decay coefficients of one token (one per state pair, or one for all states)
-    auto decays = [&](float dl, f2_t (&cf)[NS / 2]) {
+    auto decays = [&](float dl, DecayCoef2 (&cf)[NS / 2]) {
       if constexpr (SCALAR_A) {
-        const float c = decay_coef<ACC>(dl, A2s);
+        const DecayCoef2 c = decay_pair(decay_coef<ACC>(dl, A2s));
 #pragma unroll
-        for (int q = 0; q < NS / 2; q++) cf[q] = f2_pack(c, c);
+        for (int q = 0; q < NS / 2; q++) cf[q] = c;
       } else {
         const f2_t dl2 = f2_pack(dl, dl);
 #pragma unroll
@@ -342,7 +342,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
     };
     // one token: advance the states with its decays; returns this thread's part of C . h
-    auto token = [&](int i, float2 dd, const f2_t (&cf)[NS / 2]) -> float {
+    auto token = [&](int i, float2 dd, const DecayCoef2 (&cf)[NS / 2]) -> float {
       const f2_t dx2 = f2_pack(dd.y, dd.y);
       f2_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
@@ -377,7 +377,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       float acc[TPC];
       if constexpr (BATCH) {
         float2 dd[TPC];
-        f2_t cf[TPC][NS / 2];
+        DecayCoef2 cf[TPC][NS / 2];
 #pragma unroll
         for (int u = 0; u < TPC; u++) {
           dd[u] = sDD[(i0 + u) * cb + cl];
@@ -392,7 +392,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
           acc[u] = 0.0f;
           if (FULL || i0 + u < cnt) {
             const float2 dd = sDD[(i0 + u) * cb + cl];
-            f2_t cf[NS / 2];
+            DecayCoef2 cf[NS / 2];
             decays(dd.x, cf);
             acc[u] = token(i0 + u, dd, cf);
           }

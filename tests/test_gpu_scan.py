@@ -100,6 +100,30 @@ def test_scan_backward_parity(case):
     assert binding.ssm_scan_status(g["_ws"]) == 0
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_softplus_threshold_parity(io):
+    """dt biases near 20 put the softplus pre-activations of some channels on both sides of the
+    threshold (identity and derivative 1 above it); forward and gradients match the oracle."""
+    shape = (2, 96, 64, 1, 16, 1)
+    inp = _inputs(shape, io, False, True, seed=97)
+    H = shape[2]
+    inp["dt_bias"] = torch.tensor([(20.2, 19.8, 0.1, 20.6)[c % 4] for c in range(H)]).float()
+    pre = inp["dt"].float() + inp["dt_bias"]
+    assert bool((pre > 20).any()) and bool(((pre <= 20) & (inp["dt_bias"] > 19)).any())
+    y, st, ck = gpu_fwd(inp, 32, True)
+    yo, so, co = oracle_fwd(inp, 32, True)
+    t = tol(io, grad=False)
+    assert_close("y", y, yo, t)
+    assert_close("state_out", st, so, t)
+    g = gpu_bwd(inp, 32, ckpt=ck, softplus=True)
+    o = oracle_bwd(inp, 32, True)
+    t = tol(io, grad=True)
+    for k in GRADS:
+        if o.get(k) is not None and g.get(k) is not None:
+            assert_close(k, g[k], o[k], t)
+    assert binding.ssm_scan_status(g["_ws"]) == 0
+
+
 # Enough (sequence, 32-channel block) chains to fill a 152-SM GPU without time segments (40 x 32
 # = 1280 chains, 4 resident blocks per SM): the backward then runs resident blocks over (chain,
 # chunk) units, last chunk first, each handing its chunk's start adjoint to the unit of the
