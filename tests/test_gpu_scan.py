@@ -100,12 +100,20 @@ def test_scan_backward_parity(case):
     assert binding.ssm_scan_status(g["_ws"]) == 0
 
 
+THRESHOLD_SHAPES = [  # (ns, L, H, P, N, G), one A per head
+    ((2, 96, 64, 1, 16, 1), False),     # Mamba-1 layout: the TMA kernels
+    ((1, 80, 4, 64, 128, 1), True),     # Mamba-2 form: the head-tiled kernels
+]
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_softplus_threshold_parity(io):
+@pytest.mark.parametrize("shape_sa", THRESHOLD_SHAPES, ids=["mamba1", "mamba2"])
+def test_softplus_threshold_parity(io, shape_sa):
     """dt biases near 20 put the softplus pre-activations of some channels on both sides of the
-    threshold (identity and derivative 1 above it); forward and gradients match the oracle."""
-    shape = (2, 96, 64, 1, 16, 1)
-    inp = _inputs(shape, io, False, True, seed=97)
+    threshold (identity and derivative 1 above it) and make their decays tiny; forward and
+    gradients match the oracle."""
+    shape, scalar_a = shape_sa
+    inp = _inputs(shape, io, scalar_a, True, seed=97)
     H = shape[2]
     inp["dt_bias"] = torch.tensor([(20.2, 19.8, 0.1, 20.6)[c % 4] for c in range(H)]).float()
     pre = inp["dt"].float() + inp["dt_bias"]
