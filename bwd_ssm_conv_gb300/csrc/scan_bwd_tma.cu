@@ -45,6 +45,9 @@ struct BwdTma {
   uint32_t off_x, off_dt, off_z, off_dy, off_b, off_c, stage_stride;
   uint32_t off_p, off_spg, off_e, off_bf, off_cf, off_part, off_red, off_out, out_tile, out_stride;
   uint32_t off_par, off_acc, off_bar, smem;
+  // the local-adjoint kernel's own, smaller layout: the same tile stages, then its (delta, gy)
+  // records, C as fp32 rows, dt_bias and the barriers
+  uint32_t loc_off_p, loc_off_cf, loc_off_par, loc_off_bar, loc_smem;
   // persistent mode: queue counter, per-unit ready flags, units, chains, chain stride; the
   // dB/dC reduction items that share the queue: per-(sequence, group, chunk) counts of finished
   // units, items per chunk, 32-token slices per chunk, and the queue's length (units + items)
@@ -805,9 +808,9 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
   const int tid = threadIdx.x;
   const int cl = l.cl, ch = l.ch, ch0 = ch - cl, n0 = l.n0;
   const int s = blockIdx.y + 1, b = blockIdx.z;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.off_bar);
-  float2* sP = reinterpret_cast<float2*>(smem + m.off_e);  // [TT][CB] (delta, gy)
-  float* sPar = reinterpret_cast<float*>(smem + m.off_par);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.loc_off_bar);
+  float2* sP = reinterpret_cast<float2*>(smem + m.loc_off_p);  // [TT][CB] (delta, gy)
+  float* sPar = reinterpret_cast<float*>(smem + m.loc_off_par);
   const int t_begin = s * a.seg_chunks * a.chunk_b;
   const int t_end = min(p.L, t_begin + a.seg_chunks * a.chunk_b);
   const int nt = (t_end - t_begin + TT - 1) / TT;
@@ -863,7 +866,7 @@ scan_bwd_tma_local_kernel(const __grid_constant__ BwdTma m, const BwdArgs a) {
       if (p.z) gy *= siluf_(lds_f(sz + idx));
       sP[idx] = make_float2(dl, gy);
     }
-    const float* sCf = tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.off_cf), TT * N);
+    const float* sCf = tile_rows_f32<IO>(base + m.off_c, reinterpret_cast<float*>(smem + m.loc_off_cf), TT * N);
     __syncthreads();
 #pragma unroll
     for (int r = TT - 1; r >= 0; r--) {
@@ -937,6 +940,12 @@ static bool setup_bwd_tma(const BwdArgs& a, const BwdPlan& q, char* w, BwdTma* m
   m->off_acc = take(kWarps * cb * 2 * 4);
   m->off_bar = take(64);
   m->smem = off;
+  off = kBwdStages * m->stage_stride;
+  m->loc_off_p = take(TT * cb * 8);
+  m->loc_off_cf = take(TT * p.N * 4);
+  m->loc_off_par = take(2 * cb * 4);
+  m->loc_off_bar = take(64);
+  m->loc_smem = off;
   m->bytes_l1 = 2 * tile + row;
   m->bytes_l2 = (3 + (p.z ? 1 : 0)) * tile + 2 * row;
   m->bytes_loc = (2 + (p.z ? 1 : 0)) * tile + row;
@@ -1029,14 +1038,14 @@ cudaError_t launch_bwd_tma_local(const BwdArgs& a, const BwdPlan& q, char* ws, c
   cudaError_t e;
   if (p.io == SSM_BF16) {
     auto k = scan_bwd_tma_local_kernel<__nv_bfloat16>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.loc_smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+    k<<<grid, kScanThreads, m.loc_smem, st>>>(m, a), count_launches(1);
   } else {
     auto k = scan_bwd_tma_local_kernel<float>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.smem);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m.loc_smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kScanThreads, m.smem, st>>>(m, a), count_launches(1);
+    k<<<grid, kScanThreads, m.loc_smem, st>>>(m, a), count_launches(1);
   }
   return cudaGetLastError();
 }
