@@ -117,9 +117,17 @@ __device__ __forceinline__ float group_reduce_scatter(float (&v)[TPC], int sg) {
 // Registers: without the conv the compiler's own choice is kept (a minimum of 0 blocks per SM
 // states none: 64 for the d_state 16 layout, where a minimum of one block would let it spend
 // 120 and the grid would no longer fit in one wave).  The fused conv's staging would take that
-// layout past 64; its bound keeps the 8 blocks per SM that time segments aim for.
+// layout past 64; its bound keeps the 8 blocks per SM that time segments aim for.  The 8 states
+// x 2 threads layout, which bf16 takes when it needs time segments, would spend 124 (4 blocks
+// per SM); a bound of 6 blocks (80 registers) measured 4 % faster on one 16384-token sequence
+// of d_inner 2048, a bound of 8 (64 registers) 2 % slower.
+template <int NS, int TPC, int CK>
+constexpr int fwd_min_blocks() {
+  return CK > 0 ? (int)kFwdTargetBlocksPerSM : (NS == 8 && TPC == 2 ? 6 : 0);
+}
+
 template <typename IO, int NS, int TPC, int THR, bool LOCAL, bool SCALAR_A, int CK>
-__global__ void __launch_bounds__(THR, CK > 0 ? kFwdTargetBlocksPerSM : 0)
+__global__ void __launch_bounds__(THR, fwd_min_blocks<NS, TPC, CK>())
 scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   constexpr bool ACC = sizeof(IO) == 4;  // accurate decay form for fp32 I/O
   constexpr int TT = kFwdTile;
