@@ -80,14 +80,14 @@ TARGET_WORKLOADS = ("mamba1_long_bf16_b1_l16384_d2048_n16", DEFAULT_WORKLOAD)
 TRAFFIC_CAPTURES = {
     "scan_bwd": {
         "kernel": "scan_bwd_tma_kernel<bf16, persistent>",
-        "bytes": 461096448 + 360978176,
+        "bytes": 461442560 + 361737728,
         "sources": {
             "bwd_ssm_conv_gb300/csrc/scan_bwd_tma.cu":
-                "3cf909cbe1c56a4e5bfa3bd1987296ec0ec513ac799fcd7a962aa3fc9339b6a0",
+                "50f08915816a813e680fc1512b7a4133b49d337a81fdf7ecb2442007c3afc24e",
             "bwd_ssm_conv_gb300/csrc/scan_bwd.cuh":
                 "1ba6a1c2e1acc8aa74133a18acf8163297c25c51b3485aade9655a20773ec648",
             "bwd_ssm_conv_gb300/csrc/scan_common.cuh":
-                "4a263de92c114f3b898a0bf7eb5949e3841f9132b66fa3ec99e15445b373861f",
+                "ec33325a539666d13bd9bd7e0e477eef67041e67e6335846b2a0d300e8def98a",
             "bwd_ssm_conv_gb300/csrc/tmem.cuh":
                 "a55a9f2b432aed93c2a879bdb73a942f1e4300594365b99509ffbe376fc332f5",
             "bwd_ssm_conv_gb300/csrc/tma.cuh":
