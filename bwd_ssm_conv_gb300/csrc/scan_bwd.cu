@@ -328,6 +328,87 @@ __global__ void scan_bwd_carry_kernel(const BwdArgs a) {
   }
 }
 
+// Local adjoint of segments 1..S-1 for the Mamba-2 form (one A per head, d_state 128, head_dim
+// a multiple of 32): the same reverse-time scan c <- a_t (c + gy_t C_t^T) from a zero adjoint at
+// the segment's end, and sum(delta), as scan_bwd_local_kernel (same operations in the same
+// order, so the same bits), on a head-tiled block: 32 channels x 128 states, each thread 4
+// channels x 4 states in packed pairs.  A tile's 16 C rows, gy values and decays are staged in
+// shared memory once and shared by the block, where the per-channel kernel read the group's C
+// row from global memory for every channel.
+constexpr int kHlThreads = 256, kHlTT = 16, kHlCB = 32, kHlN = 128;
+template <typename IO>
+__global__ void __launch_bounds__(kHlThreads) scan_bwd_heads_local_kernel(const BwdArgs a) {
+  constexpr bool ACC = sizeof(IO) == 4;
+  __shared__ __align__(16) float sC[kHlTT][kHlN];   // C rows of the tile's tokens
+  __shared__ __align__(16) float sG[kHlTT][kHlCB];  // gy = dy silu(z)
+  __shared__ float2 sK[kHlTT];                      // the decay coefficient (c, s)
+  __shared__ float sDl[kHlTT];                      // delta
+  const ScanProblem& p = a.p;
+  const int tid = threadIdx.x, cg = tid >> 5, sg = tid & 31;
+  const int ch0 = blockIdx.x * kHlCB, h = ch0 / p.P, g = h / (p.H / p.G);
+  const int s = blockIdx.y + 1, b = blockIdx.z;
+  const IO* dt = (const IO*)p.dt;
+  const IO* Cm = (const IO*)p.C;
+  const IO* z = (const IO*)p.z;
+  const IO* dy = (const IO*)a.g.dy;
+  const float A2 = __ldg(p.A + h) * kLog2e;
+  const float bias = (p.softplus && p.dt_bias) ? __ldg(p.dt_bias + h) : 0.0f;
+  const int t_begin = s * a.seg_chunks * a.chunk_b;
+  const int t_end = min(p.L, t_begin + a.seg_chunks * a.chunk_b);
+  f2_t c2[4][2];  // channels ch0 + 4 cg + i, states 4 sg + 2 q, +1
+#pragma unroll
+  for (int i = 0; i < 4; i++) c2[i][0] = c2[i][1] = 0ull;
+  float sumd = 0.0f;
+  for (int te = t_end; te > t_begin; te -= kHlTT) {
+    const int t0 = max(t_begin, te - kHlTT), cnt = te - t0;
+    __syncthreads();  // every thread is done with the previous tile
+    for (int idx = tid; idx < cnt * (kHlN / 4); idx += kHlThreads) {
+      const int i = idx / (kHlN / 4), n4 = (idx - i * (kHlN / 4)) * 4;
+      const IO* src = Cm + (((long)b * p.L + t0 + i) * p.G + g) * kHlN + n4;
+      *reinterpret_cast<float4*>(&sC[i][n4]) = make_float4(ld(src), ld(src + 1), ld(src + 2), ld(src + 3));
+    }
+    for (int idx = tid; idx < cnt * kHlCB; idx += kHlThreads) {
+      const int i = idx / kHlCB, c = idx - i * kHlCB;
+      const long e = ((long)b * p.L + t0 + i) * p.HP + ch0 + c;
+      float gy = ld(dy + e);
+      if (z) gy *= siluf_(ld(z + e));
+      sG[i][c] = gy;
+    }
+    if (tid < cnt) {
+      float pre;
+      const float dl = delta_of(p, dt, (long)b * p.L + t0 + tid, h, bias, &pre);
+      const DecayCoef k = decay_coef<ACC, true>(dl, A2);
+      sK[tid] = make_float2(k.c, k.s);
+      sDl[tid] = dl;
+    }
+    __syncthreads();
+    for (int i = cnt - 1; i >= 0; i--) {
+      const float4 cv = *reinterpret_cast<const float4*>(&sC[i][sg * 4]);
+      const float4 gv = *reinterpret_cast<const float4*>(&sG[i][cg * 4]);
+      const float2 kk = sK[i];
+      const DecayCoef2 k2 = decay_pair(DecayCoef{kk.x, kk.y});
+      const f2_t C2[2] = {f2_pack(cv.x, cv.y), f2_pack(cv.z, cv.w)};
+      const float gys[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int ci = 0; ci < 4; ci++) {
+        const f2_t gy2 = f2_pack(gys[ci], gys[ci]);
+#pragma unroll
+        for (int q = 0; q < 2; q++) c2[ci][q] = apply2<ACC>(k2, f2_fma(gy2, C2[q], c2[ci][q]));
+      }
+      sumd += sDl[i];
+    }
+  }
+#pragma unroll
+  for (int ci = 0; ci < 4; ci++) {
+    const long si = ((long)b * a.S + s) * p.HP + ch0 + cg * 4 + ci;
+    float v[4];
+    f2_unpack(c2[ci][0], v[0], v[1]);
+    f2_unpack(c2[ci][1], v[2], v[3]);
+    *reinterpret_cast<float4*>(a.dhloc + si * kHlN + sg * 4) = make_float4(v[0], v[1], v[2], v[3]);
+    if (sg == 0) a.sumd[si] = sumd;
+  }
+}
+
 // ---- fixed-order reductions --------------------------------------------------------------
 // dA, dD and d dt_bias: the sums of the per-(sequence, segment) partials.  A block = kParOut
 // outputs x kParSlices slices of each output's terms; slice sl adds terms sl, sl + kParSlices,
@@ -539,6 +620,11 @@ static cudaError_t launch_bwd_t(BwdArgs a, const BwdPlan& q, char* w, cudaStream
   const bool persist = q.persist && tma;
   if (a.S > 1 && !persist) {
     cudaError_t e = q.tma_tt ? launch_bwd_tma_local(a, q, w, st) : cudaErrorNotSupported;
+    if (e == cudaErrorNotSupported && q.heads && p.P % kHlCB == 0 && p.N == kHlN) {
+      scan_bwd_heads_local_kernel<IO><<<dim3(p.HP / kHlCB, a.S - 1, p.ns), kHlThreads, 0, st>>>(a),
+          count_launches(1);
+      e = cudaSuccess;
+    }
     if (e == cudaErrorNotSupported) {
       dim3 g1(p.G * a.bpg, a.S - 1, p.ns);
       scan_bwd_local_kernel<IO, SCALAR_A, FULL><<<g1, kScanThreads, 0, st>>>(a), count_launches(1);
