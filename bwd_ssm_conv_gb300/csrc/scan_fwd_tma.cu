@@ -6,7 +6,7 @@
 namespace ssm {
 
 #define SSM_EXTERN_F32(NS, TPC, SA, THR, CK) \
-  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, cudaStream_t);
+  extern template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, size_t, cudaStream_t);
 SSM_FWD_TMA_VARIANTS(SSM_EXTERN_F32)
 #undef SSM_EXTERN_F32
 
@@ -127,34 +127,53 @@ cudaError_t launch_scan_fwd_tma(const ScanProblem& p, void* y, float* state_out,
   // aligned, from a base the kernel aligns to 1024 bytes
   auto al = [](uint32_t v) { return (v + 127u) & ~127u; };
   auto alk = [](uint32_t v) { return (v + 1023u) & ~1023u; };
-  a.off_x = 0;
-  a.off_dt = al(tile);
-  a.off_z = alk(a.off_dt + al(tile));
-  a.off_b = a.off_z + (p.z ? al(tile) : 0);
-  a.off_c = a.off_b + al(row);
-  a.stage_stride = alk(a.off_c + al(row));
-  a.off_dd = kFwdStages * a.stage_stride;                       // float2 (delta, delta x)
+  FwdTmaArgs::Layout& M = a.lay[0];
+  M.off_x = 0;
+  M.off_dt = al(tile);
+  M.off_z = alk(M.off_dt + al(tile));
+  M.off_b = M.off_z + (p.z ? al(tile) : 0);
+  M.off_c = M.off_b + al(row);
+  M.stage_stride = alk(M.off_c + al(row));
+  M.off_dd = kFwdStages * M.stage_stride;                       // float2 (delta, delta x)
   // B and C of a tile as fp32 rows (bf16 I/O only; fp32 I/O reads the staged rows)
   const uint32_t frow = io == 2 ? al((uint32_t)(q.tt * p.N * 4)) : 0u;
-  a.off_bf = a.off_dd + al((uint32_t)(q.tt * q.cb * 8));
-  a.off_cf = a.off_bf + frow;
-  a.off_par = a.off_cf + frow;
+  M.off_bf = M.off_dd + al((uint32_t)(q.tt * q.cb * 8));
+  M.off_cf = M.off_bf + frow;
+  M.off_par = M.off_cf + frow;
   // D, dt_bias; with the fused conv also the conv bias and weights
-  a.off_y = alk(a.off_par + al((uint32_t)((2 + (ck ? 1 + ck : 0)) * q.cb * 4)));
-  a.y_stride = alk(tile);
-  a.off_sxs = a.off_y + 2 * a.y_stride;
+  const uint32_t par = al((uint32_t)((2 + (ck ? 1 + ck : 0)) * q.cb * 4));
+  M.off_y = alk(M.off_par + par);
+  M.y_stride = alk(tile);
+  M.off_sxs = M.off_y + 2 * M.y_stride;
   const uint32_t pitch = (uint32_t)((q.tt + ck - 1) | 1);
-  a.off_bar = a.off_sxs + (ck > 0 ? al((uint32_t)(q.cb * pitch * 4)) : 0u);
-  const size_t smem = a.off_bar + 64 + 1024;  // + the kernel's alignment of its base
+  const uint32_t sxs = ck > 0 ? al((uint32_t)(q.cb * pitch * 4)) : 0u;
+  M.off_bar = M.off_sxs + sxs;
+  const size_t smem = M.off_bar + 64 + 1024;  // + the kernel's alignment of its base
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
+  // the local pass reads no z or C and writes no y: stages of x, dt and B, then its records
+  // (about two thirds of the main layout, so more blocks fit on an SM)
+  FwdTmaArgs::Layout& Lo = a.lay[1];
+  Lo = M;
+  Lo.off_b = alk(Lo.off_dt + al(tile));
+  Lo.off_z = Lo.off_c = Lo.off_b;  // not read
+  Lo.stage_stride = alk(Lo.off_b + al(row));
+  Lo.off_dd = kFwdStages * Lo.stage_stride;
+  Lo.off_bf = Lo.off_dd + al((uint32_t)(q.tt * q.cb * 8));
+  Lo.off_cf = Lo.off_bf;           // not written
+  Lo.off_par = Lo.off_bf + frow;
+  Lo.off_y = Lo.off_par;           // not written
+  Lo.y_stride = 0;
+  Lo.off_sxs = alk(Lo.off_par + par);
+  Lo.off_bar = Lo.off_sxs + sxs;
+  const size_t smem_loc = Lo.off_bar + 64 + 1024;
   // the fused conv's x slot in a stage is written by the prepass, not copied
   a.bytes_local = (ck > 0 ? 1 : 2) * tile + row;
   a.bytes_main = ((ck > 0 ? 1 : 2) + (p.z ? 1 : 0)) * tile + 2 * row;
   const bool sa = !p.a_per_state;
 #define SSM_DISPATCH(NS, TPC, SA, THR, CK)                                              \
   if (q.ns_state == NS && q.tpc == TPC && sa == SA && q.thr == THR && ck == CK)         \
-    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA, THR, CK>(a, smem, st) \
-                   : launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(a, smem, st);
+    return io == 2 ? launch_fwd_tma_t<__nv_bfloat16, NS, TPC, SA, THR, CK>(a, smem, smem_loc, st) \
+                   : launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(a, smem, smem_loc, st);
   SSM_FWD_TMA_VARIANTS(SSM_DISPATCH)
 #undef SSM_DISPATCH
   return cudaErrorNotSupported;

@@ -50,9 +50,12 @@ struct FwdTmaArgs {
   float* sumdelta;
   int has_y;
   uint32_t bytes_main, bytes_local;        // expected transaction bytes per stage
-  uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride;  // inside a stage
-  uint32_t off_dd, off_bf, off_cf, off_par, off_y, y_stride, off_bar;
-  uint32_t off_sxs;  // fused conv: [cb][odd pitch] fp32 sx columns of a tile
+  // shared-memory layouts: [0] the main pass, [1] the local pass (no z, C, y: a smaller block)
+  struct Layout {
+    uint32_t off_x, off_dt, off_z, off_b, off_c, stage_stride;  // inside a stage
+    uint32_t off_dd, off_bf, off_cf, off_par, off_y, y_stride, off_bar;
+    uint32_t off_sxs;  // fused conv: [cb][odd pitch] fp32 sx columns of a tile
+  } lay[2];
 };
 
 // Columns of sx a tile of the fused conv reads (TT tokens and the K-1 before the first) and
@@ -150,11 +153,12 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   const int ntiles = (t_end - t_begin + TT - 1) / TT;
   const uint32_t bytes = LOCAL ? a.bytes_local : a.bytes_main;
   const bool want_y = !LOCAL && a.has_y;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
-  float2* sDD = reinterpret_cast<float2*>(smem + a.off_dd);  // [TT][cb] (delta, delta x)
-  float* sBf = reinterpret_cast<float*>(smem + a.off_bf);     // [TT][N] B as fp32 (bf16 I/O)
-  float* sCf = reinterpret_cast<float*>(smem + a.off_cf);     // [TT][N] C as fp32 (bf16 I/O)
-  float* sPar = reinterpret_cast<float*>(smem + a.off_par);  // [cb] D, [cb] dt_bias
+  const FwdTmaArgs::Layout& Y = a.lay[LOCAL ? 1 : 0];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Y.off_bar);
+  float2* sDD = reinterpret_cast<float2*>(smem + Y.off_dd);  // [TT][cb] (delta, delta x)
+  float* sBf = reinterpret_cast<float*>(smem + Y.off_bf);     // [TT][N] B as fp32 (bf16 I/O)
+  float* sCf = reinterpret_cast<float*>(smem + Y.off_cf);     // [TT][N] C as fp32 (bf16 I/O)
+  float* sPar = reinterpret_cast<float*>(smem + Y.off_par);  // [cb] D, [cb] dt_bias
 
   if (tid == 0) {
     for (int i = 0; i < kFwdStages; i++) mbar_init(&full[i], 1);
@@ -180,7 +184,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   const IO* sx_rowp = CK > 0 ? reinterpret_cast<const IO*>(p.sx) +
                                    ((long)b * p.HP + ch0 + sx_r) * sx_row + sx_q
                              : nullptr;
-  float* sxs = reinterpret_cast<float*>(smem + a.off_sxs);
+  float* sxs = reinterpret_cast<float*>(smem + Y.off_sxs);
   IO sxv[SXU];
   auto sx_load = [&](int t0) {
     const IO* q = sx_rowp + t0;
@@ -207,15 +211,15 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
   __syncthreads();
   auto issue = [&](int k) {  // tile k -> stage k % kFwdStages (thread 0 only)
     const int stg = k % kFwdStages;
-    unsigned char* base = smem + stg * a.stage_stride;
+    unsigned char* base = smem + stg * Y.stage_stride;
     const int t0 = t_begin + k * TT;
     mbar_expect_tx(&full[stg], bytes);
-    if constexpr (CK == 0) tma_load_3d(base + a.off_x, &a.mx, ch0, t0, b, &full[stg]);
-    tma_load_3d(base + a.off_dt, &a.mdt, ch0, t0, b, &full[stg]);
-    tma_load_3d(base + a.off_b, &a.mb, g * N, t0, b, &full[stg]);
+    if constexpr (CK == 0) tma_load_3d(base + Y.off_x, &a.mx, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + Y.off_dt, &a.mdt, ch0, t0, b, &full[stg]);
+    tma_load_3d(base + Y.off_b, &a.mb, g * N, t0, b, &full[stg]);
     if (!LOCAL) {
-      if (p.z) tma_load_3d(base + a.off_z, &a.mz, ch0, t0, b, &full[stg]);
-      tma_load_3d(base + a.off_c, &a.mc, g * N, t0, b, &full[stg]);
+      if (p.z) tma_load_3d(base + Y.off_z, &a.mz, ch0, t0, b, &full[stg]);
+      tma_load_3d(base + Y.off_c, &a.mc, g * N, t0, b, &full[stg]);
     }
   };
   if (tid == 0)
@@ -250,10 +254,10 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
     if constexpr (CK > 0)
       if (k + 1 < ntiles) sx_load(t_begin + (k + 1) * TT);  // lands while this tile runs
     const bool ok = mbar_wait(&full[stg], (uint32_t)(k / kFwdStages) & 1u);
-    unsigned char* base = smem + stg * a.stage_stride;
-    const IO* sx = reinterpret_cast<const IO*>(base + a.off_x);
-    const IO* sdt = reinterpret_cast<const IO*>(base + a.off_dt);
-    const IO* sz = reinterpret_cast<const IO*>(base + a.off_z);
+    unsigned char* base = smem + stg * Y.stage_stride;
+    const IO* sx = reinterpret_cast<const IO*>(base + Y.off_x);
+    const IO* sdt = reinterpret_cast<const IO*>(base + Y.off_dt);
+    const IO* sz = reinterpret_cast<const IO*>(base + Y.off_z);
     const int t0 = t_begin + k * TT;
     const int cnt = min(TT, t_end - t0);
 
@@ -295,8 +299,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
     }
     if constexpr (sizeof(IO) == 2) {
-      const uint2* rb = reinterpret_cast<const uint2*>(base + a.off_b);
-      const uint2* rc = reinterpret_cast<const uint2*>(base + a.off_c);
+      const uint2* rb = reinterpret_cast<const uint2*>(base + Y.off_b);
+      const uint2* rc = reinterpret_cast<const uint2*>(base + Y.off_c);
       for (int idx = tid; idx < TT * N / 4; idx += THR) {
         const uint2 vb = rb[idx];
         reinterpret_cast<float4*>(sBf)[idx] =
@@ -319,8 +323,8 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
       return;
     }
-    const float* Bf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_b) : sBf;
-    const float* Cf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + a.off_c) : sCf;
+    const float* Bf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + Y.off_b) : sBf;
+    const float* Cf = sizeof(IO) == 4 ? reinterpret_cast<const float*>(base + Y.off_c) : sCf;
     // the next tile's sx columns: the prepass above has read these (barrier), and the next
     // prepass reads them after the barrier that ends this tile
     if constexpr (CK > 0)
@@ -372,7 +376,7 @@ scan_fwd_tma_kernel(const __grid_constant__ FwdTmaArgs a) {
       }
       return f2_sum(f2_add(acc0, acc1));
     };
-    IO* sy = reinterpret_cast<IO*>(smem + a.off_y + (k & 1) * a.y_stride);
+    IO* sy = reinterpret_cast<IO*>(smem + Y.off_y + (k & 1) * Y.y_stride);
     // fp32 I/O with one A per state: the decays of a whole group (the long accurate expm1 form)
     // are computed before its state updates, which do not feed them, so their latency overlaps
     // the update chain (measured faster).  bf16 I/O makes them token by token: batched there,
@@ -490,16 +494,16 @@ __global__ void scan_fwd_tma_carry_kernel(const __grid_constant__ FwdTmaArgs a) 
 }
 
 template <typename IO, int NS, int TPC, bool SCALAR_A, int THR, int CK>
-cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, cudaStream_t st) {
+cudaError_t launch_fwd_tma_t(FwdTmaArgs& a, size_t smem, size_t smem_loc, cudaStream_t st) {
   auto km = scan_fwd_tma_kernel<IO, NS, TPC, THR, false, SCALAR_A, CK>;
   auto kl = scan_fwd_tma_kernel<IO, NS, TPC, THR, true, SCALAR_A, CK>;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_loc);
   if (e != cudaSuccess) return e;
   const int bx = a.p.HP / a.cb;
   if (a.S > 1) {
-    kl<<<dim3(bx, a.S - 1, a.p.ns), THR, smem, st>>>(a), count_launches(1);
+    kl<<<dim3(bx, a.S - 1, a.p.ns), THR, smem_loc, st>>>(a), count_launches(1);
     const long total = (long)a.p.ns * a.p.HP * a.p.N;
     scan_fwd_tma_carry_kernel<IO><<<(int)((total + 255) / 256), 256, 0, st>>>(a), count_launches(1);
   }

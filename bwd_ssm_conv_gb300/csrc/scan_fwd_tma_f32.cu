@@ -5,7 +5,7 @@
 namespace ssm {
 
 #define SSM_INSTANTIATE_F32(NS, TPC, SA, THR, CK) \
-  template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, cudaStream_t);
+  template cudaError_t launch_fwd_tma_t<float, NS, TPC, SA, THR, CK>(FwdTmaArgs&, size_t, size_t, cudaStream_t);
 SSM_FWD_TMA_VARIANTS(SSM_INSTANTIATE_F32)
 #undef SSM_INSTANTIATE_F32
 
