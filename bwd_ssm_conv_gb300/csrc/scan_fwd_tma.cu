@@ -46,15 +46,22 @@ static FwdTmaPlan plan_fwd_tma(const ScanProblem& p, int num_sms) {
   // segments) beat 4: d_inner 2048 x one 16384-token sequence 0.321 -> 0.310 ms.  Not for
   // fp32, whose batched accurate decays then cost more (d_inner 512 x 8 x 1024: 0.093 ->
   // 0.103 ms); with 16 states per thread both lose (0.376 ms on the former).
+  // a layout applies when it is instantiated and its channel block (128 threads / threads per
+  // channel) tiles a group's channels and the rows
+  auto fits = [&](int cand) {
+    if (cand > p.N || p.N % cand != 0 || !instantiated(cand, p.N / cand, sa, ck)) return false;
+    const int cb = kScanThreads / (p.N / cand);
+    return (p.H / p.G) % cb == 0 && p.HP % cb == 0 && cb * io >= 16;
+  };
   int ns = 0;
   bool fills = false;
   for (int cand = 16; cand >= 4; cand >>= 1) {
-    if (p.N % cand != 0 || !instantiated(cand, p.N / cand, sa, ck)) continue;
+    if (!fits(cand)) continue;
     ns = cand;
     const int cb = kScanThreads / (p.N / cand);
     if ((long)p.ns * ((p.HP + cb - 1) / cb) >= 4L * num_sms) { fills = true; break; }
   }
-  if (!fills && io == 2 && ns < 8 && p.N % 8 == 0 && instantiated(8, p.N / 8, sa, ck)) ns = 8;
+  if (!fills && io == 2 && ns < 8 && fits(8)) ns = 8;
   if (ns == 0) return q;
   q.ns_state = ns;
   q.tpc = p.N / ns;
