@@ -118,8 +118,8 @@ __device__ __forceinline__ float group_reduce_scatter(float (&v)[TPC], int sg) {
 // y = (C . h + D x) silu(z) into the output tile itself.
 //
 // Registers: without the conv the compiler's own choice is kept (a minimum of 0 blocks per SM
-// states none: 64 for the d_state 16 layout, where a minimum of one block would let it spend
-// 120 and the grid would no longer fit in one wave).  The fused conv's staging would take that
+// states none: under 64 for the d_state 16 layout, where a minimum of one block would let it
+// spend 120 and the grid would no longer fit in one wave).  The fused conv's staging would take that
 // layout past 64; its bound keeps the 8 blocks per SM that time segments aim for.  The 8 states
 // x 2 threads layout, which bf16 takes when it needs time segments, would spend 124 (4 blocks
 // per SM); a bound of 6 blocks (80 registers) measured 4 % faster on one 16384-token sequence
